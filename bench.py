@@ -1,0 +1,500 @@
+#!/usr/bin/env python3
+"""Benchmark of the MoE token-routing hot path on GB300.
+
+One step = moe_gate -> moe_dispatch_layout -> moe_dispatch -> moe_combine
+over one batch of synthetic, seeded input already resident in HBM (expert
+outputs are seeded inputs: the expert FFN is not part of this path).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   (the CPU oracle, as the reference arm)
+
+Prints ONE JSON line on rank 0.  Under torchrun (N > 1) every rank routes its
+own batch (data parallel, no collective on the data path: weak scaling); the
+timed region is bracketed by a barrier and a device synchronise and the
+slowest rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "route+dispatch+combine tokens/s and HBM GB/s (fraction of GB300 roofline)"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "v2_top2"  # batch 32 x seq 512, hidden 5120, 16 experts, top-2
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (barrier + max over ranks only)
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world, device=None) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region (nvidia-smi sampler)
+# ---------------------------------------------------------------------------
+CLOCK_FIELDS = ("pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, bus_id: str | None, period_ms: int = 100):
+        self.samples = []  # (host time, dict)
+        self.bus_id = (bus_id or "").lower()
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", str(period_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            bus = parts[0].lower()
+            if self.bus_id and not (bus.endswith(self.bus_id[-12:]) or self.bus_id.endswith(bus[-12:])):
+                continue
+            try:
+                d = dict(sm=float(parts[1]), sm_max=float(parts[2]),
+                         power=float(parts[3]) if parts[3] not in ("[N/A]", "N/A") else None,
+                         active=parts[4], hw_slowdown=parts[5], hw_thermal=parts[6],
+                         sw_thermal=parts[7], sw_power_cap=parts[8])
+            except ValueError:
+                continue
+            self.samples.append((time.time(), d))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [d for (t, d) in self.samples if t0 <= t <= t1]
+        note = "samples inside the timed region"
+        if not inside and self.samples:
+            # nearest samples when the timed region is shorter than the period
+            mid = 0.5 * (t0 + t1)
+            inside = [min(self.samples, key=lambda s: abs(s[0] - mid))[1]]
+            note = "nearest sample to the timed region"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        reasons = set()
+        for d in inside:
+            for key, name in (("hw_slowdown", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                              ("sw_thermal", "sw_thermal_slowdown"), ("sw_power_cap", "sw_power_cap")):
+                if d[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(d["sm"] for d in inside),
+                "sm_max_mhz": max(d["sm_max"] for d in inside),
+                "reasons": sorted(reasons), "samples": len(inside), "note": note}
+
+
+# ---------------------------------------------------------------------------
+# byte accounting of the roofline (algorithmic bytes, not measured traffic)
+# ---------------------------------------------------------------------------
+def kernel_bytes(w, R):
+    bt = 1 if w.fp8 else 2
+    x = w.T * w.H * 2
+    packed = R * w.H * bt + (R * 8 if w.fp8 else 0)
+    eo = R * w.H * 2
+    y = w.T * w.H * 2
+    shared = w.Ks * w.T * w.H * 2
+    return {
+        "gate": w.T * w.E * 4 + w.T * w.k * 8 + w.E * 4,
+        "layout": w.T * w.k * (4 + 4 + 1 + 4) + R * 4,
+        "dispatch": x + packed,
+        "combine": eo + y + shared + w.T * w.k * 8,
+        "roofline_step": x + R * w.H * bt + eo + y,  # x read, packed written, eo read, y written
+    }
+
+
+KERNEL_SOURCES = {"dispatch": "dispatch.cu", "combine": "combine.cu", "gate": "gate.cu",
+                  "layout": "layout.cu"}
+
+
+def source_digest(name: str) -> str:
+    csrc = os.path.join(ROOT, "combine_moe_gate_warp_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in (KERNEL_SOURCES[name], "common.cuh"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            table = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = table.get(workload, {}).get(kernel)
+    if not ent or ent.get("source_digest") != source_digest(kernel):
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline (bounded sample)
+# ---------------------------------------------------------------------------
+def oracle_sample_run(w, inputs_host, T_s):
+    """Time the oracle on the first T_s tokens of the workload: gate, layout,
+    dispatch of every kept row, combine of every token.  Returns seconds."""
+    import numpy as np
+
+    import oracle
+    logits = inputs_host["logits"][:T_s]
+    x_bits = inputs_host["x"][:T_s]
+    cap = 0
+    if w.capacity:
+        cap = (5 * T_s * w.k + 4 * w.E - 1) // (4 * w.E)
+    t0 = time.perf_counter()
+    idx, g64, counts, aux, ent = oracle.gate(logits, w.k, w.mode)
+    L = oracle.layout(idx, w.E, w.P, cap, gates_f32=g64.astype(np.float32))
+    rows = np.arange(L["R"], dtype=np.int64)
+    if w.fp8:
+        packed, scales = oracle.dispatch_fp8_rows(x_bits, w.k, L["src_pos"], rows)
+    else:
+        packed = oracle.dispatch_bf16_rows(x_bits, w.k, L["src_pos"], rows)
+    t1 = time.perf_counter()
+    eo = packed if w.identity_experts else inputs_host["eo"][:max(L["R"], 1)]
+    sh = None if inputs_host.get("shared") is None else np.ascontiguousarray(inputs_host["shared"][:, :T_s])
+    t2 = time.perf_counter()
+    oracle.combine_f32order(eo, L["gates"], L["dst_row"], np.arange(T_s), T_s, w.k, sh)
+    t3 = time.perf_counter()
+    return (t1 - t0) + (t3 - t2)
+
+
+HOST_EO_ROWS = 1 << 17  # cap on host copies of the seeded expert outputs
+
+
+def max_sample_tokens(w):
+    return w.T if w.identity_experts else min(w.T, HOST_EO_ROWS // w.k)
+
+
+def cpu_baseline(w, inputs_host, target_s):
+    """Scale the token sample so that one oracle pass takes about target_s
+    seconds (whole workload at most), then time it."""
+    T_max = max_sample_tokens(w)
+    T_s = min(T_max, 256)
+    dt = oracle_sample_run(w, inputs_host, T_s)
+    while dt < 0.25 * target_s and T_s < T_max:
+        T_s = min(T_max, max(T_s * 2, int(T_s * target_s / max(dt, 1e-6) * 0.8)))
+        dt = oracle_sample_run(w, inputs_host, T_s)
+    reps = 1
+    total = dt
+    while total < 0.5 * target_s and reps < 50:
+        total += oracle_sample_run(w, inputs_host, T_s)
+        reps += 1
+    return dict(value=T_s * reps / total, unit=UNIT, cores=1, kind="oracle",
+                sample=f"first {T_s} of {w.T} tokens of {w.name}, whole path (gate, layout, "
+                       f"dispatch of every kept row, combine of every token), {reps} pass(es), "
+                       f"{total:.1f} s single-threaded C oracle")
+
+
+def host_inputs(w, inputs, eo):
+    import numpy as np
+    import torch
+    d = dict(logits=inputs["logits"].cpu().numpy(),
+             x=inputs["x"].cpu().view(torch.int16).numpy().view(np.uint16))
+    if eo is not None:
+        d["eo"] = eo[:HOST_EO_ROWS].cpu().view(torch.int16).numpy().view(np.uint16)
+    if inputs.get("shared") is not None:
+        d["shared"] = inputs["shared"].cpu().view(torch.int16).numpy().view(np.uint16)
+    return d
+
+
+def config_of(w, world):
+    return {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "P": w.P,
+            "gate": "softmax_topk" if w.mode else "topk_softmax",
+            "transport": "e4m3" if w.fp8 else "bf16", "Ks": w.Ks,
+            "capacity": w.capacity or None,
+            "l2": "no flush: each step touches ~%.2f GB, far above the 126 MB L2" % (
+                (w.T * w.H * 2 * 2 + 2 * w.T * w.k * w.H * (1 if w.fp8 else 2)) / 1e9),
+            "parallelism": f"dp{world}"}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    world, rank, local = dist_env()
+    if rank != 0:
+        return 0
+    import numpy as np
+    import torch
+
+    from combine_moe_gate_warp_gb300 import workloads
+    w = workloads.WORKLOADS[args.workload]
+    inputs = workloads.make_inputs(w, "cpu")
+    hi = dict(logits=inputs["logits"].numpy(),
+              x=inputs["x"].view(torch.int16).numpy().view(np.uint16))
+    if inputs["shared"] is not None:
+        hi["shared"] = inputs["shared"].view(torch.int16).numpy().view(np.uint16)
+    # seeded expert outputs for the sampled rows
+    hi["eo"] = workloads.make_expert_out(w, min(w.r_max, HOST_EO_ROWS), "cpu").view(torch.int16).numpy().view(np.uint16)
+    # size one step so that warmup + steps stay within about three minutes
+    budget_s = 180.0 / max(1, args.steps + args.warmup)
+    T_max = max_sample_tokens(w)
+    T_s = min(T_max, 64)
+    dt = oracle_sample_run(w, hi, T_s)
+    while dt < 0.5 * budget_s and T_s < T_max:
+        T_s = min(T_max, max(T_s * 2, int(T_s * budget_s / max(dt, 1e-6) * 0.7)))
+        dt = oracle_sample_run(w, hi, T_s)
+    for _ in range(args.warmup):
+        oracle_sample_run(w, hi, T_s)
+    total = 0.0
+    for _ in range(args.steps):
+        total += oracle_sample_run(w, hi, T_s)
+    value = T_s * args.steps / total
+    sample = f"first {T_s} of {w.T} tokens of {w.name} per step, single-threaded C oracle"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32/f64 (CPU)",
+            "data": "synthetic (seeded), same recipe as the GPU arm", "config": config_of(w, world),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+
+    from combine_moe_gate_warp_gb300 import RoutePlan, RouteShape, build, workloads
+    world, rank, local = dist_env()
+    init_dist(world, "nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    build()
+    base = workloads.WORKLOADS[args.workload]
+    w = workloads.Workload(**{**base.__dict__, "seed": base.seed + 7919 * rank})  # own batch per rank
+
+    inputs = workloads.make_inputs(w, dev)
+    shape = RouteShape(T=w.T, H=w.H, E=w.E, k=w.k, P=w.P, mode=w.mode, fp8=w.fp8, Ks=w.Ks,
+                       capacity=w.capacity)
+    plan = RoutePlan(shape, dev)
+    eo = None if w.identity_experts else workloads.make_expert_out(w, max(plan.r_max, 1), dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        plan.step(inputs["logits"], inputs["x"], plan.packed if eo is None else eo, inputs["shared"])
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    st = plan.status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} after warm-up")
+    R = int(plan.layout.offsets[w.E].item())
+
+    bus = None
+    try:
+        props = torch.cuda.get_device_properties(dev)
+        bus = "%04x:%02x:%02x.0" % (getattr(props, "pci_domain_id", 0), props.pci_bus_id, props.pci_device_id)
+    except Exception:
+        bus = None
+    sampler = ClockSampler(bus) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    start.record(stream)
+    for i in range(K):
+        e = ev[i]
+        e[0].record(stream)
+        plan.gate(inputs["logits"])
+        e[1].record(stream)
+        plan.dispatch_layout()
+        e[2].record(stream)
+        plan.dispatch(inputs["x"])
+        e[3].record(stream)
+        plan.combine(plan.packed if eo is None else eo, inputs["shared"])
+        e[4].record(stream)
+    stop.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t_wall1 = time.time()
+    elapsed_ms = start.elapsed_time(stop)
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
+    st = plan.status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} during the timed steps")
+    if sampler:
+        time.sleep(0.25)
+        sampler.stop()
+    names = ["gate", "layout", "dispatch", "combine"]
+    per = {n: statistics.fmean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K))
+           for j, n in enumerate(names)}
+    by = kernel_bytes(w, R)
+    peak, peak_kind = hbm_peak()
+    dom = max(("dispatch", "combine"), key=lambda n: per[n])
+    achieved = by[dom] / (per[dom] * 1e-3) / 1e9
+    traffic = measured_traffic(dom, w.name)
+    ms_step = elapsed_ms / K
+    tokens_per_s = world * w.T * K / (elapsed_ms * 1e-3)
+    step_gbs = by["roofline_step"] / (ms_step * 1e-3) / 1e9
+
+    # end to end through the public API: pinned host inputs copied in, result copied out
+    e2e = None
+    if not args.no_e2e:
+        pin = dict(logits=inputs["logits"].cpu().pin_memory(), x=inputs["x"].cpu().pin_memory())
+        eo_h = None if eo is None else eo.cpu().pin_memory()
+        sh_h = None if inputs["shared"] is None else inputs["shared"].cpu().pin_memory()
+        d_logits = torch.empty_like(inputs["logits"])
+        d_x = torch.empty_like(inputs["x"])
+        d_eo = None if eo is None else torch.empty_like(eo)
+        d_sh = None if sh_h is None else torch.empty_like(inputs["shared"])
+        y_h = torch.empty(plan.y.shape, dtype=plan.y.dtype, pin_memory=True)
+        stats_h = torch.empty(2, dtype=torch.float64, pin_memory=True)
+        h2d = sum(t.numel() * t.element_size() for t in (pin["logits"], pin["x"], eo_h, sh_h) if t is not None)
+        d2h = y_h.numel() * y_h.element_size() + 16
+
+        def e2e_step():
+            d_logits.copy_(pin["logits"], non_blocking=True)
+            d_x.copy_(pin["x"], non_blocking=True)
+            if d_eo is not None:
+                d_eo.copy_(eo_h, non_blocking=True)
+            if d_sh is not None:
+                d_sh.copy_(sh_h, non_blocking=True)
+            plan.step(d_logits, d_x, plan.packed if d_eo is None else d_eo, d_sh)
+            y_h.copy_(plan.y, non_blocking=True)
+            stats_h[0:1].copy_(plan.aux_loss, non_blocking=True)
+            stats_h[1:2].copy_(plan.entropy, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        K2 = max(1, args.e2e_steps)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        a.record(stream)
+        for _ in range(K2):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = max_over_ranks(a.elapsed_time(b), world, dev)
+        e2e = {"value": world * w.T * K2 / (e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / K2, "steps": K2,
+               "path": "pinned host -> device copies, the four C-ABI calls, y/aux/entropy back, one stream"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, host_inputs(w, inputs, eo), args.cpu_seconds)
+
+    clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": tokens_per_s, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if w.fp8 else "bf16",
+            "data": "synthetic (seeded): x ~ N(0,1) bf16, router logits fp32, expert outputs N(0,1) bf16",
+            "config": config_of(w, world),
+            "hbm_gbs": step_gbs, "hbm_frac": step_gbs / peak, "R": R,
+            "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                         "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": traffic, "algorithmic_bytes": by[dom]},
+            "kernels_ms": per,
+            "kernels_gbs": {n: by[n] / (per[n] * 1e-3) / 1e9 for n in names},
+            "gpu_launches": 4 * K,
+            "clocks": clocks,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,227 @@
+"""Thin Python binding of libmoeroute's C ABI (include/moe_route.h).
+
+Argument marshalling only: every function here has the name of the C entry
+point it calls, checks dtypes/devices/shapes of the torch tensors it is
+given, passes their device pointers and the current CUDA stream, and raises
+``MoeError`` on a non-zero status.  All routing work runs in the library's
+CUDA kernels; there is no CPU fallback.  PyTorch only provides device memory
+and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_UNSUPPORTED = 2
+MOE_ERR_WORKSPACE_TOO_SMALL = 3
+MOE_ERR_CUDA = 4
+MOE_ERR_TIMEOUT = 5
+MOE_ERR_DEVICE_DATA = 6
+
+MOE_TOPK_SOFTMAX = 0
+MOE_SOFTMAX_TOPK = 1
+
+MOE_MAX_EXPERTS = 256
+MOE_MAX_TOPK = 16
+MOE_MAX_SHARED = 8
+MOE_MAX_H_FP8 = 16384
+
+_LIB = None
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+class moe_layout(ctypes.Structure):
+    """Mirror of ``struct moe_layout`` (host struct of device pointers)."""
+    _fields_ = [
+        ("T", ctypes.c_int32), ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("P", ctypes.c_int32),
+        ("capacity", ctypes.c_int32), ("r_max", ctypes.c_int32),
+        ("ws", ctypes.c_void_p),
+        ("counts", ctypes.c_void_p), ("offsets", ctypes.c_void_p),
+        ("part_rows", ctypes.c_void_p), ("part_offsets", ctypes.c_void_p),
+        ("part_tokens", ctypes.c_void_p), ("src_pos", ctypes.c_void_p),
+        ("dst_row", ctypes.c_void_p), ("capacity_mask", ctypes.c_void_p),
+        ("dropped", ctypes.c_void_p),
+    ]
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib():
+    """Load libmoeroute.so.  Raises if it has not been built: the routing
+    path has no substitute implementation."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = _build.LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build the CUDA library first "
+                           "(python -c 'import __graft_entry__ as g; g.build()')")
+    L = ctypes.CDLL(path)
+    P, I, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    L.moe_workspace_size.argtypes = [I, I, I, I]
+    L.moe_workspace_size.restype = SZ
+    L.moe_workspace_init.argtypes = [P, SZ, P]
+    L.moe_workspace_init.restype = I
+    L.moe_rows_max.argtypes = [I, I, I, I]
+    L.moe_rows_max.restype = ctypes.c_int64
+    L.moe_gate.argtypes = [P, I, I, I, I, P, P, P, P, P, P, SZ, P]
+    L.moe_gate.restype = I
+    L.moe_dispatch_layout.argtypes = [P, P, I, I, I, I, I, P, ctypes.POINTER(moe_layout), P, SZ, P]
+    L.moe_dispatch_layout.restype = I
+    L.moe_dispatch.argtypes = [P, I, I, ctypes.POINTER(moe_layout), I, P, P, P]
+    L.moe_dispatch.restype = I
+    L.moe_combine.argtypes = [P, ctypes.POINTER(moe_layout), P, P, I, I, I, P, P]
+    L.moe_combine.restype = I
+    L.moe_get_status.argtypes = [P, P]
+    L.moe_get_status.restype = I
+    L.moe_status_string.argtypes = [I]
+    L.moe_status_string.restype = ctypes.c_char_p
+    _LIB = L
+    return L
+
+
+def status_string(status: int) -> str:
+    try:
+        return lib().moe_status_string(int(status)).decode()
+    except Exception:  # library not loadable: still describe the code
+        return {0: "ok", 1: "invalid argument", 2: "unsupported size or option",
+                3: "workspace too small", 4: "CUDA runtime error", 5: "device wait timed out",
+                6: "invalid data found on the device"}.get(int(status), "unknown status")
+
+
+def _check(status: int, where: str):
+    if status != MOE_OK:
+        raise MoeError(status, where)
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _nbytes(t: torch.Tensor) -> int:
+    return t.numel() * t.element_size()
+
+
+# --------------------------------------------------------------------------
+# entry points (same names as the C ABI)
+# --------------------------------------------------------------------------
+
+def moe_workspace_size(T: int, E: int, k: int, P: int) -> int:
+    return int(lib().moe_workspace_size(T, E, k, P))
+
+
+def moe_workspace_init(ws: torch.Tensor, stream=None) -> None:
+    _check(lib().moe_workspace_init(_ptr(ws, name="ws"), _nbytes(ws), _stream(stream)),
+           "moe_workspace_init")
+
+
+def moe_rows_max(T: int, E: int, k: int, capacity: int) -> int:
+    return int(lib().moe_rows_max(T, E, k, capacity))
+
+
+def moe_gate(logits, k: int, mode: int, topk_idx, gates, expert_counts, aux_loss, entropy, ws,
+             stream=None) -> None:
+    T, E = logits.shape
+    _check(lib().moe_gate(_ptr(logits, torch.float32, "logits"), T, E, k, mode,
+                          _ptr(topk_idx, torch.int32, "topk_idx"), _ptr(gates, torch.float32, "gates"),
+                          _ptr(expert_counts, torch.int32, "expert_counts"),
+                          _ptr(aux_loss, torch.float64, "aux_loss"),
+                          _ptr(entropy, torch.float64, "entropy"),
+                          _ptr(ws, name="ws"), _nbytes(ws), _stream(stream)), "moe_gate")
+
+
+def moe_dispatch_layout(topk_idx, expert_counts, T: int, E: int, k: int, P: int, capacity: int,
+                        gates_or_null, layout: "Layout", ws, stream=None) -> None:
+    _check(lib().moe_dispatch_layout(_ptr(topk_idx, torch.int32, "topk_idx"),
+                                     _ptr(expert_counts, torch.int32, "expert_counts"),
+                                     T, E, k, P, capacity,
+                                     _ptr(gates_or_null, torch.float32, "gates"),
+                                     ctypes.byref(layout.c), _ptr(ws, name="ws"), _nbytes(ws),
+                                     _stream(stream)), "moe_dispatch_layout")
+
+
+def moe_dispatch(x, T: int, H: int, layout: "Layout", fp8: int, packed, scales=None,
+                 stream=None) -> None:
+    _check(lib().moe_dispatch(_ptr(x, torch.bfloat16, "x"), T, H, ctypes.byref(layout.c), int(fp8),
+                              _ptr(packed, torch.uint8 if fp8 else torch.bfloat16, "packed"),
+                              _ptr(scales, torch.float32, "scales"), _stream(stream)), "moe_dispatch")
+
+
+def moe_combine(expert_out, layout: "Layout", gates, shared_out, Ks: int, T: int, H: int, y,
+                stream=None) -> None:
+    _check(lib().moe_combine(_ptr(expert_out, torch.bfloat16, "expert_out"), ctypes.byref(layout.c),
+                             _ptr(gates, torch.float32, "gates"),
+                             _ptr(shared_out, torch.bfloat16, "shared_out"), Ks, T, H,
+                             _ptr(y, torch.bfloat16, "y"), _stream(stream)), "moe_combine")
+
+
+def moe_get_status(ws, stream=None) -> int:
+    """Synchronise, return and clear the device status recorded in ``ws``."""
+    return int(lib().moe_get_status(_ptr(ws, name="ws"), _stream(stream)))
+
+
+# --------------------------------------------------------------------------
+# buffer helpers (allocation through PyTorch)
+# --------------------------------------------------------------------------
+
+class Layout:
+    """Device buffers of one ``moe_layout`` plus the ctypes struct that
+    points at them."""
+
+    def __init__(self, T: int, E: int, k: int, P: int, capacity: int = 0, device="cuda"):
+        r_max = moe_rows_max(T, E, k, capacity)
+        if r_max < 0:
+            raise MoeError(MOE_ERR_UNSUPPORTED, "Layout")
+        i32 = dict(dtype=torch.int32, device=device)
+        self.counts = torch.empty(E, **i32)
+        self.offsets = torch.empty(E + 1, **i32)
+        self.part_rows = torch.empty(P, **i32)
+        self.part_offsets = torch.empty(P + 1, **i32)
+        self.part_tokens = torch.empty(P, **i32)
+        self.src_pos = torch.empty(max(r_max, 1), **i32)
+        self.dst_row = torch.empty(max(T * k, 1), **i32)
+        self.capacity_mask = torch.empty(max(T * k, 1), dtype=torch.uint8, device=device)
+        self.dropped = torch.empty(1, dtype=torch.int64, device=device)
+        self.r_max = r_max
+        c = moe_layout()
+        for name in ("counts", "offsets", "part_rows", "part_offsets", "part_tokens", "src_pos",
+                     "dst_row", "capacity_mask", "dropped"):
+            setattr(c, name, getattr(self, name).data_ptr())
+        self.c = c
+
+
+def alloc_workspace(T: int, E: int, k: int, P: int, device="cuda", stream=None) -> torch.Tensor:
+    n = moe_workspace_size(T, E, k, P)
+    if n == 0:
+        raise MoeError(MOE_ERR_UNSUPPORTED, "moe_workspace_size")
+    ws = torch.empty((n + 15) // 16 * 16, dtype=torch.uint8, device=device)
+    moe_workspace_init(ws, stream)
+    return ws

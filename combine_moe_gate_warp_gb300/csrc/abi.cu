@@ -1,0 +1,171 @@
+// abi.cu -- the extern "C" entry points declared in include/moe_route.h.
+// Each call validates its arguments on the host (nothing is enqueued when
+// they are bad) and then launches the kernels of one step on `stream`.
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+int device_sm_count()
+{
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+}  // namespace moe
+
+namespace {
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline moe_status check_sizes(int T, int E, int k)
+{
+    if (T < 0) return MOE_ERR_INVALID_ARG;
+    if (E < 1 || E > MOE_MAX_EXPERTS) return MOE_ERR_UNSUPPORTED;
+    if (k < 1 || k > MOE_MAX_TOPK || k > E) return MOE_ERR_UNSUPPORTED;
+    if ((long long)T * k >= (1LL << 30)) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+inline moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_workspace_size(int T, int E, int k, int P)
+{
+    if (check_sizes(T, E, k) != MOE_OK) return 0;
+    if (P < 1 || P > E || E % P != 0) return 0;
+    return moe::kWsHeaderBytes + (size_t)moe::layout_tiles(T, k) * (size_t)E * sizeof(unsigned long long);
+}
+
+moe_status moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t stream)
+{
+    if (!ws || ws_bytes < moe::kWsHeaderBytes) return MOE_ERR_INVALID_ARG;
+    return from_cuda(cudaMemsetAsync(ws, 0, ws_bytes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int64_t moe_rows_max(int T, int E, int k, int capacity)
+{
+    if (check_sizes(T, E, k) != MOE_OK) return -1;
+    const int64_t A = (int64_t)T * k;
+    if (capacity <= 0) return A;
+    const int64_t c = (int64_t)E * capacity;
+    return c < A ? c : A;
+}
+
+moe_status moe_gate(const float *logits, int T, int E, int k, int mode, int32_t *topk_idx,
+                    float *gates, int32_t *expert_counts, double *aux_loss, double *entropy,
+                    void *ws, size_t ws_bytes, moe_stream_t stream)
+{
+    moe_status st = check_sizes(T, E, k);
+    if (st != MOE_OK) return st;
+    if (mode != MOE_TOPK_SOFTMAX && mode != MOE_SOFTMAX_TOPK) return MOE_ERR_INVALID_ARG;
+    if (!expert_counts || !aux_loss || !entropy || !ws) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!logits || !topk_idx || !gates)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(logits) || !aligned16(topk_idx) || !aligned16(gates) || !aligned16(ws))
+        return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < moe::kWsHeaderBytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    return from_cuda(moe::launch_gate(logits, T, E, k, mode, topk_idx, gates, expert_counts, aux_loss,
+                                      entropy, ws, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_dispatch_layout(const int32_t *topk_idx, const int32_t *expert_counts, int T, int E,
+                               int k, int P, int capacity, float *gates_or_null, moe_layout *L,
+                               void *ws, size_t ws_bytes, moe_stream_t stream)
+{
+    moe_status st = check_sizes(T, E, k);
+    if (st != MOE_OK) return st;
+    if (P < 1 || P > E || E % P != 0) return MOE_ERR_UNSUPPORTED;
+    if (!L || !expert_counts || !ws) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && !topk_idx) return MOE_ERR_INVALID_ARG;
+    if (!L->counts || !L->offsets || !L->part_rows || !L->part_offsets || !L->part_tokens ||
+        !L->dropped || (T > 0 && (!L->src_pos || !L->dst_row || !L->capacity_mask)))
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(ws)) return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < moe_workspace_size(T, E, k, P)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    L->T = T;
+    L->E = E;
+    L->k = k;
+    L->P = P;
+    L->capacity = capacity > 0 ? capacity : 0;
+    L->r_max = (int32_t)moe_rows_max(T, E, k, capacity);
+    L->ws = ws;
+    return from_cuda(moe::launch_layout(topk_idx, expert_counts, T, E, k, P, capacity, gates_or_null, L,
+                                        ws, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+static moe_status check_layout(const moe_layout *L, int T)
+{
+    if (!L || !L->ws || (T > 0 && !L->dst_row)) return MOE_ERR_INVALID_ARG;
+    if (L->T != T) return MOE_ERR_INVALID_ARG;
+    return check_sizes(L->T, L->E, L->k);
+}
+
+moe_status moe_dispatch(const void *x, int T, int H, const moe_layout *L, int fp8, void *packed,
+                        float *scales, moe_stream_t stream)
+{
+    moe_status st = check_layout(L, T);
+    if (st != MOE_OK) return st;
+    if (fp8 != 0 && fp8 != 1) return MOE_ERR_INVALID_ARG;
+    if (H < 8 || H % 8 != 0) return MOE_ERR_UNSUPPORTED;
+    if (fp8 && (H % 16 != 0 || H > MOE_MAX_H_FP8)) return MOE_ERR_UNSUPPORTED;
+    if (T > 0 && (!x || !packed || (fp8 && !scales))) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(packed) || !aligned16(scales)) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return from_cuda(fp8 ? moe::launch_dispatch_fp8(x, T, H, L, packed, scales, s)
+                         : moe::launch_dispatch_bf16(x, T, H, L, packed, s));
+}
+
+moe_status moe_combine(const void *expert_out, const moe_layout *L, const float *gates,
+                       const void *shared_out, int Ks, int T, int H, void *y, moe_stream_t stream)
+{
+    moe_status st = check_layout(L, T);
+    if (st != MOE_OK) return st;
+    if (H < 8 || H % 8 != 0) return MOE_ERR_UNSUPPORTED;
+    if (Ks < 0 || Ks > MOE_MAX_SHARED) return MOE_ERR_UNSUPPORTED;
+    if (T > 0 && (!expert_out || !gates || !y || (Ks > 0 && !shared_out))) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(expert_out) || !aligned16(y) || !aligned16(shared_out)) return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_combine(expert_out, L, gates, Ks > 0 ? shared_out : nullptr, Ks, T, H, y,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_get_status(void *ws, moe_stream_t stream)
+{
+    if (!ws) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    unsigned status = 0;
+    if (cudaMemcpy(&status, ws, sizeof(status), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    if (status != 0) {
+        if (cudaMemsetAsync(ws, 0, sizeof(status), s) != cudaSuccess) return MOE_ERR_CUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    return (moe_status)status;
+}
+
+const char *moe_status_string(moe_status status)
+{
+    switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported size or option";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_DEVICE_DATA: return "invalid data found on the device";
+    default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,116 @@
+// common.cuh -- pieces shared by the libmoeroute kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_route.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// Workspace.  A fixed 4 KiB header of counters followed by the decoupled
+// look-back flag words of the layout scan (one 64-bit word per tile and
+// expert).  Every counter is returned to zero by the kernel that used it, so
+// a zeroed workspace stays valid from call to call.
+// ---------------------------------------------------------------------------
+struct WsHeader {
+    unsigned status;        // first device error wins (atomicCAS from 0)
+    unsigned epoch;         // bumped once per layout launch; tags flag words
+    unsigned tile_ctr;      // layout: dynamic tile ids
+    unsigned done_ctr;      // layout: completed tiles
+    unsigned gate_ticket;   // gate: finished blocks
+    // Failure-injection hook for tests, written only from the host: when it
+    // holds tile+1, that layout tile does not publish its look-back flags,
+    // so its successor's bounded wait expires (MOE_ERR_TIMEOUT).  Zero in
+    // normal use; the layout call that sees it clears it.
+    unsigned inject_skip_publish;
+    unsigned pad0[26];
+    unsigned gate_counts[MOE_MAX_EXPERTS];  // gate: per-expert totals
+    unsigned part_tok[MOE_MAX_EXPERTS];     // layout: per-partition token totals
+};
+static_assert(sizeof(WsHeader) <= 4096, "workspace header must fit 4 KiB");
+constexpr size_t kWsHeaderBytes = 4096;
+
+__host__ __device__ inline unsigned long long *ws_flags(void *ws)
+{
+    return reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + kWsHeaderBytes);
+}
+
+// Layout tiling: about 1024 assignments per tile (T*k < 2^30 keeps every
+// count inside the 30-bit value field of a flag word).
+constexpr int kLayoutThreads = 256;
+constexpr int kLayoutWarps = kLayoutThreads / 32;
+constexpr int kLayoutTileAssign = 1024;
+__host__ __device__ inline int layout_tile_tokens(int k) { return kLayoutTileAssign / k; }
+__host__ __device__ inline int layout_tiles(long long T, int k)
+{
+    long long tt = layout_tile_tokens(k);
+    long long n = (T + tt - 1) / tt;
+    return n < 1 ? 1 : (int)n;
+}
+
+// Flag word: [63:32] epoch, [31:30] state, [29:0] value.
+constexpr unsigned long long kFlagAggregate = 1ull;
+constexpr unsigned long long kFlagInclusive = 2ull;
+__device__ __forceinline__ unsigned long long make_flag(unsigned epoch, unsigned long long state, unsigned value)
+{
+    return (static_cast<unsigned long long>(epoch) << 32) | (state << 30) | (value & 0x3FFFFFFFu);
+}
+
+// Bound on any spin-wait, in nanoseconds of %globaltimer.
+constexpr unsigned long long kSpinLimitNs = 1000000000ull;
+
+__device__ __forceinline__ unsigned long long global_timer_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void record_status(void *ws, unsigned code)
+{
+    if (ws) atomicCAS(&static_cast<WsHeader *>(ws)->status, 0u, code);
+}
+
+// Streaming 16-byte load (read once: do not keep in L1).
+__device__ __forceinline__ uint4 ld_stream_v4(const uint4 *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_v4(uint4 *p, const uint4 &v)
+{
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+// bf16 pair (one 32-bit word) -> two fp32
+__device__ __forceinline__ float bf16lo(unsigned w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(unsigned w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+}  // namespace moe
+
+// Host-side launchers (one per kernel family), called by the C ABI layer
+// after argument validation.  They enqueue on `s` and return the CUDA
+// launch status.
+namespace moe {
+cudaError_t launch_gate(const float *logits, int T, int E, int k, int mode, int32_t *topk_idx,
+                        float *gates, int32_t *expert_counts, double *aux, double *entropy,
+                        void *ws, cudaStream_t s);
+cudaError_t launch_layout(const int32_t *topk_idx, const int32_t *counts_in, int T, int E, int k,
+                          int P, int capacity, float *gates, const moe_layout *L, void *ws,
+                          cudaStream_t s);
+cudaError_t launch_dispatch_bf16(const void *x, int T, int H, const moe_layout *L, void *packed,
+                                 cudaStream_t s);
+cudaError_t launch_dispatch_fp8(const void *x, int T, int H, const moe_layout *L, void *packed,
+                                float *scales, cudaStream_t s);
+cudaError_t launch_combine(const void *eo, const moe_layout *L, const float *gates,
+                           const void *shared, int Ks, int T, int H, void *y, cudaStream_t s);
+int device_sm_count();
+}  // namespace moe

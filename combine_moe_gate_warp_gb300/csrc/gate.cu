@@ -1,0 +1,270 @@
+// gate.cu -- moe_gate: top-k gating over router logits plus routing
+// statistics, one fused kernel.
+//
+// Design (sm_103a).  A block stages a tile of TT tokens' logits in shared
+// memory with coalesced loads (row stride E|1 words, so that consecutive
+// threads reading "their" row hit distinct banks), then each thread owns one
+// token and keeps a sorted register list of its k best (value, expert)
+// pairs.  For E <= 256 and k <= 16 that is ~E compares per token, far fewer
+// instructions than k rounds of warp-wide shuffle arg-max, which is what the
+// A100 warp kernel of "DeepSeek MoE architecture evolution" (sec. 2.2)
+// spends per token.  Counts go to a shared-memory histogram, then one
+// global atomic per (block, expert) into the workspace; the last block to
+// finish (atomic ticket) publishes expert_counts and derives the aux loss
+// and entropy in fp64 from the exact integer counts, then clears the
+// workspace counters for the next call.
+//
+// Definitions: "DeepSeek MoE architecture evolution" ch.1 (top2_gating:
+// topk, softmax of the selected logits, aux = E * sum f_e^2) and sec. 2.3
+// (entropy of the expert counts, base 2, +1e-8 inside the log); "DeepSeek
+// MoE sync tax" sec. 4.1 (softmax over all experts, then top-k).
+#include <math.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kGateMaxThreads = 256;
+
+// Insert (v, e) into the descending list bv/bi of length K if it beats the
+// last entry.  Strictly-greater comparisons keep the earlier (lower) expert
+// id ahead on ties; -0.0 == +0.0 is a tie.
+template <int K>
+__device__ __forceinline__ void topk_insert(float (&bv)[K], int (&bi)[K], float v, int e)
+{
+    if (v > bv[K - 1]) {
+        bv[K - 1] = v;
+        bi[K - 1] = e;
+#pragma unroll
+        for (int j = K - 1; j > 0; --j) {
+            if (bv[j] > bv[j - 1]) {
+                float tv = bv[j]; bv[j] = bv[j - 1]; bv[j - 1] = tv;
+                int ti = bi[j]; bi[j] = bi[j - 1]; bi[j - 1] = ti;
+            }
+        }
+    }
+}
+
+template <int K>
+__device__ __forceinline__ void store_row_i32(int32_t *dst, const int (&v)[K])
+{
+    if constexpr (K % 4 == 0) {
+#pragma unroll
+        for (int j = 0; j < K; j += 4)
+            *reinterpret_cast<int4 *>(dst + j) = make_int4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+    } else if constexpr (K % 2 == 0) {
+#pragma unroll
+        for (int j = 0; j < K; j += 2) *reinterpret_cast<int2 *>(dst + j) = make_int2(v[j], v[j + 1]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < K; ++j) dst[j] = v[j];
+    }
+}
+
+template <int K>
+__device__ __forceinline__ void store_row_f32(float *dst, const float (&v)[K])
+{
+    if constexpr (K % 4 == 0) {
+#pragma unroll
+        for (int j = 0; j < K; j += 4)
+            *reinterpret_cast<float4 *>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+    } else if constexpr (K % 2 == 0) {
+#pragma unroll
+        for (int j = 0; j < K; j += 2) *reinterpret_cast<float2 *>(dst + j) = make_float2(v[j], v[j + 1]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < K; ++j) dst[j] = v[j];
+    }
+}
+
+template <int K, int MODE>
+__global__ void __launch_bounds__(kGateMaxThreads)
+gate_kernel(const float *__restrict__ logits, int T, int E, int32_t *__restrict__ topk_idx,
+            float *__restrict__ gates, int32_t *__restrict__ expert_counts,
+            double *__restrict__ aux_out, double *__restrict__ ent_out, void *ws_raw)
+{
+    extern __shared__ float s_logit[];  // [TT][stride]
+    __shared__ unsigned s_hist[MOE_MAX_EXPERTS];
+    __shared__ int s_bad;
+    __shared__ int s_last;
+    WsHeader *ws = static_cast<WsHeader *>(ws_raw);
+
+    const int TT = blockDim.x;
+    const int stride = E | 1;
+    const long long t0 = (long long)blockIdx.x * TT;
+    const int rows = (int)min((long long)TT, (long long)T - t0);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+
+    for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0u;
+    if (threadIdx.x == 0) s_bad = 0;
+
+    // Stage the tile: warp w copies rows w, w + nwarps, ... (coalesced per row).
+    for (int r = warp; r < rows; r += nwarps) {
+        const float *src = logits + (t0 + r) * (long long)E;
+        float *dst = s_logit + r * stride;
+        for (int c = lane; c < E; c += 32) dst[c] = __ldg(src + c);
+    }
+    __syncthreads();
+
+    if (threadIdx.x < rows) {
+        const float *row = s_logit + threadIdx.x * stride;
+        float bv[K];
+        int bi[K];
+        bool finite = true;
+        // First K experts: insertion-sorted in place.
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            bv[j] = row[j];
+            bi[j] = j;
+            finite &= isfinite(bv[j]);
+        }
+#pragma unroll
+        for (int i = 1; i < K; ++i) {
+#pragma unroll
+            for (int j = i; j > 0; --j) {
+                if (bv[j] > bv[j - 1]) {
+                    float tv = bv[j]; bv[j] = bv[j - 1]; bv[j - 1] = tv;
+                    int ti = bi[j]; bi[j] = bi[j - 1]; bi[j - 1] = ti;
+                }
+            }
+        }
+        for (int e = K; e < E; ++e) {
+            float v = row[e];
+            finite &= isfinite(v);
+            topk_insert<K>(bv, bi, v, e);
+        }
+        if (!finite) s_bad = 1;
+
+        // Gate weights, fp32, shifted by the largest logit.
+        const float m = bv[0];
+        float g[K];
+        if constexpr (MODE == MOE_TOPK_SOFTMAX) {
+            float ex[K];
+            float sum = 0.0f;
+#pragma unroll
+            for (int j = 0; j < K; ++j) {
+                ex[j] = expf(__fsub_rn(bv[j], m));
+                sum = __fadd_rn(sum, ex[j]);
+            }
+#pragma unroll
+            for (int j = 0; j < K; ++j) g[j] = __fdiv_rn(ex[j], sum);
+        } else {
+            float sum = 0.0f;
+            for (int e = 0; e < E; ++e) sum = __fadd_rn(sum, expf(__fsub_rn(row[e], m)));
+#pragma unroll
+            for (int j = 0; j < K; ++j) g[j] = __fdiv_rn(expf(__fsub_rn(bv[j], m)), sum);
+        }
+
+        const long long t = t0 + threadIdx.x;
+        store_row_i32<K>(topk_idx + t * K, bi);
+        store_row_f32<K>(gates + t * K, g);
+#pragma unroll
+        for (int j = 0; j < K; ++j) atomicAdd(&s_hist[bi[j]], 1u);
+    }
+    __syncthreads();
+
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        if (s_hist[e]) atomicAdd(&ws->gate_counts[e], s_hist[e]);
+    if (threadIdx.x == 0 && s_bad) record_status(ws, MOE_ERR_DEVICE_DATA);
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = (atomicAdd(&ws->gate_ticket, 1u) == gridDim.x - 1);
+    __syncthreads();
+    if (!s_last) return;
+
+    // Last block: publish the totals and the fp64 statistics.
+    __threadfence();
+    __shared__ double s_term[MOE_MAX_EXPERTS];
+    __shared__ unsigned long long s_sq[MOE_MAX_EXPERTS];
+    const double total = (double)T * (double)K;
+    for (int e = threadIdx.x; e < MOE_MAX_EXPERTS; e += blockDim.x) {
+        double term = 0.0;
+        unsigned long long sq = 0ull;
+        if (e < E) {
+            unsigned c = atomicExch(&ws->gate_counts[e], 0u);
+            expert_counts[e] = (int32_t)c;
+            sq = (unsigned long long)c * c;
+            if (T > 0) {
+                double p = (double)c / total;
+                term = p * log2(p + 1e-8);
+            }
+        }
+        s_term[e] = term;
+        s_sq[e] = sq;
+    }
+    __syncthreads();
+    // Fixed-shape tree reduction: deterministic.
+    for (int w = MOE_MAX_EXPERTS / 2; w > 0; w >>= 1) {
+        for (int e = threadIdx.x; e < w; e += blockDim.x) {
+            s_term[e] += s_term[e + w];
+            s_sq[e] += s_sq[e + w];
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        if (T > 0) {
+            *aux_out = (double)E * ((double)s_sq[0] / ((double)T * (double)T));
+            *ent_out = -s_term[0];
+        } else {
+            *aux_out = 0.0;
+            *ent_out = 0.0;
+        }
+        ws->gate_ticket = 0u;
+    }
+}
+
+template <int K, int MODE>
+cudaError_t launch_k(const float *logits, int T, int E, int32_t *idx, float *gates, int32_t *counts,
+                     double *aux, double *ent, void *ws, cudaStream_t s)
+{
+    const int stride = E | 1;
+    // Tile size: keep the staging buffer <= 64 KiB and prefer >= 2 blocks per SM.
+    int tt = kGateMaxThreads;
+    while (tt > 32 && (size_t)tt * stride * sizeof(float) > 64 * 1024) tt >>= 1;
+    const long long want_blocks = 2LL * device_sm_count();
+    while (tt > 64 && ((long long)T + tt - 1) / tt < want_blocks) tt >>= 1;
+    const size_t smem = (size_t)tt * stride * sizeof(float);
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t err = cudaFuncSetAttribute(gate_kernel<K, MODE>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+        if (err != cudaSuccess) return err;
+        attr_set = true;
+    }
+    long long blocks = ((long long)T + tt - 1) / tt;
+    if (blocks < 1) blocks = 1;
+    gate_kernel<K, MODE><<<(unsigned)blocks, tt, smem, s>>>(logits, T, E, idx, gates, counts, aux, ent, ws);
+    return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t launch_mode(const float *logits, int T, int E, int k, int32_t *idx, float *gates,
+                        int32_t *counts, double *aux, double *ent, void *ws, cudaStream_t s)
+{
+    switch (k) {
+#define MOE_GATE_CASE(KK) \
+    case KK: return launch_k<KK, MODE>(logits, T, E, idx, gates, counts, aux, ent, ws, s);
+        MOE_GATE_CASE(1) MOE_GATE_CASE(2) MOE_GATE_CASE(3) MOE_GATE_CASE(4)
+        MOE_GATE_CASE(5) MOE_GATE_CASE(6) MOE_GATE_CASE(7) MOE_GATE_CASE(8)
+        MOE_GATE_CASE(9) MOE_GATE_CASE(10) MOE_GATE_CASE(11) MOE_GATE_CASE(12)
+        MOE_GATE_CASE(13) MOE_GATE_CASE(14) MOE_GATE_CASE(15) MOE_GATE_CASE(16)
+#undef MOE_GATE_CASE
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_gate(const float *logits, int T, int E, int k, int mode, int32_t *topk_idx,
+                        float *gates, int32_t *expert_counts, double *aux, double *entropy,
+                        void *ws, cudaStream_t s)
+{
+    if (mode == MOE_TOPK_SOFTMAX)
+        return launch_mode<MOE_TOPK_SOFTMAX>(logits, T, E, k, topk_idx, gates, expert_counts, aux,
+                                             entropy, ws, s);
+    return launch_mode<MOE_SOFTMAX_TOPK>(logits, T, E, k, topk_idx, gates, expert_counts, aux,
+                                         entropy, ws, s);
+}
+
+}  // namespace moe

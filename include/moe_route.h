@@ -1,0 +1,209 @@
+/*
+ * moe_route.h -- C ABI of libmoeroute, the GB300 (sm_103a) CUDA library for
+ * the token-routing hot path of a Mixture-of-Experts layer:
+ *
+ *     moe_gate -> moe_dispatch_layout -> moe_dispatch -> (expert FFN) -> moe_combine
+ *
+ * Source pages cited below:
+ *   [P1] "Deepseek-MoE sync-tax essence and four-layer optimisation guide"
+ *        (gsyq.cn news 1572160)
+ *   [P2] "DeepSeek MoE sync tax" (wmrh.cn news 47329)
+ *   [P3] "DeepSeek MoE architecture evolution" (lpnh.cn news 699721)
+ *   [P4] "MoE data traits ... DeepEP and MoE all-to-all data handling"
+ *        (zzszmyf.github.io notes, mirror of a Zhihu article)
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every array argument is a DEVICE pointer owned by the caller.  The
+ *   library never allocates, frees or synchronises inside the four hot
+ *   calls; they only enqueue kernels on `stream` and return.
+ * - Array base pointers must be 16-byte aligned (128-bit vector access);
+ *   a misaligned pointer is MOE_ERR_INVALID_ARG.
+ * - Argument errors are detected on the host before anything is enqueued:
+ *   such a call has no effect.  Problems found on the device (out-of-range
+ *   expert ids, non-finite logits, inconsistent counts, an expired wait)
+ *   are recorded in a status word inside the workspace and read back with
+ *   moe_get_status().  Kernels never trap; they skip the bad element.
+ * - A "workspace" is a caller-owned device buffer of moe_workspace_size()
+ *   bytes, zeroed once by moe_workspace_init().  The gate and layout calls
+ *   use it for counters and cross-block flags and leave it clean for the
+ *   next call.  One workspace serves calls issued in order on ONE stream;
+ *   calls that may run concurrently need separate workspaces.
+ * - Assignment a = t*k + j is slot j (descending logit order) of token t.
+ * - bf16 tensors are raw 16-bit bfloat16 patterns; e4m3 codes are bytes in
+ *   the OCP "E4M3FN" encoding.
+ *
+ * Supported range: 1 <= E <= 256, 1 <= k <= min(E, 16), 1 <= P <= E with
+ * E % P == 0, 0 <= T and T*k < 2^30, H % 8 == 0 (H % 16 == 0 and
+ * H <= 16384 for FP8), 0 <= Ks <= 8.  Anything else is
+ * MOE_ERR_UNSUPPORTED; there is no fallback path.
+ */
+#ifndef MOE_ROUTE_H
+#define MOE_ROUTE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *moe_stream_t;
+
+typedef int moe_status;
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG 1          /* null/misaligned pointer, bad enum, T < 0 */
+#define MOE_ERR_UNSUPPORTED 2          /* outside the supported range above */
+#define MOE_ERR_WORKSPACE_TOO_SMALL 3  /* ws_bytes < moe_workspace_size(...) */
+#define MOE_ERR_CUDA 4                 /* a CUDA runtime call or launch failed */
+#define MOE_ERR_TIMEOUT 5              /* device: a cross-block wait expired */
+#define MOE_ERR_DEVICE_DATA 6          /* device: bad expert id / non-finite logit / counts mismatch */
+
+/* Gate modes. */
+#define MOE_TOPK_SOFTMAX 0  /* softmax over the k selected logits ([P3] ch.1 top2_gating) */
+#define MOE_SOFTMAX_TOPK 1  /* softmax over all E logits, keep the k selected, no renormalisation
+                               (DeepSeekMoE fine-grained routing, [P2] sec. 2.1 and 4.1) */
+
+#define MOE_MAX_EXPERTS 256
+#define MOE_MAX_TOPK 16
+#define MOE_MAX_SHARED 8
+#define MOE_MAX_H_FP8 16384
+
+/*
+ * Routing metadata written by moe_dispatch_layout and read by moe_dispatch
+ * and moe_combine: the target/source index maps the dispatch saves so that
+ * the combine needs no second routing ([P4] sec. 7.5.2, "indices" and
+ * "locations").  The struct itself lives in host memory; its array members
+ * are caller-allocated DEVICE buffers of the sizes shown.  The scalar
+ * members and `ws` are filled in by moe_dispatch_layout.
+ */
+typedef struct moe_layout {
+    int32_t T, E, k, P;      /* filled by moe_dispatch_layout */
+    int32_t capacity;        /* per-expert row limit, 0 = none (filled) */
+    int32_t r_max;           /* rows that packed buffers must hold (filled) */
+    void *ws;                /* workspace used for device status (filled) */
+    int32_t *counts;         /* [E]   kept rows per expert = min(count_e, capacity) */
+    int32_t *offsets;        /* [E+1] exclusive prefix of counts; offsets[E] = R */
+    int32_t *part_rows;      /* [P]   rows of logical partition p (experts p*E/P ..) */
+    int32_t *part_offsets;   /* [P+1] first packed row of partition p; [P] = R */
+    int32_t *part_tokens;    /* [P]   tokens with >= 1 kept assignment in partition p */
+    int32_t *src_pos;        /* [r_max] packed row -> assignment a (rows >= R untouched) */
+    int32_t *dst_row;        /* [T*k] assignment -> packed row, -1 if dropped */
+    uint8_t *capacity_mask;  /* [T*k] 1 kept, 0 dropped */
+    int64_t *dropped;        /* [1]   T*k - R */
+} moe_layout;
+
+/* Bytes of workspace needed by moe_gate and moe_dispatch_layout for these
+ * sizes (0 if the sizes are unsupported). */
+size_t moe_workspace_size(int T, int E, int k, int P);
+
+/* Zero a workspace (cudaMemsetAsync on `stream`).  Needed once after
+ * allocation, and again only if a kernel using it was aborted. */
+moe_status moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Packed rows the layout can produce: T*k, or min(T*k, E*capacity). */
+int64_t moe_rows_max(int T, int E, int k, int capacity);
+
+/*
+ * moe_gate -- top-k gating over router logits, with routing statistics.
+ * [P3] ch.1 (top2_gating: torch.topk, softmax of the selected logits, aux
+ * loss = E * sum_e f_e^2); [P3] sec. 2.3 (entropy of the expert counts);
+ * [P2] sec. 4.1 (softmax over all experts then top-k).
+ *
+ *   logits        [T, E] fp32, row-major.  Must be finite (else
+ *                 MOE_ERR_DEVICE_DATA is recorded).
+ *   topk_idx  out [T, k] int32: the k largest logits per token, value
+ *                 descending, equal values to the lower expert id
+ *                 (-0.0 equals +0.0).
+ *   gates     out [T, k] fp32 gate weights (mode above), fp32 arithmetic.
+ *   expert_counts out [E] int32: assignments per expert (sums to T*k).
+ *   aux_loss  out [1] fp64: E * sum_e (count_e / T)^2.
+ *   entropy   out [1] fp64: -sum_e p_e log2(p_e + 1e-8), p_e = count_e / (T*k).
+ *                 Both are 0 when T == 0.
+ *   ws, ws_bytes  workspace (>= moe_workspace_size(T, E, k, 1)).
+ */
+moe_status moe_gate(const float *logits, int T, int E, int k, int mode,
+                    int32_t *topk_idx, float *gates, int32_t *expert_counts,
+                    double *aux_loss, double *entropy,
+                    void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_dispatch_layout -- per-expert and per-partition counts, prefix
+ * offsets and the stable permutation.  [P4] sec. 7 "Dispatch" detail
+ * (reorder by target expert id, pack same-destination tokens
+ * contiguously); sec. 7.5.4 (sparse-aware packing: valid tokens only, no
+ * padding); sec. 8.3.A (strict per-expert capacity; assignments over it
+ * are taken in order and here dropped).
+ *
+ *   topk_idx       [T, k] int32 from moe_gate (ids outside [0, E) are
+ *                  recorded as MOE_ERR_DEVICE_DATA and treated as dropped).
+ *   expert_counts  [E] int32 from moe_gate (must match topk_idx; a
+ *                  mismatch is recorded as MOE_ERR_DEVICE_DATA).
+ *   P              logical partitions; partition p = experts
+ *                  [p*E/P, (p+1)*E/P), a contiguous slice of the packed rows.
+ *   capacity       per-expert row limit; <= 0 means none.  Within an expert
+ *                  the first `capacity` assignments in token order are kept.
+ *   gates_or_null  [T, k] fp32; if given, dropped slots are set to 0.
+ *   L              host struct with caller-allocated device arrays
+ *                  (see moe_layout); scalar members are filled in here.
+ *   ws, ws_bytes   workspace (>= moe_workspace_size(T, E, k, P)), the same
+ *                  one moe_gate used is fine.
+ * Packed row of a kept assignment: offsets[e] + (its rank within expert e).
+ * R = offsets[E] stays on the device; size packed buffers with L->r_max.
+ */
+moe_status moe_dispatch_layout(const int32_t *topk_idx, const int32_t *expert_counts,
+                               int T, int E, int k, int P, int capacity,
+                               float *gates_or_null, moe_layout *L,
+                               void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_dispatch -- permute and pack token hidden states into the
+ * expert-contiguous send buffer ([P4] sec. 7 Dispatch detail), optionally
+ * as per-token affine FP8 ([P1] sec. 3.1: per-token min/max, affine map).
+ *
+ *   x       [T, H] bf16.
+ *   fp8 = 0: packed [r_max, H] bf16; row r = x[src_pos[r] / k] bit-exactly.
+ *   fp8 = 1: packed [r_max, H] uint8 e4m3 codes, scales [r_max, 2] fp32
+ *            (scale, zero) of the row's token, with (fp32, in this order)
+ *            mx, mn = max and min of the row (-0 < +0),
+ *            zero = (mx + mn) * 0.5, scale = (mx - mn) / 896,
+ *            code = e4m3 satfinite RNE((x - zero) / scale);
+ *            a constant row has scale 0 and all-zero codes.
+ *            Dequantise as zero + scale * e4m3_value(code).  x must be finite.
+ *   Rows >= R are not written.
+ */
+moe_status moe_dispatch(const void *x, int T, int H, const moe_layout *L, int fp8,
+                        void *packed, float *scales, moe_stream_t stream);
+
+/*
+ * moe_combine -- gather the expert outputs back into token order and
+ * gate-weight them ([P4] sec. 7 "Combine": weighted sum of each token's
+ * top-k expert outputs, placed by the saved routing metadata), adding the
+ * shared experts' outputs with weight 1 ([P4] sec. 8.2.B; [P2] sec. 2.1).
+ *
+ *   expert_out  [r_max, H] bf16, packed-row layout (row r = output of the
+ *               expert for assignment src_pos[r]).
+ *   gates       [T, k] fp32 (as left by the layout: dropped slots are 0).
+ *   shared_out  [Ks, T, H] bf16 or NULL when Ks == 0.
+ *   y       out [T, H] bf16:
+ *     acc = 0; for kept j ascending: acc = fmaf(g[t,j], eo[dst_row[t,j]], acc);
+ *     for s ascending: acc = acc + shared[s,t]; y = bf16 round-to-nearest-even(acc).
+ */
+moe_status moe_combine(const void *expert_out, const moe_layout *L, const float *gates,
+                       const void *shared_out, int Ks, int T, int H, void *y,
+                       moe_stream_t stream);
+
+/* Synchronise `stream`, return the device status recorded in `ws` since the
+ * last call (MOE_OK if none) and clear it. */
+moe_status moe_get_status(void *ws, moe_stream_t stream);
+
+/* Static description of a status code. */
+const char *moe_status_string(moe_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_ROUTE_H */

@@ -1,0 +1,80 @@
+"""CPU-only checks of the C-ABI library: it builds, loads, exports every
+entry point include/moe_route.h declares, and its host-side size queries
+and argument checks behave as documented (no CUDA call is reached)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import combine_moe_gate_warp_gb300 as pkg
+    pkg.build()
+    from combine_moe_gate_warp_gb300 import abi
+    return abi.lib()
+
+
+def _declared():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"^[A-Za-z_][\w \*]*?\b(moe_\w+)\s*\(", src, flags=re.M))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert {"moe_gate", "moe_dispatch_layout", "moe_dispatch", "moe_combine", "moe_get_status",
+            "moe_workspace_size", "moe_workspace_init", "moe_rows_max", "moe_status_string"} <= names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared but not exported"
+
+
+def test_workspace_and_rows_queries(lib):
+    from combine_moe_gate_warp_gb300 import abi
+    assert abi.moe_workspace_size(16384, 16, 2, 4) == 4096 + 32 * 16 * 8
+    assert abi.moe_workspace_size(262144, 64, 8, 8) == 4096 + 2048 * 64 * 8
+    assert abi.moe_workspace_size(100, 16, 2, 3) == 0   # P does not divide E
+    assert abi.moe_workspace_size(100, 300, 2, 4) == 0  # E too large
+    assert abi.moe_rows_max(262144, 64, 8, 40960) == 2097152
+    assert abi.moe_rows_max(100, 8, 2, 5) == 40
+    assert abi.moe_rows_max(100, 8, 2, 0) == 200
+    assert abi.moe_rows_max(100, 8, 9, 0) == -1         # k > E
+
+
+def test_argument_checks_return_before_any_cuda_call(lib):
+    from combine_moe_gate_warp_gb300 import abi
+    P = ctypes.c_void_p
+    fake = P(1 << 20)
+    # k = 0, E too large, mode invalid, T < 0
+    assert lib.moe_gate(fake, 10, 8, 0, 0, fake, fake, fake, fake, fake, fake, 1 << 20, None) == abi.MOE_ERR_UNSUPPORTED
+    assert lib.moe_gate(fake, 10, 300, 2, 0, fake, fake, fake, fake, fake, fake, 1 << 20, None) == abi.MOE_ERR_UNSUPPORTED
+    assert lib.moe_gate(fake, 10, 8, 2, 9, fake, fake, fake, fake, fake, fake, 1 << 20, None) == abi.MOE_ERR_INVALID_ARG
+    assert lib.moe_gate(fake, -1, 8, 2, 0, fake, fake, fake, fake, fake, fake, 1 << 20, None) == abi.MOE_ERR_INVALID_ARG
+    assert lib.moe_gate(P((1 << 20) + 4), 10, 8, 2, 0, fake, fake, fake, fake, fake, fake, 1 << 20, None) == abi.MOE_ERR_INVALID_ARG
+    assert lib.moe_gate(fake, 10, 8, 2, 0, fake, fake, fake, fake, fake, fake, 100, None) == abi.MOE_ERR_WORKSPACE_TOO_SMALL
+    L = abi.moe_layout()
+    assert lib.moe_dispatch_layout(fake, fake, 10, 8, 2, 3, 0, None, ctypes.byref(L), fake, 1 << 20, None) == abi.MOE_ERR_UNSUPPORTED
+    assert lib.moe_dispatch_layout(fake, fake, 10, 8, 2, 4, 0, None, ctypes.byref(L), fake, 1 << 20, None) == abi.MOE_ERR_INVALID_ARG
+    assert lib.moe_dispatch(fake, 10, 64, None, 0, fake, None, None) == abi.MOE_ERR_INVALID_ARG
+    assert lib.moe_combine(fake, None, fake, None, 0, 10, 64, fake, None) == abi.MOE_ERR_INVALID_ARG
+    assert lib.moe_get_status(None, None) == abi.MOE_ERR_INVALID_ARG
+    assert lib.moe_status_string(5) == b"device wait timed out"
+
+
+def test_binding_names_match_the_c_abi():
+    from combine_moe_gate_warp_gb300 import abi
+    for n in ("moe_gate", "moe_dispatch_layout", "moe_dispatch", "moe_combine", "moe_get_status",
+              "moe_workspace_size", "moe_workspace_init", "moe_rows_max"):
+        assert callable(getattr(abi, n))
+    # the struct mirrors the header's field order
+    hdr = open(os.path.join(ROOT, "include", "moe_route.h")).read()
+    body = hdr[hdr.index("typedef struct moe_layout {"):hdr.index("} moe_layout;")]
+    fields = re.findall(r"\*?(\w+)(?:,|;)", re.sub(r"/\*.*?\*/", "", body, flags=re.S))
+    assert [f for f, _ in abi.moe_layout._fields_] == fields

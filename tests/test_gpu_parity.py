@@ -1,0 +1,234 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the CPU
+oracle on the same seeded inputs.
+
+Bit-exact: top-k ids, counts, offsets, permutation, capacity drops, packed
+bf16 rows, FP8 codes and scales, and the combine in its pinned fp32 order.
+Gate weights within 1e-6 absolute (fp32 vs the fp64 oracle); aux loss and
+entropy within 1e-9 (fp64 from the same integer counts); the combine also
+within one bf16 ulp of the fp64 reference plus the fp32 summation bound.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_moe_gate_warp_gb300 import workloads
+from gpu_util import (bits, check_combine, check_dispatch, check_gate, check_layout, run_gpu,
+                      sample_rows)
+
+pytestmark = pytest.mark.gpu
+
+W = workloads.WORKLOADS
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import combine_moe_gate_warp_gb300 as pkg
+    pkg.build()
+    oracle.build()
+    torch.cuda.init()
+
+
+def _full_check(w, rows_sample=None, token_sample=None, seed=7):
+    rng = np.random.default_rng(seed)
+    inp = workloads.make_inputs(w, "cuda")
+    plan, gates_pre, R, eo, status = run_gpu(w, inp)
+    assert status == 0, f"device status {status}"
+    logits = inp["logits"].cpu().numpy()
+    idx, counts = check_gate(w, plan, gates_pre, logits)
+    assert counts.sum() == w.T * w.k
+    L = check_layout(w, plan, idx, gates_pre)
+    assert L["R"] == R
+    x_bits = bits(inp["x"])
+    rows = np.arange(R, dtype=np.int64) if rows_sample is None else sample_rows(R, rng, rows_sample)
+    check_dispatch(w, plan, L, x_bits, rows)
+    toks = np.arange(w.T, dtype=np.int64) if token_sample is None else sample_rows(w.T, rng, token_sample)
+    frac = check_combine(w, plan, L, eo, inp["shared"], toks)
+    return plan, L, frac
+
+
+# --- small cases: every output compared element by element ----------------
+# Token counts span several gate/layout tiles with a ragged tail.
+SMALL = [
+    W["tiny"],
+    W["v2_top2"].scaled(1000),
+    W["fine_shared"].scaled(333),
+    W["fp8_skewed"].scaled(1500),
+    W["prefill_cap"].scaled(700),
+]
+
+
+@pytest.mark.parametrize("w", SMALL, ids=[w.name for w in SMALL])
+def test_small_workloads_exact(w):
+    plan, L, frac = _full_check(w)
+    if w.identity_experts:
+        assert np.array_equal(bits(plan.y), bits(workloads.make_x(w, "cuda")))
+
+
+# --- the full-size workloads: gate and layout in full, dispatch and combine
+# on sampled rows/tokens (first, last and random) --------------------------
+@pytest.mark.parametrize("name", ["tiny", "v2_top2", "fine_shared", "fp8_skewed", "prefill_cap"])
+def test_full_size_workloads(name):
+    w = W[name]
+    plan, L, frac = _full_check(w, rows_sample=600, token_sample=600)
+    if name == "prefill_cap":
+        assert L["dropped"] > 0 and np.all(L["counts"] <= w.capacity)
+
+
+# --- edge cases --------------------------------------------------------------
+def _custom(T, H, E, k, P, mode=0, fp8=False, Ks=0, cap_factor=0.0, seed=99, **kw):
+    return workloads.Workload(f"edge_T{T}_E{E}_k{k}", T=T, H=H, E=E, k=k, P=P, mode=mode, fp8=fp8, Ks=Ks,
+                              capacity_factor=cap_factor, seed=seed, **kw)
+
+
+EDGE = [
+    _custom(1, 8, 8, 2, 4),                    # one token, smallest H
+    _custom(3, 16, 8, 8, 8),                   # k == E
+    _custom(257, 64, 256, 16, 256),            # largest E and k, one expert per partition
+    _custom(2049, 24, 5, 3, 1, mode=1),        # odd E, P = 1, many tiles
+    _custom(129, 16, 8, 1, 2, fp8=True),       # k = 1, smallest FP8 row
+    _custom(300, 8200, 16, 2, 4),              # H > 8192: looped copy
+    _custom(64, 16384, 8, 2, 2, fp8=True),     # largest FP8 row
+    _custom(500, 40, 12, 4, 3, Ks=3, mode=1),  # ragged H / 8, three shared experts
+]
+
+
+@pytest.mark.parametrize("w", EDGE, ids=[w.name for w in EDGE])
+def test_edge_shapes(w):
+    _full_check(w)
+
+
+def test_empty_batch():
+    w = _custom(0, 64, 8, 2, 4)
+    inp = workloads.make_inputs(w, "cuda")
+    plan, gates_pre, R, eo, status = run_gpu(w, inp)
+    assert status == 0 and R == 0
+    assert plan.expert_counts.cpu().tolist() == [0] * 8
+    assert plan.aux_loss.item() == 0.0 and plan.entropy.item() == 0.0
+    assert plan.layout.offsets.cpu().tolist() == [0] * 9
+    assert plan.layout.part_tokens.cpu().tolist() == [0] * 4
+
+
+def _run_with_logits(w, logits):
+    inp = dict(logits=logits.contiguous(), x=workloads.make_x(w, "cuda"), shared=None)
+    plan, gates_pre, R, eo, status = run_gpu(w, inp)
+    assert status == 0
+    idx, _ = check_gate(w, plan, gates_pre, inp["logits"].cpu().numpy())
+    L = check_layout(w, plan, idx, gates_pre)
+    check_dispatch(w, plan, L, bits(inp["x"]), np.arange(R, dtype=np.int64))
+    check_combine(w, plan, L, eo, None, np.arange(w.T, dtype=np.int64))
+    return plan, L
+
+
+def test_ties_and_signed_zeros():
+    w = _custom(1100, 32, 16, 4, 4)
+    g = torch.Generator(device="cuda").manual_seed(5)
+    logits = torch.randint(-2, 3, (w.T, w.E), generator=g, device="cuda").float()
+    logits[torch.rand((w.T, w.E), generator=g, device="cuda") < 0.2] = -0.0
+    _run_with_logits(w, logits)
+
+
+def test_all_tokens_one_expert_capacity_hit_exactly_and_exceeded():
+    """Every token picks experts 5 then 2; capacity at, one below, and far
+    below the per-expert load."""
+    from combine_moe_gate_warp_gb300 import RoutePlan
+    from gpu_util import shape_of
+    w = workloads.Workload("hot", T=1000, H=32, E=8, k=2, P=4, seed=3)
+    logits = torch.zeros((w.T, w.E), device="cuda")
+    logits[:, 5] = 4.0
+    logits[:, 2] = 3.0
+    x = workloads.make_x(w, "cuda")
+    for cap in (1000, 999, 1):
+        shp = shape_of(w)
+        shp.capacity = cap
+        plan = RoutePlan(shp, "cuda")
+        plan.gate(logits)
+        gpre = plan.gates.clone()
+        plan.dispatch_layout()
+        plan.dispatch(x)
+        assert plan.status() == 0
+        idx = plan.topk_idx.cpu().numpy()
+        assert np.all(idx == [5, 2])
+        L = oracle.layout(idx, 8, 4, cap, gates_f32=gpre.cpu().numpy())
+        assert np.array_equal(plan.layout.dst_row.cpu().numpy(), L["dst_row"])
+        assert np.array_equal(plan.layout.src_pos.cpu().numpy()[:L["R"]], L["src_pos"])
+        assert np.array_equal(plan.layout.part_tokens.cpu().numpy(), L["part_tokens"])
+        assert int(plan.layout.dropped.item()) == 2 * 1000 - 2 * min(cap, 1000)
+        wc = workloads.Workload("hot", T=1000, H=32, E=8, k=2, P=4, seed=3)
+        check_dispatch(wc, plan, L, bits(x), np.arange(L["R"], dtype=np.int64))
+
+
+def test_fp8_constant_and_signed_zero_rows():
+    w = _custom(6, 32, 8, 2, 4, fp8=True)
+    inp = workloads.make_inputs(w, "cuda")
+    x = inp["x"]
+    x[0] = 0.75                       # constant row
+    x[1] = 0.0
+    x[1, ::2] = -0.0                  # +-0 mix: max +0, min -0, flat
+    x[2] = -0.0                       # all -0: zero word is -0
+    x[3, :] = 1.0
+    x[3, 7] = -448.0                  # min hits -448 exactly
+    plan, gates_pre, R, eo, status = run_gpu(w, inp)
+    assert status == 0
+    idx, _ = check_gate(w, plan, gates_pre, inp["logits"].cpu().numpy())
+    L = check_layout(w, plan, idx, gates_pre)
+    check_dispatch(w, plan, L, bits(x), np.arange(R, dtype=np.int64))
+
+
+def test_fp8_bf16_pattern_sweep():
+    """Every finite bf16 value x, placed in rows headed by (M, -M) with
+    M = 448 * 2^m, so that (unless x itself exceeds M) scale = 2^m and
+    v = x / 2^m is exact; m runs so that v's binary exponent covers
+    [-12, 8]: every rounding regime of e4m3 (subnormal ties, normal ties,
+    carries into the next binade)."""
+    pats = np.arange(65536, dtype=np.uint32)
+    f = (pats << 16).view(np.float32)
+    pats = pats[np.isfinite(f)]
+    f = f[np.isfinite(f)]
+    ex = np.where(f == 0, -140, np.floor(np.log2(np.abs(np.where(f == 0, 1, f).astype(np.float64)))))
+    vals, heads = [], []
+    for s in range(-12, 9):
+        m = ex - s
+        ok = (m >= -139) & (m <= 118)
+        for mm in np.unique(m[ok]):
+            sel = pats[ok & (m == mm)]
+            M = np.float32(448.0 * 2.0 ** mm)
+            Mb = np.uint32(M.view(np.uint32)) >> 16
+            assert (np.uint32(Mb) << 16).view(np.float32) == M
+            for c in range(0, sel.size, 62):
+                vals.append(sel[c:c + 62])
+                heads.append(Mb)
+    T = len(vals)
+    H = 64
+    rows = np.zeros((T, H), np.uint16)
+    for i, (v, Mb) in enumerate(zip(vals, heads)):
+        rows[i, 0] = Mb
+        rows[i, 1] = Mb | 0x8000
+        rows[i, 2:2 + v.size] = v
+        rows[i, 2 + v.size:] = 0
+    w = _custom(T, H, 8, 1, 1, fp8=True)
+    x = torch.from_numpy(rows.view(np.int16)).cuda().view(torch.bfloat16)
+    inp = dict(logits=workloads.make_logits(w, "cuda"), x=x, shared=None)
+    plan, gates_pre, R, eo, status = run_gpu(w, inp)
+    assert status == 0 and R == T
+    L = oracle.layout(plan.topk_idx.cpu().numpy(), 8, 1, 0)
+    check_dispatch(w, plan, L, rows, np.arange(R, dtype=np.int64))
+
+
+def test_repeated_calls_reuse_workspace():
+    """The workspace returns to a clean state after every call: three passes
+    over different inputs on one plan match fresh oracle runs."""
+    from gpu_util import shape_of
+    from combine_moe_gate_warp_gb300 import RoutePlan
+    w = W["prefill_cap"].scaled(3000)
+    plan = RoutePlan(shape_of(w), "cuda")
+    for rep in range(3):
+        wr = workloads.Workload(**{**w.__dict__, "seed": 500 + rep})
+        inp = workloads.make_inputs(wr, "cuda")
+        plan.gate(inp["logits"])
+        gpre = plan.gates.clone()
+        plan.dispatch_layout()
+        plan.dispatch(inp["x"])
+        assert plan.status() == 0
+        idx, _ = check_gate(wr, plan, gpre, inp["logits"].cpu().numpy())
+        check_layout(wr, plan, idx, gpre)
