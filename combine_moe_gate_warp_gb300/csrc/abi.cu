@@ -107,7 +107,7 @@ moe_status moe_dispatch_layout(const int32_t *topk_idx, const int32_t *expert_co
 
 static moe_status check_layout(const moe_layout *L, int T)
 {
-    if (!L || !L->ws || (T > 0 && !L->dst_row)) return MOE_ERR_INVALID_ARG;
+    if (!L || !L->ws || !L->offsets || (T > 0 && !L->dst_row)) return MOE_ERR_INVALID_ARG;
     if (L->T != T) return MOE_ERR_INVALID_ARG;
     return check_sizes(L->T, L->E, L->k);
 }

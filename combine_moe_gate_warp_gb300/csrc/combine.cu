@@ -59,9 +59,13 @@ __device__ __forceinline__ unsigned pack_bf16x2(float lo, float hi)
 template <int K, int U>
 __global__ void __launch_bounds__(kCombThreads)
 combine_kernel(const uint4 *__restrict__ eo, const float *__restrict__ gates,
-               const int32_t *__restrict__ dst_row, int r_max, const uint4 *__restrict__ shared,
-               int Ks, long long T, int nvec, uint4 *__restrict__ y, void *ws)
+               const int32_t *__restrict__ dst_row, int r_max, const int32_t *__restrict__ R_ptr,
+               const uint4 *__restrict__ shared, int Ks, long long T, int nvec, uint4 *__restrict__ y,
+               void *ws)
 {
+    // rows at or beyond R (= offsets[E]) are reported and skipped, so an
+    // expert-output buffer sized to R is never over-read
+    const int rows_valid = min(r_max, __ldg(R_ptr));
     for (long long t = blockIdx.x; t < T; t += gridDim.x) {
         int rows[K];
         float g[K];
@@ -69,7 +73,7 @@ combine_kernel(const uint4 *__restrict__ eo, const float *__restrict__ gates,
         for (int j = 0; j < K; ++j) {
             rows[j] = __ldg(dst_row + t * K + j);
             g[j] = __ldg(gates + t * K + j);
-            if (rows[j] >= r_max) {
+            if (rows[j] >= rows_valid) {
                 if (threadIdx.x == 0) record_status(ws, MOE_ERR_DEVICE_DATA);
                 rows[j] = -1;
             }
@@ -124,7 +128,8 @@ combine_kernel(const uint4 *__restrict__ eo, const float *__restrict__ gates,
 
 template <int K>
 cudaError_t launch_k(const uint4 *eo, const float *gates, const int32_t *dst_row, int r_max,
-                     const uint4 *shared, int Ks, int T, int nvec, uint4 *y, void *ws, cudaStream_t s)
+                     const int32_t *R_ptr, const uint4 *shared, int Ks, int T, int nvec, uint4 *y,
+                     void *ws, cudaStream_t s)
 {
     const long long cap = 1LL << 30;
     const unsigned grid = (unsigned)(T < cap ? T : cap);
@@ -132,7 +137,8 @@ cudaError_t launch_k(const uint4 *eo, const float *gates, const int32_t *dst_row
     // keep K*U row loads (16 B each) <= 8 per thread: <= 32 data registers
     constexpr int kUMax = (8 / K) < 1 ? 1 : (8 / K);
 #define MOE_COMBINE(UU) \
-    combine_kernel<K, UU><<<grid, kCombThreads, 0, s>>>(eo, gates, dst_row, r_max, shared, Ks, T, nvec, y, ws)
+    combine_kernel<K, UU><<<grid, kCombThreads, 0, s>>>(eo, gates, dst_row, r_max, R_ptr, shared, Ks, T, \
+                                                        nvec, y, ws)
     if (per_thread <= 1 || kUMax == 1) {
         MOE_COMBINE(1);
     } else if (per_thread <= 2 || kUMax == 2) {
@@ -158,7 +164,9 @@ cudaError_t launch_combine(const void *eo, const moe_layout *L, const float *gat
     const int nvec = H / 8;
     switch (L->k) {
 #define MOE_COMBINE_CASE(KK) \
-    case KK: return launch_k<KK>(ep, gates, L->dst_row, L->r_max, sp, Ks, T, nvec, yp, L->ws, s);
+    case KK:                                                                                       \
+        return launch_k<KK>(ep, gates, L->dst_row, L->r_max, L->offsets + L->E, sp, Ks, T, nvec, yp, \
+                            L->ws, s);
         MOE_COMBINE_CASE(1) MOE_COMBINE_CASE(2) MOE_COMBINE_CASE(3) MOE_COMBINE_CASE(4)
         MOE_COMBINE_CASE(5) MOE_COMBINE_CASE(6) MOE_COMBINE_CASE(7) MOE_COMBINE_CASE(8)
         MOE_COMBINE_CASE(9) MOE_COMBINE_CASE(10) MOE_COMBINE_CASE(11) MOE_COMBINE_CASE(12)

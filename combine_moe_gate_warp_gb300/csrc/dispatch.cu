@@ -28,14 +28,16 @@ namespace {
 constexpr int kDispThreads = 128;
 
 // Kept destination rows of token t, compacted in slot order into s_rows.
+// Rows at or beyond R (= offsets[E], the rows the layout produced) are
+// reported and skipped, so packed buffers sized to R are never overrun.
 __device__ __forceinline__ int load_token_rows(const int32_t *__restrict__ dst_row, long long t, int k,
-                                               int r_max, int *s_rows, int *s_n, void *ws)
+                                               int rows_valid, int *s_rows, int *s_n, void *ws)
 {
     if (threadIdx.x < 32) {
         int r = -1;
         if ((int)threadIdx.x < k) {
             r = dst_row[t * k + threadIdx.x];
-            if (r >= r_max) {
+            if (r >= rows_valid) {
                 record_status(ws, MOE_ERR_DEVICE_DATA);
                 r = -1;
             }
@@ -51,12 +53,14 @@ __device__ __forceinline__ int load_token_rows(const int32_t *__restrict__ dst_r
 template <int U>
 __global__ void __launch_bounds__(kDispThreads)
 dispatch_bf16_kernel(const uint4 *__restrict__ x, long long T, int nvec, int k,
-                     const int32_t *__restrict__ dst_row, int r_max, uint4 *__restrict__ packed, void *ws)
+                     const int32_t *__restrict__ dst_row, int r_max, const int32_t *__restrict__ R_ptr,
+                     uint4 *__restrict__ packed, void *ws)
 {
     __shared__ int s_rows[MOE_MAX_TOPK];
     __shared__ int s_n;
+    const int rows_valid = min(r_max, __ldg(R_ptr));
     for (long long t = blockIdx.x; t < T; t += gridDim.x) {
-        const int n = load_token_rows(dst_row, t, k, r_max, s_rows, &s_n, ws);
+        const int n = load_token_rows(dst_row, t, k, rows_valid, s_rows, &s_n, ws);
         const uint4 *src = x + t * nvec;
         for (int c0 = 0; c0 < nvec; c0 += kDispThreads * U) {
             uint4 v[U];
@@ -107,15 +111,16 @@ __device__ __forceinline__ unsigned quant_pair(unsigned w, float zero, float sca
 template <int CPT>
 __global__ void __launch_bounds__(kDispThreads)
 dispatch_fp8_kernel(const uint4 *__restrict__ x, long long T, int npairs, int k,
-                    const int32_t *__restrict__ dst_row, int r_max, uint4 *__restrict__ packed,
-                    float2 *__restrict__ scales, void *ws)
+                    const int32_t *__restrict__ dst_row, int r_max, const int32_t *__restrict__ R_ptr,
+                    uint4 *__restrict__ packed, float2 *__restrict__ scales, void *ws)
 {
     __shared__ int s_rows[MOE_MAX_TOPK];
     __shared__ int s_n;
     __shared__ int s_max[kDispThreads / 32], s_min[kDispThreads / 32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int rows_valid = min(r_max, __ldg(R_ptr));
     for (long long t = blockIdx.x; t < T; t += gridDim.x) {
-        const int n = load_token_rows(dst_row, t, k, r_max, s_rows, &s_n, ws);
+        const int n = load_token_rows(dst_row, t, k, rows_valid, s_rows, &s_n, ws);
         const uint4 *src = x + t * (2LL * npairs);
         uint4 v[CPT][2];
         int kmax = INT_MIN, kmin = INT_MAX;
@@ -206,7 +211,7 @@ cudaError_t launch_dispatch_bf16(const void *x, int T, int H, const moe_layout *
     uint4 *pp = static_cast<uint4 *>(packed);
 #define MOE_DISPATCH_BF16(UU)                                                                     \
     dispatch_bf16_kernel<UU><<<grid, kDispThreads, 0, s>>>(xp, T, nvec, L->k, L->dst_row,         \
-                                                           L->r_max, pp, L->ws)
+                                                           L->r_max, L->offsets + L->E, pp, L->ws)
     if (per_thread <= 1) MOE_DISPATCH_BF16(1);
     else if (per_thread <= 2) MOE_DISPATCH_BF16(2);
     else if (per_thread <= 3) MOE_DISPATCH_BF16(3);
@@ -230,7 +235,7 @@ cudaError_t launch_dispatch_fp8(const void *x, int T, int H, const moe_layout *L
     float2 *sp = reinterpret_cast<float2 *>(scales);
 #define MOE_DISPATCH_FP8(CC)                                                                      \
     dispatch_fp8_kernel<CC><<<grid, kDispThreads, 0, s>>>(xp, T, npairs, L->k, L->dst_row,        \
-                                                          L->r_max, pp, sp, L->ws)
+                                                          L->r_max, L->offsets + L->E, pp, sp, L->ws)
     if (per_thread <= 1) MOE_DISPATCH_FP8(1);
     else if (per_thread <= 2) MOE_DISPATCH_FP8(2);
     else if (per_thread <= 4) MOE_DISPATCH_FP8(4);
