@@ -276,6 +276,13 @@ def host_inputs(w, inputs, eo):
     return d
 
 
+def rank_workload(base, rank: int):
+    """Data-parallel sharding: every rank routes its own batch of the same
+    shape (its own seed); nothing on the data path is exchanged."""
+    from combine_moe_gate_warp_gb300 import workloads
+    return workloads.Workload(**{**base.__dict__, "seed": base.seed + 7919 * rank})
+
+
 def config_of(w, world):
     return {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "P": w.P,
             "gate": "softmax_topk" if w.mode else "topk_softmax",
@@ -344,7 +351,7 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     build()
     base = workloads.WORKLOADS[args.workload]
-    w = workloads.Workload(**{**base.__dict__, "seed": base.seed + 7919 * rank})  # own batch per rank
+    w = rank_workload(base, rank)
 
     inputs = workloads.make_inputs(w, dev)
     shape = RouteShape(T=w.T, H=w.H, E=w.E, k=w.k, P=w.P, mode=w.mode, fp8=w.fp8, Ks=w.Ks,
