@@ -31,6 +31,7 @@ MOE_MAX_EXPERTS = 256
 MOE_MAX_TOPK = 16
 MOE_MAX_SHARED = 8
 MOE_MAX_H_FP8 = 16384
+MOE_NOALLOC_SCRATCH_BYTES = 2 << 20
 
 _LIB = None
 
@@ -81,6 +82,8 @@ def lib():
     L.moe_gate.restype = I
     L.moe_dispatch_layout.argtypes = [P, P, I, I, I, I, I, P, ctypes.POINTER(moe_layout), P, SZ, P]
     L.moe_dispatch_layout.restype = I
+    L.moe_dispatch_layout_noalloc.argtypes = [P, P, I, I, I, I, I, P, ctypes.POINTER(moe_layout), P]
+    L.moe_dispatch_layout_noalloc.restype = I
     L.moe_dispatch.argtypes = [P, I, I, ctypes.POINTER(moe_layout), I, P, P, P]
     L.moe_dispatch.restype = I
     L.moe_combine.argtypes = [P, ctypes.POINTER(moe_layout), P, P, I, I, I, P, P]
@@ -166,6 +169,18 @@ def moe_dispatch_layout(topk_idx, expert_counts, T: int, E: int, k: int, P: int,
                                      _ptr(gates_or_null, torch.float32, "gates"),
                                      ctypes.byref(layout.c), _ptr(ws, name="ws"), _nbytes(ws),
                                      _stream(stream)), "moe_dispatch_layout")
+
+
+def moe_dispatch_layout_noalloc(topk_idx, expert_counts, T: int, E: int, k: int, P: int,
+                                capacity: int, gates_or_null, layout: "Layout", stream=None) -> None:
+    """moe_dispatch_layout without a workspace argument: the library's own
+    fixed scratch is used (no device allocation anywhere in the call)."""
+    _check(lib().moe_dispatch_layout_noalloc(_ptr(topk_idx, torch.int32, "topk_idx"),
+                                             _ptr(expert_counts, torch.int32, "expert_counts"),
+                                             T, E, k, P, capacity,
+                                             _ptr(gates_or_null, torch.float32, "gates"),
+                                             ctypes.byref(layout.c), _stream(stream)),
+           "moe_dispatch_layout_noalloc")
 
 
 def moe_dispatch(x, T: int, H: int, layout: "Layout", fp8: int, packed, scales=None,

@@ -159,6 +159,40 @@ moe_status moe_dispatch_layout(const int32_t *topk_idx, const int32_t *expert_co
                                void *ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * moe_dispatch_layout_noalloc -- the same layout as moe_dispatch_layout,
+ * for callers that cannot allocate device memory.  The source pages have no
+ * counterpart to this entry point; it exists for integration only.
+ *
+ * Some callers are not allowed to allocate: a plug-in running inside a
+ * host framework that owns every byte of device memory through its own
+ * pool, or a latency-critical loop that must not enter the CUDA allocator
+ * (cudaMalloc can synchronise the device and take unbounded time) after
+ * start-up.  This variant takes no workspace: it uses a scratch array
+ * compiled into the library (a file-scope static __device__ buffer of
+ * MOE_NOALLOC_SCRATCH_BYTES bytes, held by every GPU that loads the library
+ * until the process exits).  The caller still provides all inputs and the
+ * moe_layout output arrays.
+ *
+ *   Arguments and outputs: as moe_dispatch_layout, minus ws / ws_bytes.
+ *   L->ws is set to the scratch's device address, so moe_dispatch,
+ *   moe_combine and moe_get_status(L->ws, stream) work as usual.
+ *   Sizes whose moe_workspace_size(T, E, k, P) exceeds
+ *   MOE_NOALLOC_SCRATCH_BYTES are rejected with MOE_ERR_WORKSPACE_TOO_SMALL
+ *   before anything is enqueued.
+ *   The first call on each device looks up the scratch's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.  Every call clears the scratch counters that
+ *   must start at zero.  All calls in the process share the one array, so
+ *   calls that may overlap on the GPU (different streams, or several host
+ *   threads) race with each other: serialise them.
+ *   No cudaMalloc, cudaFree or other allocating routine is called.
+ */
+#define MOE_NOALLOC_SCRATCH_BYTES (2u << 20)
+moe_status moe_dispatch_layout_noalloc(const int32_t *topk_idx, const int32_t *expert_counts,
+                                       int T, int E, int k, int P, int capacity,
+                                       float *gates_or_null, moe_layout *L, moe_stream_t stream);
+
+/*
  * moe_dispatch -- permute and pack token hidden states into the
  * expert-contiguous send buffer ([P4] sec. 7 Dispatch detail), optionally
  * as per-token affine FP8 ([P1] sec. 3.1: per-token min/max, affine map).
