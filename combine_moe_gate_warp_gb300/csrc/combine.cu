@@ -9,22 +9,56 @@
 // all-to-all, outputs added); "DeepSeek MoE sync tax" sec. 2.1 (K_s shared
 // experts).
 //
-// Design (sm_103a): gather form -- y is written exactly once and every
-// kept expert-output row is read exactly once (each packed row belongs to
-// one assignment), so the traffic is the algorithmic minimum.  One block
-// per token; each thread owns U 16-byte column chunks, issues all K*U row
-// loads before any arithmetic (K is a template parameter so the slot loop
-// unrolls into independent loads), then accumulates in fp32 with explicit
-// round-to-nearest FMA/add intrinsics in the pinned order (kept slots
-// ascending, then shared experts ascending) and rounds once to bf16.
+// Design (sm_103a): gather form -- y is written exactly once and every kept
+// expert-output row is read exactly once, so the traffic is the algorithmic
+// minimum.  A persistent grid (as many blocks as fit on the SMs) works
+// through units = (token, column chunk of the row).  Each block owns a ring
+// of S shared-memory stages and is warp-specialised: a producer warp reads
+// the routing metadata of 32 upcoming units in one round trip and fills
+// stages with 1-D bulk copies (cp.async.bulk, the TMA engine) of the kept
+// expert-output chunks and the shared-expert chunks, completing on the
+// stage's "full" mbarrier; four consumer warps wait on "full", accumulate
+// in fp32 with explicit round-to-nearest FMA/add in the pinned order (kept
+// slots ascending, then shared experts ascending), round once to bf16,
+// store y with 16-byte coalesced stores, and release the stage on its
+// "empty" mbarrier.  No block-wide barrier sits in the loop, and the bytes
+// in flight per SM are bounded by shared memory, not registers.  Every
+// mbarrier wait is bounded; on expiry the waiter records MOE_ERR_TIMEOUT,
+// and the producer always waits (bounded) for its copies still in flight
+// before it returns.
 #include <cuda_bf16.h>
 
+#include <mutex>
+#include <unordered_map>
+
 #include "common.cuh"
+#include "tma.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kCombThreads = 128;
+constexpr int kMaxStages = 8;
+constexpr int kStageBudget = 108 * 1024;  // dynamic shared memory per block (two blocks per SM)
+
+struct CombineArgs {
+    const char *eo;        // [rows, H] bf16
+    const float *gates;    // [T, K]
+    const int32_t *dst_row;
+    const int32_t *R_ptr;  // offsets + E: rows the layout produced
+    const char *shared;    // [Ks, T, H] bf16 or null
+    char *y;               // [T, H] bf16
+    void *ws;
+    long long T;
+    long long units;       // T * nch
+    int r_max;
+    int Ks;
+    int rowbytes;          // H * 2
+    int nch;               // column chunks per row
+    int cb;                // chunk bytes (multiple of 16)
+    int stages;
+    int slots;             // K + Ks
+};
 
 __device__ __forceinline__ void fma8(float (&acc)[8], float g, const uint4 &v)
 {
@@ -56,99 +90,195 @@ __device__ __forceinline__ unsigned pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<unsigned *>(&h);
 }
 
-template <int K, int U>
-__global__ void __launch_bounds__(kCombThreads)
-combine_kernel(const uint4 *__restrict__ eo, const float *__restrict__ gates,
-               const int32_t *__restrict__ dst_row, int r_max, const int32_t *__restrict__ R_ptr,
-               const uint4 *__restrict__ shared, int Ks, long long T, int nvec, uint4 *__restrict__ y,
-               void *ws)
+// Bounded wait on a stage barrier.  Returns false if the bound expired.
+__device__ __forceinline__ bool wait_stage(uint64_t *bar, uint32_t parity)
 {
-    // rows at or beyond R (= offsets[E]) are reported and skipped, so an
-    // expert-output buffer sized to R is never over-read
-    const int rows_valid = min(r_max, __ldg(R_ptr));
-    for (long long t = blockIdx.x; t < T; t += gridDim.x) {
-        int rows[K];
-        float g[K];
-#pragma unroll
-        for (int j = 0; j < K; ++j) {
-            rows[j] = __ldg(dst_row + t * K + j);
-            g[j] = __ldg(gates + t * K + j);
-            if (rows[j] >= rows_valid) {
-                if (threadIdx.x == 0) record_status(ws, MOE_ERR_DEVICE_DATA);
-                rows[j] = -1;
-            }
-        }
-        for (int c0 = 0; c0 < nvec; c0 += kCombThreads * U) {
-            uint4 v[K][U];
-#pragma unroll
-            for (int j = 0; j < K; ++j) {
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int c = c0 + u * kCombThreads + threadIdx.x;
-                    if (rows[j] >= 0 && c < nvec) v[j][u] = ld_stream_v4(eo + (long long)rows[j] * nvec + c);
-                }
-            }
-            float acc[U][8];
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-#pragma unroll
-                for (int q = 0; q < 8; ++q) acc[u][q] = 0.0f;
-#pragma unroll
-            for (int j = 0; j < K; ++j) {
-                if (rows[j] < 0) continue;
-#pragma unroll
-                for (int u = 0; u < U; ++u) fma8(acc[u], g[j], v[j][u]);
-            }
-            for (int sidx = 0; sidx < Ks; ++sidx) {
-                const uint4 *sh = shared + ((long long)sidx * T + t) * nvec;
-                uint4 sv[U];
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int c = c0 + u * kCombThreads + threadIdx.x;
-                    if (c < nvec) sv[u] = ld_stream_v4(sh + c);
-                }
-#pragma unroll
-                for (int u = 0; u < U; ++u) add8(acc[u], sv[u]);
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int c = c0 + u * kCombThreads + threadIdx.x;
-                if (c < nvec) {
-                    uint4 o;
-                    o.x = pack_bf16x2(acc[u][0], acc[u][1]);
-                    o.y = pack_bf16x2(acc[u][2], acc[u][3]);
-                    o.z = pack_bf16x2(acc[u][4], acc[u][5]);
-                    o.w = pack_bf16x2(acc[u][6], acc[u][7]);
-                    st_v4(y + t * nvec + c, o);
-                }
-            }
-        }
-    }
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_timer_ns() - t0 > kSpinLimitNs) return false;
+    return true;
 }
 
 template <int K>
-cudaError_t launch_k(const uint4 *eo, const float *gates, const int32_t *dst_row, int r_max,
-                     const int32_t *R_ptr, const uint4 *shared, int Ks, int T, int nvec, uint4 *y,
-                     void *ws, cudaStream_t s)
+__global__ void __launch_bounds__(kCombThreads + 32) combine_tma_kernel(CombineArgs a)
 {
-    const long long cap = 1LL << 30;
-    const unsigned grid = (unsigned)(T < cap ? T : cap);
-    const int per_thread = (nvec + kCombThreads - 1) / kCombThreads;
-    // keep K*U row loads (16 B each) <= 8 per thread: <= 32 data registers
-    constexpr int kUMax = (8 / K) < 1 ? 1 : (8 / K);
-#define MOE_COMBINE(UU) \
-    combine_kernel<K, UU><<<grid, kCombThreads, 0, s>>>(eo, gates, dst_row, r_max, R_ptr, shared, Ks, T, \
-                                                        nvec, y, ws)
-    if (per_thread <= 1 || kUMax == 1) {
-        MOE_COMBINE(1);
-    } else if (per_thread <= 2 || kUMax == 2) {
-        if constexpr (kUMax >= 2) MOE_COMBINE(2);
-    } else if (per_thread <= 4 || kUMax == 4) {
-        if constexpr (kUMax >= 4) MOE_COMBINE(4);
-    } else {
-        if constexpr (kUMax >= 8) MOE_COMBINE(8);
+    extern __shared__ __align__(128) unsigned char s_stage[];  // [stages][slots][cb]
+    __shared__ uint64_t s_full[kMaxStages];   // producer -> consumers: stage loaded
+    __shared__ uint64_t s_empty[kMaxStages];  // consumers -> producer: stage free
+    __shared__ float s_g[kMaxStages][K];
+    __shared__ int s_n[kMaxStages];
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const long long stride = gridDim.x;
+    const size_t stage_bytes = (size_t)a.slots * a.cb;
+
+    if (tid == 0) {
+        for (int s = 0; s < a.stages; ++s) {
+            mbar_init(&s_full[s], 1);
+            mbar_init(&s_empty[s], kCombThreads);
+        }
+        mbar_fence_init();
     }
-#undef MOE_COMBINE
+    __syncthreads();
+
+    if (warp == 0) {
+        // ---- producer warp ----------------------------------------------
+        // Lane l fetches the routing metadata (kept rows, gates) of the l-th
+        // unit of the current batch of 32, so one memory round trip serves
+        // 32 stage fills; lane 0 issues the bulk copies.
+        const int rows_valid = min(a.r_max, __ldg(a.R_ptr));
+        unsigned issued = 0;  // parity of each stage's last fill (bit) once filled
+        long long i = 0;
+        bool stop = false;
+        for (long long batch = 0; !stop; batch += 32) {
+            const long long ul = blockIdx.x + (batch + lane) * stride;
+            int rows[K];
+            float g[K];
+            if (ul < a.units) {
+                const long long t = ul / a.nch;
+#pragma unroll
+                for (int j = 0; j < K; ++j) {
+                    rows[j] = __ldg(a.dst_row + t * K + j);
+                    g[j] = __ldg(a.gates + t * K + j);
+                }
+            }
+            for (int b = 0; b < 32; ++b, ++i) {
+                const long long u = blockIdx.x + i * stride;
+                if (u >= a.units) { stop = true; break; }
+                const int s = (int)(i % a.stages);
+                const long long use = i / a.stages;  // how many times stage s was filled before
+                if (use > 0) {
+                    bool ok = mbar_try_wait(&s_empty[s], (uint32_t)((use - 1) & 1));
+                    if (!ok) {
+                        const unsigned long long t0 = global_timer_ns();
+                        while (!(ok = mbar_try_wait(&s_empty[s], (uint32_t)((use - 1) & 1))) &&
+                               global_timer_ns() - t0 < kSpinLimitNs) {
+                        }
+                    }
+                    if (!ok) {
+                        if (lane == 0) record_status(a.ws, MOE_ERR_TIMEOUT);
+                        stop = true;
+                        break;
+                    }
+                }
+                int rb[K];
+                float gb[K];
+#pragma unroll
+                for (int j = 0; j < K; ++j) {
+                    rb[j] = __shfl_sync(0xffffffffu, rows[j], b);
+                    gb[j] = __shfl_sync(0xffffffffu, g[j], b);
+                }
+                if (lane == 0) {
+                    const long long t = u / a.nch;
+                    const int col0 = (int)(u - t * a.nch) * a.cb;
+                    const int bytes = min(a.cb, a.rowbytes - col0);
+                    int n = 0;
+#pragma unroll
+                    for (int j = 0; j < K; ++j) {
+                        if (rb[j] >= rows_valid) {
+                            record_status(a.ws, MOE_ERR_DEVICE_DATA);
+                            rb[j] = -1;
+                        }
+                        if (rb[j] >= 0) s_g[s][n++] = gb[j];  // gates of the kept slots, in slot order
+                    }
+                    s_n[s] = n;
+                    // expected bytes first (release: s_g / s_n become visible to the waiters)
+                    mbar_arrive_expect_tx(&s_full[s], (uint32_t)((n + a.Ks) * bytes));
+                    unsigned char *st = s_stage + (size_t)s * stage_bytes;
+                    int slot = 0;
+#pragma unroll
+                    for (int j = 0; j < K; ++j) {
+                        if (rb[j] >= 0) {
+                            bulk_load(st + (size_t)slot * a.cb, a.eo + (long long)rb[j] * a.rowbytes + col0,
+                                      bytes, &s_full[s]);
+                            ++slot;
+                        }
+                    }
+                    for (int q = 0; q < a.Ks; ++q)
+                        bulk_load(st + (size_t)(K + q) * a.cb,
+                                  a.shared + ((long long)q * a.T + t) * a.rowbytes + col0, bytes, &s_full[s]);
+                }
+                issued = (issued & ~(1u << s)) | ((unsigned)(use & 1) << s) | (1u << (s + 16));
+            }
+        }
+        // drain: never leave with copies still landing in this block's shared memory
+        if (lane == 0) {
+            for (int s = 0; s < a.stages; ++s) {
+                if (!(issued & (1u << (s + 16)))) continue;
+                const uint32_t par = (issued >> s) & 1u;
+                const unsigned long long t0 = global_timer_ns();
+                while (!mbar_try_wait(&s_full[s], par) && global_timer_ns() - t0 < kSpinLimitNs) {
+                }
+            }
+        }
+        return;
+    }
+
+    // ---- consumer warps ---------------------------------------------------
+    const int ct = tid - 32;
+    long long i = 0;
+    for (long long u = blockIdx.x; u < a.units; u += stride, ++i) {
+        const int s = (int)(i % a.stages);
+        const uint32_t par = (uint32_t)((i / a.stages) & 1);
+        if (!wait_stage(&s_full[s], par)) {
+            if (ct == 0) record_status(a.ws, MOE_ERR_TIMEOUT);
+            return;
+        }
+        const long long t = u / a.nch;
+        const int col0 = (int)(u - t * a.nch) * a.cb;
+        const int nv = min(a.cb, a.rowbytes - col0) >> 4;
+        const int n = s_n[s];
+        const unsigned char *st = s_stage + (size_t)s * stage_bytes;
+        uint4 *yrow = reinterpret_cast<uint4 *>(a.y + t * a.rowbytes + col0);
+        for (int v = ct; v < nv; v += kCombThreads) {
+            float acc[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+            // pinned order: kept slots ascending, then shared experts ascending
+            for (int r = 0; r < n; ++r) fma8(acc, s_g[s][r], lds_v4(st + (size_t)r * a.cb + v * 16));
+            for (int q = 0; q < a.Ks; ++q) add8(acc, lds_v4(st + (size_t)(K + q) * a.cb + v * 16));
+            uint4 o;
+            o.x = pack_bf16x2(acc[0], acc[1]);
+            o.y = pack_bf16x2(acc[2], acc[3]);
+            o.z = pack_bf16x2(acc[4], acc[5]);
+            o.w = pack_bf16x2(acc[6], acc[7]);
+            st_v4(yrow + v, o);
+        }
+        mbar_arrive(&s_empty[s]);
+    }
+}
+
+int blocks_per_sm(const void *fn, size_t smem)
+{
+    static std::mutex mu;
+    static std::unordered_map<unsigned long long, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const unsigned long long key = (reinterpret_cast<unsigned long long>(fn) * 1315423911ull) ^
+                                   ((unsigned long long)smem << 8) ^ (unsigned long long)dev;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kCombThreads + 32, smem) != cudaSuccess || n < 1) n = 1;
+    cache[key] = n;
+    return n;
+}
+
+template <int K>
+cudaError_t launch_k(const CombineArgs &a, cudaStream_t s)
+{
+    const void *fn = reinterpret_cast<const void *>(combine_tma_kernel<K>);
+    const size_t smem = (size_t)a.stages * a.slots * a.cb;
+    if (smem > 48 * 1024) {
+        cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kStageBudget);
+        if (err != cudaSuccess) return err;
+    }
+    const long long resident = (long long)device_sm_count() * blocks_per_sm(fn, smem);
+    const unsigned grid = (unsigned)(a.units < resident ? a.units : resident);
+    combine_tma_kernel<K><<<grid, kCombThreads + 32, smem, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -158,15 +288,31 @@ cudaError_t launch_combine(const void *eo, const moe_layout *L, const float *gat
                            int Ks, int T, int H, void *y, cudaStream_t s)
 {
     if (T == 0) return cudaSuccess;
-    const uint4 *ep = static_cast<const uint4 *>(eo);
-    const uint4 *sp = static_cast<const uint4 *>(shared);
-    uint4 *yp = static_cast<uint4 *>(y);
-    const int nvec = H / 8;
+    CombineArgs a;
+    a.eo = static_cast<const char *>(eo);
+    a.gates = gates;
+    a.dst_row = L->dst_row;
+    a.R_ptr = L->offsets + L->E;
+    a.shared = static_cast<const char *>(shared);
+    a.y = static_cast<char *>(y);
+    a.ws = L->ws;
+    a.T = T;
+    a.r_max = L->r_max;
+    a.Ks = Ks;
+    a.rowbytes = H * 2;
+    a.slots = L->k + Ks;
+    // Chunk the row so that at least three stages fit the budget, then use as
+    // many stages (<= kMaxStages) as the budget holds.
+    const int cb_max = (kStageBudget / 3 / a.slots) & ~15;
+    a.nch = (a.rowbytes + cb_max - 1) / cb_max;
+    a.cb = (((a.rowbytes + a.nch - 1) / a.nch) + 15) & ~15;
+    a.stages = kStageBudget / (a.slots * a.cb);
+    if (a.stages > kMaxStages) a.stages = kMaxStages;
+    if (a.stages < 1) return cudaErrorInvalidValue;
+    a.units = (long long)T * a.nch;
     switch (L->k) {
 #define MOE_COMBINE_CASE(KK) \
-    case KK:                                                                                       \
-        return launch_k<KK>(ep, gates, L->dst_row, L->r_max, L->offsets + L->E, sp, Ks, T, nvec, yp, \
-                            L->ws, s);
+    case KK: return launch_k<KK>(a, s);
         MOE_COMBINE_CASE(1) MOE_COMBINE_CASE(2) MOE_COMBINE_CASE(3) MOE_COMBINE_CASE(4)
         MOE_COMBINE_CASE(5) MOE_COMBINE_CASE(6) MOE_COMBINE_CASE(7) MOE_COMBINE_CASE(8)
         MOE_COMBINE_CASE(9) MOE_COMBINE_CASE(10) MOE_COMBINE_CASE(11) MOE_COMBINE_CASE(12)

@@ -37,16 +37,31 @@ __host__ __device__ inline unsigned long long *ws_flags(void *ws)
     return reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + kWsHeaderBytes);
 }
 
-// Layout tiling: about 1024 assignments per tile (T*k < 2^30 keeps every
-// count inside the 30-bit value field of a flag word).
+// Layout tiling.  A tile holds tile_tokens(T, k) consecutive tokens, i.e.
+// up to kLayoutMaxTileAssign assignments: about A/256 assignments rounded up
+// to a multiple of 1024, within [1024, 8192], so large problems use at most
+// ~256 tiles (short look-back chains) and small ones still spread over many
+// blocks.  The rule depends only on (T, k): the workspace size is known on
+// the host without a device.  T*k < 2^30 keeps every count inside the
+// 30-bit value field of a flag word.
 constexpr int kLayoutThreads = 256;
 constexpr int kLayoutWarps = kLayoutThreads / 32;
-constexpr int kLayoutTileAssign = 1024;
-__host__ __device__ inline int layout_tile_tokens(int k) { return kLayoutTileAssign / k; }
+constexpr int kLayoutMinTileAssign = 1024;
+constexpr int kLayoutMaxTileAssign = 8192;
+__host__ __device__ inline int layout_tile_tokens(long long T, int k)
+{
+    const long long A = T * k;
+    long long t = (A + 255) / 256;
+    t = (t + kLayoutMinTileAssign - 1) / kLayoutMinTileAssign * kLayoutMinTileAssign;
+    if (t < kLayoutMinTileAssign) t = kLayoutMinTileAssign;
+    if (t > kLayoutMaxTileAssign) t = kLayoutMaxTileAssign;
+    const int tt = (int)(t / k);
+    return tt < 1 ? 1 : tt;
+}
 __host__ __device__ inline int layout_tiles(long long T, int k)
 {
-    long long tt = layout_tile_tokens(k);
-    long long n = (T + tt - 1) / tt;
+    const long long tt = layout_tile_tokens(T, k);
+    const long long n = (T + tt - 1) / tt;
     return n < 1 ? 1 : (int)n;
 }
 

@@ -26,6 +26,7 @@ namespace moe {
 namespace {
 
 constexpr int kGateMaxThreads = 256;
+constexpr int kStageLoads = 8;  // loads in flight per thread while staging logits
 
 // Insert (v, e) into the descending list bv/bi of length K if it beats the
 // last entry.  Strictly-greater comparisons keep the earlier (lower) expert
@@ -94,16 +95,54 @@ gate_kernel(const float *__restrict__ logits, int T, int E, int32_t *__restrict_
     const int stride = E | 1;
     const long long t0 = (long long)blockIdx.x * TT;
     const int rows = (int)min((long long)TT, (long long)T - t0);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
 
     for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0u;
     if (threadIdx.x == 0) s_bad = 0;
 
-    // Stage the tile: warp w copies rows w, w + nwarps, ... (coalesced per row).
-    for (int r = warp; r < rows; r += nwarps) {
-        const float *src = logits + (t0 + r) * (long long)E;
-        float *dst = s_logit + r * stride;
-        for (int c = lane; c < E; c += 32) dst[c] = __ldg(src + c);
+    // Stage the tile.  Its rows are contiguous in global memory, so it is one
+    // flat copy: every thread issues kStageLoads independent 16-byte loads
+    // before any shared-memory store, so the whole tile is in flight at once.
+    {
+        const float *src = logits + t0 * (long long)E;
+        const int n = rows * E;
+        if ((E & 3) == 0) {
+            const float4 *src4 = reinterpret_cast<const float4 *>(src);
+            const int n4 = n >> 2;
+            for (int base = 0; base < n4; base += kStageLoads * blockDim.x) {
+                float4 v[kStageLoads];
+#pragma unroll
+                for (int u = 0; u < kStageLoads; ++u) {
+                    const int i = base + u * blockDim.x + threadIdx.x;
+                    if (i < n4) v[u] = __ldg(src4 + i);
+                }
+#pragma unroll
+                for (int u = 0; u < kStageLoads; ++u) {
+                    const int i = base + u * blockDim.x + threadIdx.x;
+                    if (i < n4) {
+                        const int r = (4 * i) / E, c = 4 * i - r * E;
+                        float *d = s_logit + r * stride + c;
+                        d[0] = v[u].x; d[1] = v[u].y; d[2] = v[u].z; d[3] = v[u].w;
+                    }
+                }
+            }
+        } else {
+            for (int base = 0; base < n; base += kStageLoads * blockDim.x) {
+                float v[kStageLoads];
+#pragma unroll
+                for (int u = 0; u < kStageLoads; ++u) {
+                    const int i = base + u * blockDim.x + threadIdx.x;
+                    if (i < n) v[u] = __ldg(src + i);
+                }
+#pragma unroll
+                for (int u = 0; u < kStageLoads; ++u) {
+                    const int i = base + u * blockDim.x + threadIdx.x;
+                    if (i < n) {
+                        const int r = i / E;
+                        s_logit[r * stride + (i - r * E)] = v[u];
+                    }
+                }
+            }
+        }
     }
     __syncthreads();
 

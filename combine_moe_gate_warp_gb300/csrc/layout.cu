@@ -7,20 +7,22 @@
 // padding rows) and sec. 8.3.A (strict per-expert capacity, assignments
 // over it taken in order -- here: dropped, token-index order).
 //
-// Design (sm_103a): one block per tile of ~1024 consecutive assignments,
-// tile ids handed out by an atomic counter so that every tile a block waits
-// on has already started.
+// Design (sm_103a): one block per tile of consecutive tokens (1024..8192
+// assignments, see layout_tile_tokens), tile ids handed out by an atomic
+// counter so that every tile a block waits on has already started.
 //   1. Per-expert packed offsets from expert_counts (exclusive scan of
 //      min(count, capacity); E <= 256, every block recomputes it).
 //   2. Tile-local stable ranks: each warp walks its contiguous slice of the
 //      tile 32 assignments at a time; __match_any_sync groups equal expert
 //      ids, the rank is the popcount of lower peers plus a per-warp running
 //      count in shared memory.  Warp slices are then scanned per expert.
-//   3. Decoupled look-back across tiles, one thread per expert column: a
-//      64-bit flag word per (tile, expert) carries an epoch tag, a state
-//      (aggregate / inclusive prefix) and the 30-bit value, so no flag array
-//      ever needs clearing; every wait is bounded by %globaltimer and
-//      records MOE_ERR_TIMEOUT instead of hanging.
+//   3. Decoupled look-back across tiles.  A 64-bit flag word per (tile,
+//      expert) carries an epoch tag, a state (aggregate / inclusive prefix)
+//      and the 30-bit value, so no flag array ever needs clearing.  The
+//      whole block looks back at once: 256/E threads per expert each read
+//      one predecessor's word per round, so a round covers 256/E tiles for
+//      every expert with a single memory round trip.  Every wait is bounded
+//      by %globaltimer and records MOE_ERR_TIMEOUT instead of hanging.
 //   4. Rank r = prefix + warp offset + local rank; kept iff r < capacity;
 //      dst_row / src_pos / capacity_mask written, dropped gates zeroed.
 //   5. Distinct-partition tokens per tile, summed with integer atomics; the
@@ -29,6 +31,8 @@
 
 namespace moe {
 namespace {
+
+constexpr int kLoadBatch = 8;  // expert-id loads in flight per thread
 
 struct LayoutArgs {
     const int32_t *idx;
@@ -56,55 +60,37 @@ __device__ __forceinline__ void st_volatile_u64(unsigned long long *p, unsigned 
 
 __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
 {
-    __shared__ int s_idx[kLayoutTileAssign];
-    __shared__ int s_rank[kLayoutTileAssign];
+    extern __shared__ int s_dyn[];   // s_idx[tile assignments], s_rank[tile assignments]
     __shared__ unsigned s_whist[kLayoutWarps][MOE_MAX_EXPERTS];
     __shared__ int s_off[MOE_MAX_EXPERTS + 1];
     __shared__ unsigned s_excl[MOE_MAX_EXPERTS];
+    __shared__ int s_base[MOE_MAX_EXPERTS];
     __shared__ unsigned s_ptok[MOE_MAX_EXPERTS];
+    __shared__ unsigned long long s_win[kLayoutThreads];
     __shared__ unsigned s_warp_tot[kLayoutWarps];
     __shared__ unsigned s_tile, s_epoch;
-    __shared__ int s_last, s_bad, s_skip;
+    __shared__ int s_last, s_bad, s_skip, s_abort;
 
     WsHeader *ws = static_cast<WsHeader *>(a.ws);
     unsigned long long *flags = ws_flags(a.ws);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int E = a.E, k = a.k;
+    int *s_idx = s_dyn;
+    int *s_rank = s_dyn + a.tile_tokens * k;
 
+    const int raw_count = (tid < E) ? __ldg(a.counts_in + tid) : 0;
     if (tid == 0) {
         unsigned ep = *reinterpret_cast<volatile unsigned *>(&ws->epoch);
         __threadfence();
         s_tile = atomicAdd(&ws->tile_ctr, 1u);
         s_epoch = ep;
         s_bad = 0;
+        s_abort = 0;
         s_skip = (*reinterpret_cast<volatile unsigned *>(&ws->inject_skip_publish) == s_tile + 1u);
     }
     for (int i = tid; i < kLayoutWarps * MOE_MAX_EXPERTS; i += kLayoutThreads)
         (&s_whist[0][0])[i] = 0u;
     for (int p = tid; p < a.P; p += kLayoutThreads) s_ptok[p] = 0u;
-    __syncthreads();
-
-    // 1. packed offsets: exclusive scan of kept counts (block-wide, E <= 256).
-    {
-        int c = 0;
-        if (tid < E) {
-            int raw = a.counts_in[tid];
-            if (raw < 0 || (long long)raw > (long long)a.T * k) { raw = 0; s_bad = 1; }
-            c = ((unsigned)raw < a.cap) ? raw : (int)a.cap;
-        }
-        int incl = c;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            int n = __shfl_up_sync(0xffffffffu, incl, d);
-            if (lane >= d) incl += n;
-        }
-        if (lane == 31) s_warp_tot[warp] = (unsigned)incl;
-        __syncthreads();
-        int base = 0;
-        for (int w = 0; w < warp; ++w) base += (int)s_warp_tot[w];
-        if (tid < E) s_off[tid] = base + incl - c;
-        if (tid == E - 1) s_off[E] = base + incl;
-    }
     __syncthreads();
 
     const unsigned tile = s_tile, epoch = s_epoch;
@@ -117,13 +103,47 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
     const long long a0 = tok0 * k;
     const int A = (int)(max(0LL, tok1 - tok0) * k);
 
-    // load the tile's expert ids; out-of-range ids become the sentinel E
-    for (int i = tid; i < A; i += kLayoutThreads) {
-        int e = a.idx[a0 + i];
-        if (e < 0 || e >= E) { e = E; s_bad = 1; }
-        s_idx[i] = e;
+    // the tile's expert ids, kLoadBatch loads in flight per thread; ids
+    // outside [0, E) become the sentinel E
+    for (int base = 0; base < A; base += kLoadBatch * kLayoutThreads) {
+        int v[kLoadBatch];
+#pragma unroll
+        for (int u = 0; u < kLoadBatch; ++u) {
+            const int i = base + u * kLayoutThreads + tid;
+            if (i < A) v[u] = __ldg(a.idx + a0 + i);
+        }
+#pragma unroll
+        for (int u = 0; u < kLoadBatch; ++u) {
+            const int i = base + u * kLayoutThreads + tid;
+            if (i < A) {
+                int e = v[u];
+                if (e < 0 || e >= E) { e = E; s_bad = 1; }
+                s_idx[i] = e;
+            }
+        }
     }
-    __syncthreads();
+
+    // 1. packed offsets: exclusive scan of kept counts (block-wide, E <= 256).
+    {
+        int c = 0;
+        if (tid < E) {
+            int raw = raw_count;
+            if (raw < 0 || (long long)raw > (long long)a.T * k) { raw = 0; s_bad = 1; }
+            c = ((unsigned)raw < a.cap) ? raw : (int)a.cap;
+        }
+        int incl = c;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            int n = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += n;
+        }
+        if (lane == 31) s_warp_tot[warp] = (unsigned)incl;
+        __syncthreads();  // also publishes s_idx
+        int base = 0;
+        for (int w = 0; w < warp; ++w) base += (int)s_warp_tot[w];
+        if (tid < E) s_off[tid] = base + incl - c;
+        if (tid == E - 1) s_off[E] = base + incl;
+    }
 
     // 2. tile-local stable ranks
     const int per_warp = (((A + kLayoutWarps - 1) / kLayoutWarps) + 31) & ~31;
@@ -147,8 +167,10 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
     }
     __syncthreads();
 
-    // per-expert scan across warps -> warp offsets, tile aggregate
+    // per-expert scan across warps -> warp offsets, tile aggregate; publish
+    // the aggregate (tile 0: the inclusive prefix) right away
     unsigned agg = 0;
+    const bool publish = !s_skip;
     if (tid < E) {
 #pragma unroll
         for (int w = 0; w < kLayoutWarps; ++w) {
@@ -156,43 +178,64 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
             s_whist[w][tid] = agg;
             agg += v;
         }
-    }
-
-    // 3. decoupled look-back, one thread per expert column
-    if (tid < E) {
-        unsigned excl = 0;
         unsigned long long *my = flags + (size_t)tile * E + tid;
-        const bool publish = !s_skip;
-        if (tile == 0) {
-            if (publish) st_volatile_u64(my, make_flag(epoch, kFlagInclusive, agg));
-        } else {
-            if (publish) st_volatile_u64(my, make_flag(epoch, kFlagAggregate, agg));
-            long long p = (long long)tile - 1;
-            unsigned long long t_start = 0;
-            unsigned spins = 0;
-            while (p >= 0) {
-                const unsigned long long w = ld_volatile_u64(flags + (size_t)p * E + tid);
-                const unsigned state = (unsigned)(w >> 30) & 3u;
-                if ((unsigned)(w >> 32) == epoch && state != 0u) {
-                    excl += (unsigned)(w & 0x3FFFFFFFull);
-                    if (state == (unsigned)kFlagInclusive) break;
-                    --p;
-                    continue;
-                }
-                if ((++spins & 63u) == 0u) {
-                    const unsigned long long now = global_timer_ns();
-                    if (t_start == 0) t_start = now;
-                    else if (now - t_start > kSpinLimitNs ||
-                             *reinterpret_cast<volatile unsigned *>(&ws->status) == MOE_ERR_TIMEOUT) {
-                        record_status(a.ws, MOE_ERR_TIMEOUT);
-                        break;
-                    }
+        if (publish) st_volatile_u64(my, make_flag(epoch, tile == 0 ? kFlagInclusive : kFlagAggregate, agg));
+        s_excl[tid] = 0u;
+        s_base[tid] = (int)tile - 1;  // next predecessor to read; -1 = prefix complete
+    }
+    __syncthreads();
+
+    // 3. block-wide decoupled look-back
+    {
+        const int W = kLayoutThreads / E;  // predecessors read per expert per round
+        const int my_e = tid / W, my_w = tid - (tid / W) * W;
+        unsigned long long t_start = 0;
+        while (true) {
+            if (my_e < E) {
+                const int b = s_base[my_e];
+                if (b >= 0) {
+                    const int p = b - my_w;
+                    s_win[tid] = (p >= 0) ? ld_volatile_u64(flags + (size_t)p * E + my_e)
+                                          : make_flag(epoch, kFlagInclusive, 0u);
                 }
             }
-            if (publish) st_volatile_u64(my, make_flag(epoch, kFlagInclusive, excl + agg));
+            __syncthreads();
+            int open = 0;
+            if (tid < E && s_base[tid] >= 0) {
+                unsigned add = 0;
+                int used = 0;
+                bool done = false;
+                for (int w = 0; w < W; ++w) {
+                    const unsigned long long f = s_win[tid * W + w];
+                    const unsigned state = (unsigned)(f >> 30) & 3u;
+                    if ((unsigned)(f >> 32) != epoch || state == 0u) break;  // not published yet
+                    add += (unsigned)(f & 0x3FFFFFFFull);
+                    ++used;
+                    if (state == (unsigned)kFlagInclusive) { done = true; break; }
+                }
+                s_excl[tid] += add;
+                s_base[tid] = done ? -1 : s_base[tid] - used;
+                open = !done;
+            }
+            if (!__syncthreads_or(open)) break;
+            if (tid == 0) {
+                const unsigned long long now = global_timer_ns();
+                if (t_start == 0) t_start = now;
+                else if (now - t_start > kSpinLimitNs ||
+                         *reinterpret_cast<volatile unsigned *>(&ws->status) == MOE_ERR_TIMEOUT) {
+                    record_status(a.ws, MOE_ERR_TIMEOUT);
+                    s_abort = 1;
+                }
+            }
+            __syncthreads();
+            if (s_abort) break;
         }
-        s_excl[tid] = excl;
-        if (tile == (unsigned)a.ntiles - 1 && (int)(excl + agg) != a.counts_in[tid]) s_bad = 1;
+    }
+    if (tid < E) {
+        const unsigned excl = s_excl[tid];
+        if (tile > 0 && publish)
+            st_volatile_u64(flags + (size_t)tile * E + tid, make_flag(epoch, kFlagInclusive, excl + agg));
+        if (tile == (unsigned)a.ntiles - 1 && (int)(excl + agg) != raw_count) s_bad = 1;
     }
     __syncthreads();
 
@@ -292,7 +335,7 @@ cudaError_t launch_layout(const int32_t *topk_idx, const int32_t *counts_in, int
     a.P = P;
     a.cap = capacity > 0 ? (unsigned)capacity : 0xFFFFFFFFu;
     a.r_max = L->r_max;
-    a.tile_tokens = layout_tile_tokens(k);
+    a.tile_tokens = layout_tile_tokens(T, k);
     a.ntiles = layout_tiles(T, k);
     a.gates = gates;
     a.counts_out = L->counts;
@@ -305,7 +348,13 @@ cudaError_t launch_layout(const int32_t *topk_idx, const int32_t *counts_in, int
     a.cmask = L->capacity_mask;
     a.dropped = L->dropped;
     a.ws = ws;
-    layout_kernel<<<a.ntiles, kLayoutThreads, 0, s>>>(a);
+    const size_t smem = 2 * sizeof(int) * (size_t)a.tile_tokens * k;
+    if (smem > 48 * 1024) {
+        cudaError_t err = cudaFuncSetAttribute(layout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)(2 * sizeof(int) * kLayoutMaxTileAssign));
+        if (err != cudaSuccess) return err;
+    }
+    layout_kernel<<<a.ntiles, kLayoutThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
 
