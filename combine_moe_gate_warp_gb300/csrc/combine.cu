@@ -122,6 +122,8 @@ __global__ void __launch_bounds__(kCombThreads + 32) combine_tma_kernel(CombineA
         mbar_fence_init();
     }
     __syncthreads();
+    pdl_wait();
+    pdl_launch_dependents();
 
     if (warp == 0) {
         // ---- producer warp ----------------------------------------------
@@ -278,8 +280,7 @@ cudaError_t launch_k(const CombineArgs &a, cudaStream_t s)
     }
     const long long resident = (long long)device_sm_count() * blocks_per_sm(fn, smem);
     const unsigned grid = (unsigned)(a.units < resident ? a.units : resident);
-    combine_tma_kernel<K><<<grid, kCombThreads + 32, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(combine_tma_kernel<K>, dim3(grid), dim3(kCombThreads + 32), smem, s, a);
 }
 
 }  // namespace

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "moe_route.h"
 
 namespace moe {
@@ -105,6 +107,17 @@ __device__ __forceinline__ void st_v4(uint4 *p, const uint4 &v)
                  : "memory");
 }
 
+// Programmatic dependent launch.  Every kernel of the path is launched so
+// that it may start while the previous kernel in the stream finishes.  It
+// first waits for that kernel to complete (all its memory visible), and only
+// then allows the next kernel to launch, so "kernel N+1 running" implies
+// "kernel N-1 complete".  Without the launch attribute both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // bf16 pair (one 32-bit word) -> two fp32
 __device__ __forceinline__ float bf16lo(unsigned w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(unsigned w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -128,4 +141,22 @@ cudaError_t launch_dispatch_fp8(const void *x, int T, int H, const moe_layout *L
 cudaError_t launch_combine(const void *eo, const moe_layout *L, const float *gates,
                            const void *shared, int Ks, int T, int H, void *y, cudaStream_t s);
 int device_sm_count();
+
+// Launch `kernel` on `s` with programmatic stream serialization allowed.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 }  // namespace moe

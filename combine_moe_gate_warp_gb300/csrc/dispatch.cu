@@ -58,6 +58,8 @@ dispatch_bf16_kernel(const uint4 *__restrict__ x, long long T, int nvec, int k,
 {
     __shared__ int s_rows[MOE_MAX_TOPK];
     __shared__ int s_n;
+    pdl_wait();
+    pdl_launch_dependents();
     const int rows_valid = min(r_max, __ldg(R_ptr));
     for (long long t = blockIdx.x; t < T; t += gridDim.x) {
         const int n = load_token_rows(dst_row, t, k, rows_valid, s_rows, &s_n, ws);
@@ -118,6 +120,8 @@ dispatch_fp8_kernel(const uint4 *__restrict__ x, long long T, int npairs, int k,
     __shared__ int s_n;
     __shared__ int s_max[kDispThreads / 32], s_min[kDispThreads / 32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    pdl_wait();
+    pdl_launch_dependents();
     const int rows_valid = min(r_max, __ldg(R_ptr));
     for (long long t = blockIdx.x; t < T; t += gridDim.x) {
         const int n = load_token_rows(dst_row, t, k, rows_valid, s_rows, &s_n, ws);
@@ -210,8 +214,9 @@ cudaError_t launch_dispatch_bf16(const void *x, int T, int H, const moe_layout *
     const uint4 *xp = static_cast<const uint4 *>(x);
     uint4 *pp = static_cast<uint4 *>(packed);
 #define MOE_DISPATCH_BF16(UU)                                                                     \
-    dispatch_bf16_kernel<UU><<<grid, kDispThreads, 0, s>>>(xp, T, nvec, L->k, L->dst_row,         \
-                                                           L->r_max, L->offsets + L->E, pp, L->ws)
+    return launch_pdl(dispatch_bf16_kernel<UU>, dim3(grid), dim3(kDispThreads), 0, s, xp, (long long)T, nvec, \
+                      L->k, (const int32_t *)L->dst_row, L->r_max, (const int32_t *)(L->offsets + L->E), pp,  \
+                      L->ws)
     if (per_thread <= 1) MOE_DISPATCH_BF16(1);
     else if (per_thread <= 2) MOE_DISPATCH_BF16(2);
     else if (per_thread <= 3) MOE_DISPATCH_BF16(3);
@@ -234,8 +239,9 @@ cudaError_t launch_dispatch_fp8(const void *x, int T, int H, const moe_layout *L
     uint4 *pp = static_cast<uint4 *>(packed);
     float2 *sp = reinterpret_cast<float2 *>(scales);
 #define MOE_DISPATCH_FP8(CC)                                                                      \
-    dispatch_fp8_kernel<CC><<<grid, kDispThreads, 0, s>>>(xp, T, npairs, L->k, L->dst_row,        \
-                                                          L->r_max, L->offsets + L->E, pp, sp, L->ws)
+    return launch_pdl(dispatch_fp8_kernel<CC>, dim3(grid), dim3(kDispThreads), 0, s, xp, (long long)T, npairs, \
+                      L->k, (const int32_t *)L->dst_row, L->r_max, (const int32_t *)(L->offsets + L->E), pp,   \
+                      sp, L->ws)
     if (per_thread <= 1) MOE_DISPATCH_FP8(1);
     else if (per_thread <= 2) MOE_DISPATCH_FP8(2);
     else if (per_thread <= 4) MOE_DISPATCH_FP8(4);

@@ -98,6 +98,8 @@ gate_kernel(const float *__restrict__ logits, int T, int E, int32_t *__restrict_
 
     for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0u;
     if (threadIdx.x == 0) s_bad = 0;
+    pdl_wait();
+    pdl_launch_dependents();
 
     // Stage the tile.  Its rows are contiguous in global memory, so it is one
     // flat copy: every thread issues kStageLoads independent 16-byte loads
@@ -273,8 +275,8 @@ cudaError_t launch_k(const float *logits, int T, int E, int32_t *idx, float *gat
     }
     long long blocks = ((long long)T + tt - 1) / tt;
     if (blocks < 1) blocks = 1;
-    gate_kernel<K, MODE><<<(unsigned)blocks, tt, smem, s>>>(logits, T, E, idx, gates, counts, aux, ent, ws);
-    return cudaGetLastError();
+    return launch_pdl(gate_kernel<K, MODE>, dim3((unsigned)blocks), dim3(tt), smem, s, logits, T, E, idx, gates,
+                      counts, aux, ent, ws);
 }
 
 template <int MODE>

@@ -78,6 +78,8 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
     int *s_idx = s_dyn;
     int *s_rank = s_dyn + a.tile_tokens * k;
 
+    pdl_wait();
+    pdl_launch_dependents();
     const int raw_count = (tid < E) ? __ldg(a.counts_in + tid) : 0;
     if (tid == 0) {
         unsigned ep = *reinterpret_cast<volatile unsigned *>(&ws->epoch);
@@ -354,8 +356,7 @@ cudaError_t launch_layout(const int32_t *topk_idx, const int32_t *counts_in, int
                                                (int)(2 * sizeof(int) * kLayoutMaxTileAssign));
         if (err != cudaSuccess) return err;
     }
-    layout_kernel<<<a.ntiles, kLayoutThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(layout_kernel, dim3(a.ntiles), dim3(kLayoutThreads), smem, s, a);
 }
 
 }  // namespace moe

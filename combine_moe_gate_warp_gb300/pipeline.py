@@ -27,11 +27,23 @@ class RouteShape:
     capacity: int = 0
 
 
+def _check_input(t, dtype, shape, name):
+    if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == dtype and t.is_contiguous()):
+        raise ValueError(f"{name}: expected a contiguous CUDA tensor of {dtype}")
+    if tuple(t.shape[:len(shape)]) != tuple(shape):
+        raise ValueError(f"{name}: expected leading shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
 class RoutePlan:
+    """Buffers and bound arguments of one problem size.  The plan is bound to
+    ``stream`` (default: the stream current when it is built); its methods
+    call the C entry points with cached pointers, so the per-call host cost
+    is one foreign call plus input checks."""
+
     def __init__(self, shape: RouteShape, device="cuda", stream=None):
         s = self.shape = shape
         self.device = torch.device(device)
-        self.stream = stream
+        self.stream = torch.cuda.current_stream(self.device) if stream is None else stream
         T, E, k = s.T, s.E, s.k
         i32 = dict(dtype=torch.int32, device=self.device)
         self.topk_idx = torch.empty((max(T, 1), k), **i32)
@@ -50,26 +62,49 @@ class RoutePlan:
             self.packed = torch.empty((rows, s.H), dtype=torch.bfloat16, device=self.device)
             self.scales = None
         self.y = torch.empty((max(T, 1), s.H), dtype=torch.bfloat16, device=self.device)
+        self._bind()
+
+    def _bind(self):
+        import ctypes
+        s = self.shape
+        self._lib = abi.lib()
+        self._s = ctypes.c_void_p(self.stream.cuda_stream)
+        self._Lref = ctypes.byref(self.layout.c)
+        self._ws_bytes = self.ws.numel()
+        self._gate_tail = (self.topk_idx.data_ptr(), self.gates.data_ptr(), self.expert_counts.data_ptr(),
+                           self.aux_loss.data_ptr(), self.entropy.data_ptr(), self.ws.data_ptr(),
+                           self._ws_bytes, self._s)
+        self._layout_args = (self.topk_idx.data_ptr(), self.expert_counts.data_ptr(), s.T, s.E, s.k, s.P,
+                             s.capacity, self.gates.data_ptr(), self._Lref, self.ws.data_ptr(),
+                             self._ws_bytes, self._s)
+        self._scales_ptr = None if self.scales is None else self.scales.data_ptr()
 
     # the four hot-path calls -------------------------------------------------
     def gate(self, logits: torch.Tensor):
         s = self.shape
-        abi.moe_gate(logits, s.k, s.mode, self.topk_idx, self.gates, self.expert_counts,
-                     self.aux_loss, self.entropy, self.ws, self.stream)
+        _check_input(logits, torch.float32, (s.T, s.E), "logits")
+        abi._check(self._lib.moe_gate(logits.data_ptr(), s.T, s.E, s.k, s.mode, *self._gate_tail), "moe_gate")
 
     def dispatch_layout(self):
-        s = self.shape
-        abi.moe_dispatch_layout(self.topk_idx, self.expert_counts, s.T, s.E, s.k, s.P, s.capacity,
-                                self.gates, self.layout, self.ws, self.stream)
+        abi._check(self._lib.moe_dispatch_layout(*self._layout_args), "moe_dispatch_layout")
 
     def dispatch(self, x: torch.Tensor):
         s = self.shape
-        abi.moe_dispatch(x, s.T, s.H, self.layout, int(s.fp8), self.packed, self.scales, self.stream)
+        _check_input(x, torch.bfloat16, (s.T, s.H), "x")
+        abi._check(self._lib.moe_dispatch(x.data_ptr(), s.T, s.H, self._Lref, int(s.fp8), self.packed.data_ptr(),
+                                          self._scales_ptr, self._s), "moe_dispatch")
 
     def combine(self, expert_out: torch.Tensor, shared_out: torch.Tensor | None = None):
         s = self.shape
-        abi.moe_combine(expert_out, self.layout, self.gates, shared_out, s.Ks, s.T, s.H, self.y,
-                        self.stream)
+        _check_input(expert_out, torch.bfloat16, (), "expert_out")
+        if expert_out.shape[-1] != s.H:
+            raise ValueError("expert_out: last dimension must be H")
+        sh = None
+        if s.Ks:
+            _check_input(shared_out, torch.bfloat16, (s.Ks, s.T, s.H), "shared_out")
+            sh = shared_out.data_ptr()
+        abi._check(self._lib.moe_combine(expert_out.data_ptr(), self._Lref, self.gates.data_ptr(), sh, s.Ks, s.T,
+                                         s.H, self.y.data_ptr(), self._s), "moe_combine")
 
     def step(self, logits, x, expert_out, shared_out=None):
         """gate -> layout -> dispatch -> combine (4 kernel launches)."""
