@@ -12,16 +12,19 @@
 // Design (sm_103a): gather form -- y is written exactly once and every kept
 // expert-output row is read exactly once, so the traffic is the algorithmic
 // minimum.  A persistent grid (as many blocks as fit on the SMs) works
-// through units = (token, column chunk of the row).  Each block owns a ring
-// of S shared-memory stages and is warp-specialised: a producer warp reads
-// the routing metadata of 32 upcoming units in one round trip and fills
-// stages with 1-D bulk copies (cp.async.bulk, the TMA engine) of the kept
-// expert-output chunks and the shared-expert chunks, completing on the
-// stage's "full" mbarrier; four consumer warps wait on "full", accumulate
+// through units = (token, column chunk of the row).  Each block owns a byte
+// ring in shared memory and is warp-specialised: a producer warp reads the
+// routing metadata of 32 upcoming units in one round trip, allocates
+// exactly (kept rows + shared experts) x chunk bytes per unit in the ring
+// (dropped slots take no space, so skewed or capacity-limited routing keeps
+// as many bytes in flight as dense routing), and fills them with 1-D bulk
+// copies (cp.async.bulk, the TMA engine) completing on the unit's "full"
+// mbarrier; four consumer warps (one unit per warp for small units, all
+// four on one unit for large ones) wait on "full", accumulate
 // in fp32 with explicit round-to-nearest FMA/add in the pinned order (kept
 // slots ascending, then shared experts ascending), round once to bf16,
-// store y with 16-byte coalesced stores, and release the stage on its
-// "empty" mbarrier.  No block-wide barrier sits in the loop, and the bytes
+// store y with 16-byte coalesced stores, and release the unit on its
+// "empty" mbarrier; the producer reclaims ring space in unit order.  No block-wide barrier sits in the loop, and the bytes
 // in flight per SM are bounded by shared memory, not registers.  Every
 // mbarrier wait is bounded; on expiry the waiter records MOE_ERR_TIMEOUT,
 // and the producer always waits (bounded) for its copies still in flight
@@ -38,8 +41,8 @@ namespace moe {
 namespace {
 
 constexpr int kCombThreads = 128;
-constexpr int kMaxStages = 8;
-constexpr int kStageBudget = 108 * 1024;  // dynamic shared memory per block (two blocks per SM)
+constexpr int kDesc = 16;                  // units in flight per block at most
+constexpr int kRingBytes = 108 * 1024;     // dynamic shared memory per block (two blocks per SM)
 
 struct CombineArgs {
     const char *eo;        // [rows, H] bf16
@@ -56,8 +59,8 @@ struct CombineArgs {
     int rowbytes;          // H * 2
     int nch;               // column chunks per row
     int cb;                // chunk bytes (multiple of 16)
-    int stages;
-    int slots;             // K + Ks
+    int ring_bytes;        // shared-memory byte ring per block
+    int group;             // consumer warps per unit (1, 2 or 4)
 };
 
 __device__ __forceinline__ void fma8(float (&acc)[8], float g, const uint4 &v)
@@ -103,21 +106,23 @@ __device__ __forceinline__ bool wait_stage(uint64_t *bar, uint32_t parity)
 template <int K>
 __global__ void __launch_bounds__(kCombThreads + 32) combine_tma_kernel(CombineArgs a)
 {
-    extern __shared__ __align__(128) unsigned char s_stage[];  // [stages][slots][cb]
-    __shared__ uint64_t s_full[kMaxStages];   // producer -> consumers: stage loaded
-    __shared__ uint64_t s_empty[kMaxStages];  // consumers -> producer: stage free
-    __shared__ float s_g[kMaxStages][K];
-    __shared__ int s_n[kMaxStages];
+    extern __shared__ __align__(128) unsigned char s_ring[];  // byte ring of a.ring_bytes
+    __shared__ uint64_t s_full[kDesc];   // producer -> consumers: unit loaded
+    __shared__ uint64_t s_empty[kDesc];  // consumers -> producer: unit consumed
+    __shared__ float s_g[kDesc][K];
+    __shared__ int s_n[kDesc];
+    __shared__ int s_off[kDesc];
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const long long stride = gridDim.x;
-    const size_t stage_bytes = (size_t)a.slots * a.cb;
+    const long long n_units = (a.units - blockIdx.x + stride - 1) / stride;  // units of this block
+    if (n_units <= 0) return;
 
     if (tid == 0) {
-        for (int s = 0; s < a.stages; ++s) {
-            mbar_init(&s_full[s], 1);
-            mbar_init(&s_empty[s], kCombThreads);
+        for (int d = 0; d < kDesc; ++d) {
+            mbar_init(&s_full[d], 1);
+            mbar_init(&s_empty[d], 32 * a.group);  // released by the warps that consumed the unit
         }
         mbar_fence_init();
     }
@@ -127,44 +132,39 @@ __global__ void __launch_bounds__(kCombThreads + 32) combine_tma_kernel(CombineA
 
     if (warp == 0) {
         // ---- producer warp ----------------------------------------------
-        // Lane l fetches the routing metadata (kept rows, gates) of the l-th
-        // unit of the current batch of 32, so one memory round trip serves
-        // 32 stage fills; lane 0 issues the bulk copies.
+        // Lane l fetches the routing metadata of the l-th unit of the current
+        // batch of 32 (one round trip per 32 units); lane 0 allocates each
+        // unit's bytes in the ring and issues its bulk copies.
         const int rows_valid = min(a.r_max, __ldg(a.R_ptr));
-        unsigned issued = 0;  // parity of each stage's last fill (bit) once filled
-        long long i = 0;
+        long long oldest = 0;  // first unit whose bytes are not yet known to be free
+        int head = 0;          // next free byte of the ring
         bool stop = false;
-        for (long long batch = 0; !stop; batch += 32) {
-            const long long ul = blockIdx.x + (batch + lane) * stride;
+        long long i = 0;
+        // wait (bounded) until unit `oldest` has been consumed, then retire it
+        auto retire_oldest = [&]() -> bool {
+            const int d = (int)(oldest % kDesc);
+            const uint32_t par = (uint32_t)((oldest / kDesc) & 1);
+            bool ok = mbar_try_wait(&s_empty[d], par);
+            if (!ok) {
+                const unsigned long long t0 = global_timer_ns();
+                while (!(ok = mbar_try_wait(&s_empty[d], par)) && global_timer_ns() - t0 < kSpinLimitNs) {
+                }
+            }
+            ++oldest;
+            return ok;
+        };
+        for (long long batch = 0; !stop && batch < n_units; batch += 32) {
             int rows[K];
             float g[K];
-            if (ul < a.units) {
-                const long long t = ul / a.nch;
+            if (batch + lane < n_units) {
+                const long long t = (blockIdx.x + (batch + lane) * stride) / a.nch;
 #pragma unroll
                 for (int j = 0; j < K; ++j) {
                     rows[j] = __ldg(a.dst_row + t * K + j);
                     g[j] = __ldg(a.gates + t * K + j);
                 }
             }
-            for (int b = 0; b < 32; ++b, ++i) {
-                const long long u = blockIdx.x + i * stride;
-                if (u >= a.units) { stop = true; break; }
-                const int s = (int)(i % a.stages);
-                const long long use = i / a.stages;  // how many times stage s was filled before
-                if (use > 0) {
-                    bool ok = mbar_try_wait(&s_empty[s], (uint32_t)((use - 1) & 1));
-                    if (!ok) {
-                        const unsigned long long t0 = global_timer_ns();
-                        while (!(ok = mbar_try_wait(&s_empty[s], (uint32_t)((use - 1) & 1))) &&
-                               global_timer_ns() - t0 < kSpinLimitNs) {
-                        }
-                    }
-                    if (!ok) {
-                        if (lane == 0) record_status(a.ws, MOE_ERR_TIMEOUT);
-                        stop = true;
-                        break;
-                    }
-                }
+            for (int b = 0; b < 32 && i < n_units; ++b, ++i) {
                 int rb[K];
                 float gb[K];
 #pragma unroll
@@ -172,7 +172,9 @@ __global__ void __launch_bounds__(kCombThreads + 32) combine_tma_kernel(CombineA
                     rb[j] = __shfl_sync(0xffffffffu, rows[j], b);
                     gb[j] = __shfl_sync(0xffffffffu, g[j], b);
                 }
+                int ok = 1;
                 if (lane == 0) {
+                    const long long u = blockIdx.x + i * stride;
                     const long long t = u / a.nch;
                     const int col0 = (int)(u - t * a.nch) * a.cb;
                     const int bytes = min(a.cb, a.rowbytes - col0);
@@ -183,35 +185,61 @@ __global__ void __launch_bounds__(kCombThreads + 32) combine_tma_kernel(CombineA
                             record_status(a.ws, MOE_ERR_DEVICE_DATA);
                             rb[j] = -1;
                         }
-                        if (rb[j] >= 0) s_g[s][n++] = gb[j];  // gates of the kept slots, in slot order
+                        n += rb[j] >= 0;
                     }
-                    s_n[s] = n;
-                    // expected bytes first (release: s_g / s_n become visible to the waiters)
-                    mbar_arrive_expect_tx(&s_full[s], (uint32_t)((n + a.Ks) * bytes));
-                    unsigned char *st = s_stage + (size_t)s * stage_bytes;
-                    int slot = 0;
-#pragma unroll
-                    for (int j = 0; j < K; ++j) {
-                        if (rb[j] >= 0) {
-                            bulk_load(st + (size_t)slot * a.cb, a.eo + (long long)rb[j] * a.rowbytes + col0,
-                                      bytes, &s_full[s]);
-                            ++slot;
+                    const int need = (n + a.Ks) * bytes;
+                    // a free descriptor, then `need` contiguous ring bytes
+                    while (ok && oldest <= i - kDesc) ok = retire_oldest();
+                    int pos = 0;
+                    while (ok) {
+                        if (oldest == i) { pos = 0; break; }  // nothing in flight
+                        const int tail = s_off[oldest % kDesc];
+                        if (head > tail) {
+                            if (a.ring_bytes - head >= need) { pos = head; break; }
+                            if (tail >= need) { pos = 0; break; }
+                        } else if (tail - head >= need) {
+                            pos = head;
+                            break;
                         }
+                        ok = retire_oldest();
                     }
-                    for (int q = 0; q < a.Ks; ++q)
-                        bulk_load(st + (size_t)(K + q) * a.cb,
-                                  a.shared + ((long long)q * a.T + t) * a.rowbytes + col0, bytes, &s_full[s]);
+                    if (ok) {
+                        const int d = (int)(i % kDesc);
+                        int k2 = 0;
+#pragma unroll
+                        for (int j = 0; j < K; ++j)
+                            if (rb[j] >= 0) s_g[d][k2++] = gb[j];  // kept slots, in slot order
+                        s_n[d] = n;
+                        s_off[d] = pos;
+                        head = pos + need;
+                        // expected bytes first (release: s_g / s_n / s_off visible to the waiters)
+                        mbar_arrive_expect_tx(&s_full[d], (uint32_t)need);
+                        unsigned char *dst = s_ring + pos;
+#pragma unroll
+                        for (int j = 0; j < K; ++j) {
+                            if (rb[j] >= 0) {
+                                bulk_load(dst, a.eo + (long long)rb[j] * a.rowbytes + col0, bytes, &s_full[d]);
+                                dst += bytes;
+                            }
+                        }
+                        for (int q = 0; q < a.Ks; ++q) {
+                            bulk_load(dst, a.shared + ((long long)q * a.T + t) * a.rowbytes + col0, bytes, &s_full[d]);
+                            dst += bytes;
+                        }
+                    } else {
+                        record_status(a.ws, MOE_ERR_TIMEOUT);
+                    }
                 }
-                issued = (issued & ~(1u << s)) | ((unsigned)(use & 1) << s) | (1u << (s + 16));
+                if (!__shfl_sync(0xffffffffu, ok, 0)) { stop = true; break; }
             }
         }
         // drain: never leave with copies still landing in this block's shared memory
         if (lane == 0) {
-            for (int s = 0; s < a.stages; ++s) {
-                if (!(issued & (1u << (s + 16)))) continue;
-                const uint32_t par = (issued >> s) & 1u;
+            for (long long q = oldest; q < i; ++q) {
+                const int d = (int)(q % kDesc);
                 const unsigned long long t0 = global_timer_ns();
-                while (!mbar_try_wait(&s_full[s], par) && global_timer_ns() - t0 < kSpinLimitNs) {
+                while (!mbar_try_wait(&s_full[d], (uint32_t)((q / kDesc) & 1)) &&
+                       global_timer_ns() - t0 < kSpinLimitNs) {
                 }
             }
         }
@@ -219,28 +247,36 @@ __global__ void __launch_bounds__(kCombThreads + 32) combine_tma_kernel(CombineA
     }
 
     // ---- consumer warps ---------------------------------------------------
-    const int ct = tid - 32;
-    long long i = 0;
-    for (long long u = blockIdx.x; u < a.units; u += stride, ++i) {
-        const int s = (int)(i % a.stages);
-        const uint32_t par = (uint32_t)((i / a.stages) & 1);
-        if (!wait_stage(&s_full[s], par)) {
-            if (ct == 0) record_status(a.ws, MOE_ERR_TIMEOUT);
+    // Groups of a.group warps consume units round-robin: with one-warp groups
+    // four units are combined concurrently (small units do not serialise);
+    // with one four-warp group a large unit is spread over 128 threads.
+    const int cw = warp - 1;
+    constexpr int kConsumerWarps = kCombThreads / 32;
+    const int ngroups = kConsumerWarps / a.group;
+    const int grp = cw / a.group;
+    const int gt = (cw - grp * a.group) * 32 + lane;  // thread index within the group
+    const int gthreads = 32 * a.group;
+    for (long long i = grp; i < n_units; i += ngroups) {
+        const int d = (int)(i % kDesc);
+        if (!wait_stage(&s_full[d], (uint32_t)((i / kDesc) & 1))) {
+            if (gt == 0) record_status(a.ws, MOE_ERR_TIMEOUT);
             return;
         }
+        const long long u = blockIdx.x + i * stride;
         const long long t = u / a.nch;
         const int col0 = (int)(u - t * a.nch) * a.cb;
-        const int nv = min(a.cb, a.rowbytes - col0) >> 4;
-        const int n = s_n[s];
-        const unsigned char *st = s_stage + (size_t)s * stage_bytes;
+        const int bytes = min(a.cb, a.rowbytes - col0);
+        const int nv = bytes >> 4;
+        const int n = s_n[d];
+        const unsigned char *st = s_ring + s_off[d];
         uint4 *yrow = reinterpret_cast<uint4 *>(a.y + t * a.rowbytes + col0);
-        for (int v = ct; v < nv; v += kCombThreads) {
+        for (int v = gt; v < nv; v += gthreads) {
             float acc[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
             // pinned order: kept slots ascending, then shared experts ascending
-            for (int r = 0; r < n; ++r) fma8(acc, s_g[s][r], lds_v4(st + (size_t)r * a.cb + v * 16));
-            for (int q = 0; q < a.Ks; ++q) add8(acc, lds_v4(st + (size_t)(K + q) * a.cb + v * 16));
+            for (int r = 0; r < n; ++r) fma8(acc, s_g[d][r], lds_v4(st + (size_t)r * bytes + v * 16));
+            for (int q = 0; q < a.Ks; ++q) add8(acc, lds_v4(st + (size_t)(n + q) * bytes + v * 16));
             uint4 o;
             o.x = pack_bf16x2(acc[0], acc[1]);
             o.y = pack_bf16x2(acc[2], acc[3]);
@@ -248,7 +284,7 @@ __global__ void __launch_bounds__(kCombThreads + 32) combine_tma_kernel(CombineA
             o.w = pack_bf16x2(acc[6], acc[7]);
             st_v4(yrow + v, o);
         }
-        mbar_arrive(&s_empty[s]);
+        mbar_arrive(&s_empty[d]);
     }
 }
 
@@ -273,9 +309,9 @@ template <int K>
 cudaError_t launch_k(const CombineArgs &a, cudaStream_t s)
 {
     const void *fn = reinterpret_cast<const void *>(combine_tma_kernel<K>);
-    const size_t smem = (size_t)a.stages * a.slots * a.cb;
+    const size_t smem = (size_t)a.ring_bytes;
     if (smem > 48 * 1024) {
-        cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kStageBudget);
+        cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
         if (err != cudaSuccess) return err;
     }
     const long long resident = (long long)device_sm_count() * blocks_per_sm(fn, smem);
@@ -301,15 +337,16 @@ cudaError_t launch_combine(const void *eo, const moe_layout *L, const float *gat
     a.r_max = L->r_max;
     a.Ks = Ks;
     a.rowbytes = H * 2;
-    a.slots = L->k + Ks;
-    // Chunk the row so that at least three stages fit the budget, then use as
-    // many stages (<= kMaxStages) as the budget holds.
-    const int cb_max = (kStageBudget / 3 / a.slots) & ~15;
+    // Whole rows per unit unless a unit with every slot kept would take more
+    // than 60% of the ring; then equal 16-byte-aligned column chunks.
+    const int slots = L->k + Ks;
+    const int cb_max = (kRingBytes * 3 / 5 / slots) & ~15;
     a.nch = (a.rowbytes + cb_max - 1) / cb_max;
     a.cb = (((a.rowbytes + a.nch - 1) / a.nch) + 15) & ~15;
-    a.stages = kStageBudget / (a.slots * a.cb);
-    if (a.stages > kMaxStages) a.stages = kMaxStages;
-    if (a.stages < 1) return cudaErrorInvalidValue;
+    a.ring_bytes = kRingBytes;
+    // a unit of >= 32 KiB (all slots kept) is shared by all four consumer
+    // warps; smaller units go one per warp
+    a.group = (slots * a.cb >= 32 * 1024) ? 4 : 1;
     a.units = (long long)T * a.nch;
     switch (L->k) {
 #define MOE_COMBINE_CASE(KK) \
