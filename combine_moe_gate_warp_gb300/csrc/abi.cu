@@ -3,6 +3,10 @@
 // they are bad) and then launches the kernels of one step on `stream`.
 #include <stdint.h>
 
+#include <map>
+#include <mutex>
+#include <utility>
+
 #include "common.cuh"
 
 namespace moe {
@@ -19,6 +23,23 @@ int device_sm_count()
         cached[dev] = n;
     }
     return cached[dev];
+}
+
+cudaError_t allow_dynamic_smem(const void *fn, int bytes)
+{
+    // The attribute is a per-kernel maximum: only ever raise it, so a later
+    // smaller request never lowers the limit a larger launch relies on.
+    static std::mutex mu;
+    static std::map<std::pair<const void *, int>, int> limit;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    std::lock_guard<std::mutex> lock(mu);
+    int &cur = limit[std::make_pair(fn, dev)];
+    if (bytes <= cur) return cudaSuccess;
+    err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (err == cudaSuccess) cur = bytes;
+    return err;
 }
 
 }  // namespace moe

@@ -42,7 +42,7 @@ namespace {
 
 constexpr int kCombThreads = 128;
 constexpr int kDesc = 16;                  // units in flight per block at most
-constexpr int kRingBytes = 108 * 1024;     // dynamic shared memory per block (two blocks per SM)
+constexpr int kRingBytes = 108 * 1024;     // byte ring per block: two blocks per SM
 
 struct CombineArgs {
     const char *eo;        // [rows, H] bf16
@@ -310,10 +310,8 @@ cudaError_t launch_k(const CombineArgs &a, cudaStream_t s)
 {
     const void *fn = reinterpret_cast<const void *>(combine_tma_kernel<K>);
     const size_t smem = (size_t)a.ring_bytes;
-    if (smem > 48 * 1024) {
-        cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
-        if (err != cudaSuccess) return err;
-    }
+    cudaError_t err = allow_dynamic_smem(fn, (int)smem);
+    if (err != cudaSuccess) return err;
     const long long resident = (long long)device_sm_count() * blocks_per_sm(fn, smem);
     const unsigned grid = (unsigned)(a.units < resident ? a.units : resident);
     return launch_pdl(combine_tma_kernel<K>, dim3(grid), dim3(kCombThreads + 32), smem, s, a);

@@ -39,13 +39,13 @@ __host__ __device__ inline unsigned long long *ws_flags(void *ws)
     return reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + kWsHeaderBytes);
 }
 
-// Layout tiling.  A tile holds tile_tokens(T, k) consecutive tokens, i.e.
-// up to kLayoutMaxTileAssign assignments: about A/256 assignments rounded up
-// to a multiple of 1024, within [1024, 8192], so large problems use at most
-// ~256 tiles (short look-back chains) and small ones still spread over many
-// blocks.  The rule depends only on (T, k): the workspace size is known on
-// the host without a device.  T*k < 2^30 keeps every count inside the
-// 30-bit value field of a flag word.
+// Layout tiling.  A tile holds layout_tile_tokens(T, k) consecutive tokens,
+// i.e. up to kLayoutMaxTileAssign assignments: about A/256 assignments
+// rounded up to a multiple of 1024, within [1024, 8192], so that large
+// problems use ~256 tiles (short look-back chains) and small ones still
+// spread over many blocks.  The rule depends only on (T, k): the
+// workspace size is known on the host without a device.  T*k < 2^30 keeps
+// every count inside the 30-bit value field of a flag word.
 constexpr int kLayoutThreads = 256;
 constexpr int kLayoutWarps = kLayoutThreads / 32;
 constexpr int kLayoutMinTileAssign = 1024;
@@ -141,6 +141,10 @@ cudaError_t launch_dispatch_fp8(const void *x, int T, int H, const moe_layout *L
 cudaError_t launch_combine(const void *eo, const moe_layout *L, const float *gates,
                            const void *shared, int Ks, int T, int H, void *y, cudaStream_t s);
 int device_sm_count();
+
+// Allow `fn` up to `bytes` of dynamic shared memory on the current device
+// (once per kernel, device and size; static + dynamic above 48 KiB needs it).
+cudaError_t allow_dynamic_smem(const void *fn, int bytes);
 
 // Launch `kernel` on `s` with programmatic stream serialization allowed.
 template <typename... KArgs, typename... Args>

@@ -148,10 +148,12 @@ gate_kernel(const float *__restrict__ logits, int T, int E, int32_t *__restrict_
     }
     __syncthreads();
 
-    if (threadIdx.x < rows) {
+    float bv[K];
+    int bi[K];
+    float g[K];
+    const bool active = threadIdx.x < rows;
+    if (active) {
         const float *row = s_logit + threadIdx.x * stride;
-        float bv[K];
-        int bi[K];
         bool finite = true;
         // First K experts: insertion-sorted in place.
 #pragma unroll
@@ -179,7 +181,6 @@ gate_kernel(const float *__restrict__ logits, int T, int E, int32_t *__restrict_
 
         // Gate weights, fp32, shifted by the largest logit.
         const float m = bv[0];
-        float g[K];
         if constexpr (MODE == MOE_TOPK_SOFTMAX) {
             float ex[K];
             float sum = 0.0f;
@@ -197,20 +198,24 @@ gate_kernel(const float *__restrict__ logits, int T, int E, int32_t *__restrict_
             for (int j = 0; j < K; ++j) g[j] = __fdiv_rn(expf(__fsub_rn(bv[j], m)), sum);
         }
 
-        const long long t = t0 + threadIdx.x;
-        store_row_i32<K>(topk_idx + t * K, bi);
-        store_row_f32<K>(gates + t * K, g);
 #pragma unroll
         for (int j = 0; j < K; ++j) atomicAdd(&s_hist[bi[j]], 1u);
     }
     __syncthreads();
 
+    // counts first: the fence before the ticket then covers only these few
+    // atomics, not the block's output stores, which follow it
     for (int e = threadIdx.x; e < E; e += blockDim.x)
         if (s_hist[e]) atomicAdd(&ws->gate_counts[e], s_hist[e]);
     if (threadIdx.x == 0 && s_bad) record_status(ws, MOE_ERR_DEVICE_DATA);
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) s_last = (atomicAdd(&ws->gate_ticket, 1u) == gridDim.x - 1);
+    if (active) {
+        const long long t = t0 + threadIdx.x;
+        store_row_i32<K>(topk_idx + t * K, bi);
+        store_row_f32<K>(gates + t * K, g);
+    }
     __syncthreads();
     if (!s_last) return;
 
@@ -266,13 +271,8 @@ cudaError_t launch_k(const float *logits, int T, int E, int32_t *idx, float *gat
     const long long want_blocks = 2LL * device_sm_count();
     while (tt > 64 && ((long long)T + tt - 1) / tt < want_blocks) tt >>= 1;
     const size_t smem = (size_t)tt * stride * sizeof(float);
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t err = cudaFuncSetAttribute(gate_kernel<K, MODE>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
-        if (err != cudaSuccess) return err;
-        attr_set = true;
-    }
+    cudaError_t err = allow_dynamic_smem(reinterpret_cast<const void *>(gate_kernel<K, MODE>), (int)smem);
+    if (err != cudaSuccess) return err;
     long long blocks = ((long long)T + tt - 1) / tt;
     if (blocks < 1) blocks = 1;
     return launch_pdl(gate_kernel<K, MODE>, dim3((unsigned)blocks), dim3(tt), smem, s, logits, T, E, idx, gates,

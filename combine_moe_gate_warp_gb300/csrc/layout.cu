@@ -20,9 +20,10 @@
 //      expert) carries an epoch tag, a state (aggregate / inclusive prefix)
 //      and the 30-bit value, so no flag array ever needs clearing.  The
 //      whole block looks back at once: 256/E threads per expert each read
-//      one predecessor's word per round, so a round covers 256/E tiles for
-//      every expert with a single memory round trip.  Every wait is bounded
-//      by %globaltimer and records MOE_ERR_TIMEOUT instead of hanging.
+//      four predecessors' words per round, so a round covers 1024/E tiles
+//      for every expert with a single memory round trip.  Every wait is
+//      bounded by %globaltimer and records MOE_ERR_TIMEOUT instead of
+//      hanging.
 //   4. Rank r = prefix + warp offset + local rank; kept iff r < capacity;
 //      dst_row / src_pos / capacity_mask written, dropped gates zeroed.
 //   5. Distinct-partition tokens per tile, summed with integer atomics; the
@@ -33,6 +34,7 @@ namespace moe {
 namespace {
 
 constexpr int kLoadBatch = 8;  // expert-id loads in flight per thread
+constexpr int kLookPer = 4;    // look-back words read per thread per round
 
 struct LayoutArgs {
     const int32_t *idx;
@@ -66,7 +68,7 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
     __shared__ unsigned s_excl[MOE_MAX_EXPERTS];
     __shared__ int s_base[MOE_MAX_EXPERTS];
     __shared__ unsigned s_ptok[MOE_MAX_EXPERTS];
-    __shared__ unsigned long long s_win[kLayoutThreads];
+    __shared__ unsigned long long s_win[kLookPer * kLayoutThreads];
     __shared__ unsigned s_warp_tot[kLayoutWarps];
     __shared__ unsigned s_tile, s_epoch;
     __shared__ int s_last, s_bad, s_skip, s_abort;
@@ -187,18 +189,24 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
     }
     __syncthreads();
 
-    // 3. block-wide decoupled look-back
+    // 3. block-wide decoupled look-back: each round, thread (e, w) reads the
+    // flag words of kLookPer predecessors of expert e, so a round covers
+    // kLookPer * 256/E tiles per expert with one memory round trip
     {
-        const int W = kLayoutThreads / E;  // predecessors read per expert per round
+        const int W = kLayoutThreads / E;  // threads per expert
         const int my_e = tid / W, my_w = tid - (tid / W) * W;
         unsigned long long t_start = 0;
         while (true) {
             if (my_e < E) {
                 const int b = s_base[my_e];
                 if (b >= 0) {
-                    const int p = b - my_w;
-                    s_win[tid] = (p >= 0) ? ld_volatile_u64(flags + (size_t)p * E + my_e)
-                                          : make_flag(epoch, kFlagInclusive, 0u);
+#pragma unroll
+                    for (int q = 0; q < kLookPer; ++q) {
+                        const int p = b - (q * W + my_w);
+                        s_win[q * kLayoutThreads + tid] =
+                            (p >= 0) ? ld_volatile_u64(flags + (size_t)p * E + my_e)
+                                     : make_flag(epoch, kFlagInclusive, 0u);
+                    }
                 }
             }
             __syncthreads();
@@ -207,13 +215,15 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
                 unsigned add = 0;
                 int used = 0;
                 bool done = false;
-                for (int w = 0; w < W; ++w) {
-                    const unsigned long long f = s_win[tid * W + w];
-                    const unsigned state = (unsigned)(f >> 30) & 3u;
-                    if ((unsigned)(f >> 32) != epoch || state == 0u) break;  // not published yet
-                    add += (unsigned)(f & 0x3FFFFFFFull);
-                    ++used;
-                    if (state == (unsigned)kFlagInclusive) { done = true; break; }
+                for (int q = 0; q < kLookPer && !done; ++q) {
+                    for (int w = 0; w < W; ++w) {
+                        const unsigned long long f = s_win[q * kLayoutThreads + tid * W + w];
+                        const unsigned state = (unsigned)(f >> 30) & 3u;
+                        if ((unsigned)(f >> 32) != epoch || state == 0u) { q = kLookPer; break; }  // not published yet
+                        add += (unsigned)(f & 0x3FFFFFFFull);
+                        ++used;
+                        if (state == (unsigned)kFlagInclusive) { done = true; break; }
+                    }
                 }
                 s_excl[tid] += add;
                 s_base[tid] = done ? -1 : s_base[tid] - used;
@@ -241,30 +251,20 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
     }
     __syncthreads();
 
-    // 4. ranks -> rows
+    // 4. ranks -> rows (kept to shared memory first: the completion step
+    // below must not wait behind this block's output stores)
     for (int i = tid; i < A; i += kLayoutThreads) {
-        const long long as = a0 + i;
         const int e = s_idx[i];
-        int kept = 0;
+        int row = -1;
         if (e < E) {
             const unsigned r = s_excl[e] + s_whist[i / per_warp][e] + (unsigned)s_rank[i];
             if (r < a.cap) {
-                const int row = s_off[e] + (int)r;
-                if (row < s_off[e + 1] && row < a.r_max) {
-                    a.dst_row[as] = row;
-                    a.src_pos[row] = (int32_t)as;
-                    kept = 1;
-                } else {
-                    s_bad = 1;  // counts do not match the ids: keep writes in bounds
-                }
+                const int cand = s_off[e] + (int)r;
+                if (cand < s_off[e + 1] && cand < a.r_max) row = cand;
+                else s_bad = 1;  // counts do not match the ids: keep writes in bounds
             }
         }
-        if (!kept) {
-            a.dst_row[as] = -1;
-            if (a.gates) a.gates[as] = 0.0f;
-        }
-        a.cmask[as] = (uint8_t)kept;
-        s_rank[i] = kept;
+        s_rank[i] = row;
     }
     __syncthreads();
 
@@ -274,12 +274,12 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
     for (int tl = tid; tl < ntok; tl += kLayoutThreads) {
         for (int j = 0; j < k; ++j) {
             const int i = tl * k + j;
-            if (!s_rank[i]) continue;
+            if (s_rank[i] < 0) continue;
             const int p = s_idx[i] / per;
             bool first = true;
             for (int jj = 0; jj < j; ++jj) {
                 const int ii = tl * k + jj;
-                if (s_rank[ii] && s_idx[ii] / per == p) { first = false; break; }
+                if (s_rank[ii] >= 0 && s_idx[ii] / per == p) { first = false; break; }
             }
             if (first) atomicAdd(&s_ptok[p], 1u);
         }
@@ -288,8 +288,35 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
     for (int p = tid; p < a.P; p += kLayoutThreads)
         if (s_ptok[p]) atomicAdd(&ws->part_tok[p], s_ptok[p]);
 
-    // tile 0 publishes the per-expert / per-partition summary
-    if (tile == 0) {
+    // completion: the last tile to get here publishes partition tokens and
+    // returns every counter to zero; the epoch bump retires this call's flags
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = (atomicAdd(&ws->done_ctr, 1u) == (unsigned)a.ntiles - 1);
+    __syncthreads();
+    if (s_last) {
+        __threadfence();
+        for (int p = tid; p < a.P; p += kLayoutThreads)
+            a.part_tokens[p] = (int32_t)atomicExch(&ws->part_tok[p], 0u);
+        if (tid == 0) {
+            ws->done_ctr = 0u;
+            ws->tile_ctr = 0u;
+            ws->inject_skip_publish = 0u;
+            __threadfence();
+            ws->epoch = epoch + 1u;
+        }
+    }
+
+    // outputs of this tile (no block reads the workspace after this point)
+    for (int i = tid; i < A; i += kLayoutThreads) {
+        const long long as = a0 + i;
+        const int row = s_rank[i];
+        a.dst_row[as] = row;
+        a.cmask[as] = (uint8_t)(row >= 0);
+        if (row >= 0) a.src_pos[row] = (int32_t)as;
+        else if (a.gates) a.gates[as] = 0.0f;
+    }
+    if (tile == 0) {  // the per-expert / per-partition summary
         for (int e = tid; e < E; e += kLayoutThreads) a.counts_out[e] = s_off[e + 1] - s_off[e];
         for (int e = tid; e <= E; e += kLayoutThreads) a.offsets[e] = s_off[e];
         for (int p = tid; p < a.P; p += kLayoutThreads) {
@@ -301,25 +328,8 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
             *a.dropped = (int64_t)a.T * k - s_off[E];
         }
     }
+    __syncthreads();
     if (tid == 0 && s_bad) record_status(a.ws, MOE_ERR_DEVICE_DATA);
-
-    // completion: the last tile to finish publishes partition tokens and
-    // returns every counter to zero; the epoch bump retires this call's flags
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) s_last = (atomicAdd(&ws->done_ctr, 1u) == (unsigned)a.ntiles - 1);
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    for (int p = tid; p < a.P; p += kLayoutThreads)
-        a.part_tokens[p] = (int32_t)atomicExch(&ws->part_tok[p], 0u);
-    if (tid == 0) {
-        ws->done_ctr = 0u;
-        ws->tile_ctr = 0u;
-        ws->inject_skip_publish = 0u;
-        __threadfence();
-        ws->epoch = epoch + 1u;
-    }
 }
 
 }  // namespace
@@ -351,11 +361,8 @@ cudaError_t launch_layout(const int32_t *topk_idx, const int32_t *counts_in, int
     a.dropped = L->dropped;
     a.ws = ws;
     const size_t smem = 2 * sizeof(int) * (size_t)a.tile_tokens * k;
-    if (smem > 48 * 1024) {
-        cudaError_t err = cudaFuncSetAttribute(layout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)(2 * sizeof(int) * kLayoutMaxTileAssign));
-        if (err != cudaSuccess) return err;
-    }
+    cudaError_t err = allow_dynamic_smem(reinterpret_cast<const void *>(layout_kernel), (int)smem);
+    if (err != cudaSuccess) return err;
     return launch_pdl(layout_kernel, dim3(a.ntiles), dim3(kLayoutThreads), smem, s, a);
 }
 
