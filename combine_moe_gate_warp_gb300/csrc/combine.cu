@@ -41,8 +41,21 @@ namespace moe {
 namespace {
 
 constexpr int kCombThreads = 128;
-constexpr int kDesc = 16;                  // units in flight per block at most
-constexpr int kRingBytes = 108 * 1024;     // byte ring per block: two blocks per SM
+// Ring policy (compile-time): ring size per block, the share of the ring a
+// fully kept unit may take before rows are split into column chunks (in
+// percent), and the unit size from which all four consumer warps share a
+// unit.
+#ifndef MOE_COMBINE_RING_KB
+#define MOE_COMBINE_RING_KB 108
+#endif
+#ifndef MOE_COMBINE_UNIT_PCT
+#define MOE_COMBINE_UNIT_PCT 60
+#endif
+#ifndef MOE_COMBINE_GROUP_KB
+#define MOE_COMBINE_GROUP_KB 32
+#endif
+constexpr int kDesc = 16;                                  // units in flight per block at most
+constexpr int kRingBytes = MOE_COMBINE_RING_KB * 1024;     // byte ring per block (108 KiB: two blocks per SM)
 
 struct CombineArgs {
     const char *eo;        // [rows, H] bf16
@@ -336,15 +349,16 @@ cudaError_t launch_combine(const void *eo, const moe_layout *L, const float *gat
     a.Ks = Ks;
     a.rowbytes = H * 2;
     // Whole rows per unit unless a unit with every slot kept would take more
-    // than 60% of the ring; then equal 16-byte-aligned column chunks.
+    // than MOE_COMBINE_UNIT_PCT% of the ring; then equal 16-byte-aligned
+    // column chunks.
     const int slots = L->k + Ks;
-    const int cb_max = (kRingBytes * 3 / 5 / slots) & ~15;
+    const int cb_max = (kRingBytes / 100 * MOE_COMBINE_UNIT_PCT / slots) & ~15;
     a.nch = (a.rowbytes + cb_max - 1) / cb_max;
     a.cb = (((a.rowbytes + a.nch - 1) / a.nch) + 15) & ~15;
     a.ring_bytes = kRingBytes;
-    // a unit of >= 32 KiB (all slots kept) is shared by all four consumer
-    // warps; smaller units go one per warp
-    a.group = (slots * a.cb >= 32 * 1024) ? 4 : 1;
+    // a unit of >= MOE_COMBINE_GROUP_KB KiB (all slots kept) is shared by all
+    // four consumer warps; smaller units go one per warp
+    a.group = (slots * a.cb >= MOE_COMBINE_GROUP_KB * 1024) ? 4 : 1;
     a.units = (long long)T * a.nch;
     switch (L->k) {
 #define MOE_COMBINE_CASE(KK) \

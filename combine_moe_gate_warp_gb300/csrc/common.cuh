@@ -17,16 +17,18 @@ namespace moe {
 // a zeroed workspace stays valid from call to call.
 // ---------------------------------------------------------------------------
 struct WsHeader {
-    unsigned status;        // first device error wins (atomicCAS from 0)
-    unsigned epoch;         // bumped once per layout launch; tags flag words
-    unsigned tile_ctr;      // layout: dynamic tile ids
-    unsigned done_ctr;      // layout: completed tiles
-    unsigned gate_ticket;   // gate: finished blocks
+    unsigned status;               // first device error wins (atomicCAS from 0)
+    unsigned done_ctr;             // layout: completed tiles
+    unsigned gate_ticket;          // gate: finished blocks
     // Failure-injection hook for tests, written only from the host: when it
     // holds tile+1, that layout tile does not publish its look-back flags,
     // so its successor's bounded wait expires (MOE_ERR_TIMEOUT).  Zero in
     // normal use; the layout call that sees it clears it.
     unsigned inject_skip_publish;
+    // layout: {tile id (low 32 bits), epoch (high 32 bits)} in one word, so a
+    // block learns both with a single atomic; the epoch tags flag words and
+    // is bumped by the block that draws the last tile id of a call
+    unsigned long long tile_epoch;
     unsigned pad0[26];
     unsigned gate_counts[MOE_MAX_EXPERTS];  // gate: per-expert totals
     unsigned part_tok[MOE_MAX_EXPERTS];     // layout: per-partition token totals

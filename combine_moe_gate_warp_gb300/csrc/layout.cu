@@ -26,8 +26,11 @@
 //      hanging.
 //   4. Rank r = prefix + warp offset + local rank; kept iff r < capacity;
 //      dst_row / src_pos / capacity_mask written, dropped gates zeroed.
-//   5. Distinct-partition tokens per tile, summed with integer atomics; the
-//      last block to finish publishes them and resets the counters.
+//   5. Distinct-partition tokens: a kept assignment counts when no earlier
+//      kept slot of its token falls in the same partition; warp-aggregated,
+//      then summed over tiles with integer atomics; the last block to finish
+//      publishes them.  Output stores come last, after the completion
+//      ticket, so no fence waits behind them.
 #include "common.cuh"
 
 namespace moe {
@@ -35,6 +38,7 @@ namespace {
 
 constexpr int kLoadBatch = 8;  // expert-id loads in flight per thread
 constexpr int kLookPer = 4;    // look-back words read per thread per round
+constexpr int kSpecLoads = kLoadBatch;  // ids of the guessed tile fetched before the tile id is known
 
 struct LayoutArgs {
     const int32_t *idx;
@@ -68,6 +72,7 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
     __shared__ unsigned s_excl[MOE_MAX_EXPERTS];
     __shared__ int s_base[MOE_MAX_EXPERTS];
     __shared__ unsigned s_ptok[MOE_MAX_EXPERTS];
+    __shared__ int s_epart[MOE_MAX_EXPERTS];  // partition of each expert
     __shared__ unsigned long long s_win[kLookPer * kLayoutThreads];
     __shared__ unsigned s_warp_tot[kLayoutWarps];
     __shared__ unsigned s_tile, s_epoch;
@@ -84,10 +89,13 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
     pdl_launch_dependents();
     const int raw_count = (tid < E) ? __ldg(a.counts_in + tid) : 0;
     if (tid == 0) {
-        unsigned ep = *reinterpret_cast<volatile unsigned *>(&ws->epoch);
-        __threadfence();
-        s_tile = atomicAdd(&ws->tile_ctr, 1u);
-        s_epoch = ep;
+        const unsigned long long te = atomicAdd(&ws->tile_epoch, 1ull);
+        s_tile = (unsigned)te;
+        s_epoch = (unsigned)(te >> 32);
+        // the block that draws the last tile id retires this call's epoch:
+        // every other block of the call has drawn (and knows the epoch)
+        if (s_tile == (unsigned)a.ntiles - 1)
+            atomicExch(&ws->tile_epoch, (unsigned long long)(s_epoch + 1u) << 32);
         s_bad = 0;
         s_abort = 0;
         s_skip = (*reinterpret_cast<volatile unsigned *>(&ws->inject_skip_publish) == s_tile + 1u);
@@ -95,6 +103,23 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
     for (int i = tid; i < kLayoutWarps * MOE_MAX_EXPERTS; i += kLayoutThreads)
         (&s_whist[0][0])[i] = 0u;
     for (int p = tid; p < a.P; p += kLayoutThreads) s_ptok[p] = 0u;
+    const int per = E / a.P;
+    for (int e = tid; e < E; e += kLayoutThreads) s_epart[e] = e / per;
+
+    // Tiles are drawn in launch order, so this block almost always gets tile
+    // blockIdx.x: fetch that tile's expert ids while the tile-id atomic is in
+    // flight, and fetch again only if the guess was wrong.
+    int v[kSpecLoads];
+    {
+        const long long g0 = (long long)blockIdx.x * a.tile_tokens;
+        const long long g1 = min((long long)a.T, g0 + a.tile_tokens);
+        const int gA = (int)(max(0LL, g1 - g0) * k);
+#pragma unroll
+        for (int u = 0; u < kSpecLoads; ++u) {
+            const int i = u * kLayoutThreads + tid;
+            if (i < gA) v[u] = __ldg(a.idx + g0 * k + i);
+        }
+    }
     __syncthreads();
 
     const unsigned tile = s_tile, epoch = s_epoch;
@@ -107,20 +132,22 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
     const long long a0 = tok0 * k;
     const int A = (int)(max(0LL, tok1 - tok0) * k);
 
-    // the tile's expert ids, kLoadBatch loads in flight per thread; ids
+    // the tile's expert ids (kLoadBatch loads in flight per thread); ids
     // outside [0, E) become the sentinel E
+    const bool guessed = (tile == blockIdx.x);
     for (int base = 0; base < A; base += kLoadBatch * kLayoutThreads) {
-        int v[kLoadBatch];
+        int w[kLoadBatch];
+        const bool spec = guessed && base == 0;
 #pragma unroll
         for (int u = 0; u < kLoadBatch; ++u) {
             const int i = base + u * kLayoutThreads + tid;
-            if (i < A) v[u] = __ldg(a.idx + a0 + i);
+            if (i < A) w[u] = spec ? v[u] : __ldg(a.idx + a0 + i);
         }
 #pragma unroll
         for (int u = 0; u < kLoadBatch; ++u) {
             const int i = base + u * kLayoutThreads + tid;
             if (i < A) {
-                int e = v[u];
+                int e = w[u];
                 if (e < 0 || e >= E) { e = E; s_bad = 1; }
                 s_idx[i] = e;
             }
@@ -166,7 +193,7 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
             __syncwarp();
             if (counted && rank == 0) s_whist[warp][e] = before + __popc(peers);
             __syncwarp();
-            if (valid) s_rank[i] = counted ? (int)(before + rank) : -1;
+            if (valid) s_rank[i] = counted ? (int)(((unsigned)warp << 24) | (before + rank)) : -1;
         }
     }
     __syncthreads();
@@ -251,37 +278,46 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
     }
     __syncthreads();
 
-    // 4. ranks -> rows (kept to shared memory first: the completion step
-    // below must not wait behind this block's output stores)
-    for (int i = tid; i < A; i += kLayoutThreads) {
-        const int e = s_idx[i];
-        int row = -1;
-        if (e < E) {
-            const unsigned r = s_excl[e] + s_whist[i / per_warp][e] + (unsigned)s_rank[i];
-            if (r < a.cap) {
-                const int cand = s_off[e] + (int)r;
-                if (cand < s_off[e + 1] && cand < a.r_max) row = cand;
-                else s_bad = 1;  // counts do not match the ids: keep writes in bounds
-            }
-        }
-        s_rank[i] = row;
-    }
-    __syncthreads();
-
-    // 5. tokens with >= 1 kept assignment per partition (distinct partitions)
-    const int per = E / a.P;
+    // 4+5. ranks -> rows, one thread per token, kept in shared memory first
+    // (the completion step below must not wait behind this block's output
+    // stores); s_rank[i] becomes the packed row or -1.  A token counts once
+    // for every partition holding at least one of its kept slots (partition
+    // bitmask when P <= 64, pairwise check otherwise).
     const int ntok = (int)max(0LL, tok1 - tok0);
     for (int tl = tid; tl < ntok; tl += kLayoutThreads) {
+        unsigned long long pmask = 0ull;
         for (int j = 0; j < k; ++j) {
             const int i = tl * k + j;
-            if (s_rank[i] < 0) continue;
-            const int p = s_idx[i] / per;
-            bool first = true;
-            for (int jj = 0; jj < j; ++jj) {
-                const int ii = tl * k + jj;
-                if (s_rank[ii] >= 0 && s_idx[ii] / per == p) { first = false; break; }
+            const int e = s_idx[i];
+            int row = -1;
+            if (e < E) {
+                const unsigned pr = (unsigned)s_rank[i];
+                const unsigned r = s_excl[e] + s_whist[pr >> 24][e] + (pr & 0xFFFFFFu);
+                if (r < a.cap) {
+                    const int cand = s_off[e] + (int)r;
+                    if (cand < s_off[e + 1] && cand < a.r_max) row = cand;
+                    else s_bad = 1;  // counts do not match the ids: keep writes in bounds
+                }
             }
-            if (first) atomicAdd(&s_ptok[p], 1u);
+            s_rank[i] = row;
+            if (row >= 0) {
+                const int p = s_epart[e];
+                if (a.P <= 64) {
+                    pmask |= 1ull << p;
+                } else {
+                    bool first = true;
+                    for (int jj = 0; jj < j; ++jj) {
+                        const int ii = tl * k + jj;
+                        if (s_rank[ii] >= 0 && s_epart[s_idx[ii]] == p) { first = false; break; }
+                    }
+                    if (first) atomicAdd(&s_ptok[p], 1u);
+                }
+            }
+        }
+        while (pmask) {
+            const int p = __ffsll((long long)pmask) - 1;
+            pmask &= pmask - 1;
+            atomicAdd(&s_ptok[p], 1u);
         }
     }
     __syncthreads();
@@ -289,7 +325,8 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
         if (s_ptok[p]) atomicAdd(&ws->part_tok[p], s_ptok[p]);
 
     // completion: the last tile to get here publishes partition tokens and
-    // returns every counter to zero; the epoch bump retires this call's flags
+    // returns the done counter and the test hook to zero (the tile/epoch word
+    // was advanced when the last tile id was drawn)
     __threadfence();
     __syncthreads();
     if (tid == 0) s_last = (atomicAdd(&ws->done_ctr, 1u) == (unsigned)a.ntiles - 1);
@@ -300,10 +337,7 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
             a.part_tokens[p] = (int32_t)atomicExch(&ws->part_tok[p], 0u);
         if (tid == 0) {
             ws->done_ctr = 0u;
-            ws->tile_ctr = 0u;
             ws->inject_skip_publish = 0u;
-            __threadfence();
-            ws->epoch = epoch + 1u;
         }
     }
 

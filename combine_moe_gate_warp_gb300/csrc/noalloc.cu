@@ -59,13 +59,15 @@ extern "C" moe_status moe_dispatch_layout_noalloc(const int32_t *topk_idx, const
     moe_status st = scratch_address(&scratch);
     if (st != MOE_OK) return st;
     // Counters that each layout call expects at zero (they are reset by a
-    // completed call; an aborted one could leave them dirty).  The status
-    // word and the flag epoch are kept: the epoch tags old flag words so they
-    // are never mistaken for this call's.
+    // completed call; an aborted one could leave them dirty): the done and
+    // gate tickets, the test hook, the tile-id half of the tile/epoch word,
+    // and the partition-token totals.  The status word and the flag epoch
+    // are kept: the epoch tags old flag words so they are never mistaken for
+    // this call's.
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     char *base = static_cast<char *>(scratch);
-    const size_t c0 = offsetof(moe::WsHeader, tile_ctr);
-    const size_t c1 = offsetof(moe::WsHeader, pad0);
+    const size_t c0 = offsetof(moe::WsHeader, done_ctr);
+    const size_t c1 = offsetof(moe::WsHeader, tile_epoch) + sizeof(unsigned);  // low (tile) half, little-endian
     if (cudaMemsetAsync(base + c0, 0, c1 - c0, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaMemsetAsync(base + offsetof(moe::WsHeader, part_tok), 0,
                         sizeof(((moe::WsHeader *)nullptr)->part_tok), s) != cudaSuccess)
