@@ -11,8 +11,9 @@
 // spends per token.  Counts go to a shared-memory histogram, then one
 // global atomic per (block, expert) into the workspace; the last block to
 // finish (atomic ticket) publishes expert_counts and derives the aux loss
-// and entropy in fp64 from the exact integer counts, then clears the
-// workspace counters for the next call.
+// (fp64, from exact integer sums) and the entropy (exponent + fp32 mantissa
+// logarithms, summed exactly in fixed point; ~1e-7 absolute), then clears
+// the workspace counters for the next call.
 //
 // Definitions: "DeepSeek MoE architecture evolution" ch.1 (top2_gating:
 // topk, softmax of the selected logits, aux = E * sum f_e^2) and sec. 2.3
@@ -45,6 +46,27 @@ __device__ __forceinline__ void topk_insert(float (&bv)[K], int (&bi)[K], float 
             }
         }
     }
+}
+
+// log2 of a positive, finite double: exact binary exponent plus log2f of the
+// mantissa in [1, 2) (absolute error ~1e-7), avoiding fp64 transcendentals.
+__device__ __forceinline__ double log2_via_mantissa(double x)
+{
+    const long long bits = __double_as_longlong(x);
+    const int ex = (int)((bits >> 52) & 0x7FF) - 1023;
+    const double m = __longlong_as_double((bits & 0x000FFFFFFFFFFFFFll) | 0x3FF0000000000000ll);
+    return (double)ex + (double)log2f((float)m);
+}
+
+// 1/x for a positive double: the fp32 reciprocal refined by two
+// Newton-Raphson steps (r <- r (2 - x r); each doubles the correct bits:
+// 24 -> 48 -> full double), instead of an fp64 divide.
+__device__ __forceinline__ double rcp_newton(double x)
+{
+    double r = (double)__frcp_rn((float)x);
+    r = r * (2.0 - x * r);
+    r = r * (2.0 - x * r);
+    return r;
 }
 
 template <int K>
@@ -172,6 +194,7 @@ gate_kernel(const float *__restrict__ logits, int T, int E, int32_t *__restrict_
                 }
             }
         }
+#pragma unroll 8
         for (int e = K; e < E; ++e) {
             float v = row[e];
             finite &= isfinite(v);
@@ -219,39 +242,54 @@ gate_kernel(const float *__restrict__ logits, int T, int E, int32_t *__restrict_
     __syncthreads();
     if (!s_last) return;
 
-    // Last block: publish the totals and the fp64 statistics.
+    // Last block: publish the totals and the statistics.  FP64 units are
+    // scarce on this part, so the per-expert work avoids fp64 transcendentals:
+    //   entropy = -sum_e p_e log2(p_e + eps),  p_e = c_e / N,  N = T*k
+    //           = log2(N) * SUM / N - (1/N) sum_e c_e log2(c_e + eps*N),  SUM = sum_e c_e
+    // with each log2 of a double taken as exponent + log2f(mantissa) (error
+    // ~1e-7 absolute), the products c_e*log2(.) summed exactly in 2^-32
+    // fixed point with integer warp shuffles (deterministic), and
+    //   aux = E * (sum_e c_e^2) / T^2  from the exact integer sum of squares.
     __threadfence();
-    __shared__ double s_term[MOE_MAX_EXPERTS];
-    __shared__ unsigned long long s_sq[MOE_MAX_EXPERTS];
-    const double total = (double)T * (double)K;
-    for (int e = threadIdx.x; e < MOE_MAX_EXPERTS; e += blockDim.x) {
-        double term = 0.0;
-        unsigned long long sq = 0ull;
-        if (e < E) {
-            unsigned c = atomicExch(&ws->gate_counts[e], 0u);
-            expert_counts[e] = (int32_t)c;
-            sq = (unsigned long long)c * c;
-            if (T > 0) {
-                double p = (double)c / total;
-                term = p * log2(p + 1e-8);
-            }
-        }
-        s_term[e] = term;
-        s_sq[e] = sq;
+    __shared__ long long s_fix[kGateMaxThreads / 32];
+    __shared__ unsigned long long s_sq[kGateMaxThreads / 32], s_sum[kGateMaxThreads / 32];
+    const double n_assign = (double)T * (double)K;
+    const double eps_n = 1e-8 * n_assign;
+    long long fix = 0;
+    unsigned long long sq = 0ull, sum = 0ull;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const unsigned c = atomicExch(&ws->gate_counts[e], 0u);
+        expert_counts[e] = (int32_t)c;
+        sq += (unsigned long long)c * c;
+        sum += c;
+        if (c) fix += llrint((double)c * log2_via_mantissa((double)c + eps_n) * 4294967296.0);
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) {
+        fix += __shfl_xor_sync(0xffffffffu, fix, d);
+        sq += __shfl_xor_sync(0xffffffffu, sq, d);
+        sum += __shfl_xor_sync(0xffffffffu, sum, d);
+    }
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    if (lane == 0) {
+        s_fix[wid] = fix;
+        s_sq[wid] = sq;
+        s_sum[wid] = sum;
     }
     __syncthreads();
-    // Fixed-shape tree reduction: deterministic.
-    for (int w = MOE_MAX_EXPERTS / 2; w > 0; w >>= 1) {
-        for (int e = threadIdx.x; e < w; e += blockDim.x) {
-            s_term[e] += s_term[e + w];
-            s_sq[e] += s_sq[e + w];
-        }
-        __syncthreads();
-    }
     if (threadIdx.x == 0) {
+        long long F = 0;
+        unsigned long long SQ = 0ull, SUM = 0ull;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+            F += s_fix[w];
+            SQ += s_sq[w];
+            SUM += s_sum[w];
+        }
         if (T > 0) {
-            *aux_out = (double)E * ((double)s_sq[0] / ((double)T * (double)T));
-            *ent_out = -s_term[0];
+            const double inv_t = rcp_newton((double)T);
+            *aux_out = (double)E * ((double)SQ * inv_t * inv_t);
+            *ent_out = (log2_via_mantissa(n_assign) * (double)SUM - (double)F * (1.0 / 4294967296.0)) *
+                       rcp_newton(n_assign);
         } else {
             *aux_out = 0.0;
             *ent_out = 0.0;

@@ -51,7 +51,8 @@ def check_gate(w, plan, gates_pre, logits_np, tol_gate=1e-6):
     assert gerr <= tol_gate, f"gate error {gerr}"
     # aux: both sides work from the same integer counts in fp64 (bound asked: 1e-6)
     assert abs(plan.aux_loss.item() - aux) <= 1e-9, (plan.aux_loss.item(), aux)
-    assert abs(plan.entropy.item() - ent) <= 1e-9, (plan.entropy.item(), ent)
+    # entropy: exponent + fp32-mantissa logarithms on the device (~1e-7); bound 1e-6
+    assert abs(plan.entropy.item() - ent) <= 1e-6, (plan.entropy.item(), ent)
     return idx, counts
 
 

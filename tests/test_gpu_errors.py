@@ -108,7 +108,7 @@ def test_lookback_wait_expires_with_timeout_status():
     inp = workloads.make_inputs(w, "cuda")
     p.gate(inp["logits"])
     assert p.status() == 0
-    p.ws.view(torch.int32)[5] = 2  # inject_skip_publish = tile 1 + 1
+    p.ws.view(torch.int32)[3] = 2  # inject_skip_publish (byte offset 12) = tile 1 + 1
     p.dispatch_layout()
     assert p.status() == abi.MOE_ERR_TIMEOUT
     # the hook is cleared and the workspace usable again
