@@ -166,6 +166,10 @@ def kernel_bytes(w, R):
         "dispatch": x + packed,
         "combine": eo + y + shared + w.T * w.k * 8,
         "roofline_step": x + R * w.H * bt + eo + y,  # x read, packed written, eo read, y written
+        # every byte the step moves: the roofline bytes plus logits, shared
+        # experts, FP8 scales and the routing metadata
+        "all_step": (x + R * w.H * bt + eo + y + w.T * w.E * 4 + shared + (R * 8 if w.fp8 else 0)
+                     + w.T * w.k * (4 + 4) + w.T * w.k * (4 + 4 + 1 + 4) + w.T * w.k * 8),
     }
 
 
@@ -485,6 +489,8 @@ def run_ours(args):
             "data": "synthetic (seeded): x ~ N(0,1) bf16, router logits fp32, expert outputs N(0,1) bf16",
             "config": config_of(w, world),
             "hbm_gbs": step_gbs, "hbm_frac": step_gbs / peak, "R": R,
+            "hbm_gbs_all_bytes": by["all_step"] / (ms_step * 1e-3) / 1e9,
+            "hbm_frac_all_bytes": by["all_step"] / (ms_step * 1e-3) / 1e9 / peak,
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                          "traffic": traffic, "algorithmic_bytes": by[dom]},
