@@ -66,6 +66,12 @@ def _lib():
         lib.oracle_combine_f32order_tokens.restype = None
         lib.oracle_combine_ref64_tokens.argtypes = [P, I64, I, P, P, P, I, I64, P, I64, P, P]
         lib.oracle_combine_ref64_tokens.restype = None
+        lib.oracle_combine_backward_tokens.argtypes = [P, P, I64, I, P, P, P, I64, P, P]
+        lib.oracle_combine_backward_tokens.restype = None
+        lib.oracle_dispatch_backward_tokens.argtypes = [P, I64, I, P, P, I64, P, P]
+        lib.oracle_dispatch_backward_tokens.restype = None
+        lib.oracle_gate_backward.argtypes = [P, P, P, I64, I, I, I, P]
+        lib.oracle_gate_backward.restype = I
         lib.oracle_bf16_from_float.argtypes = [ctypes.c_float]
         lib.oracle_bf16_from_float.restype = ctypes.c_uint16
         _LIB = lib
@@ -253,6 +259,49 @@ def combine_ref64(eo_bits, gates_f32, dst_row, tokens, T, k, shared_bits=None):
     _lib().oracle_combine_ref64_tokens(_p(eo_bits), H, k, _p(gates_f32), _p(dst_row),
                                        _p(sh), Ks, T, _p(tokens), tokens.size, _p(ref), _p(mag))
     return ref, mag
+
+
+def combine_backward(dy_bits, eo_bits, gates_f32, dst_row, tokens, k):
+    """(d_eo rows bf16 bits [n*k, H] (row i*k+j for slot j of token i;
+    zero for dropped slots), d_gates fp64 [n, k]) for the listed tokens."""
+    dy_bits = _c(dy_bits, np.uint16)
+    eo_bits = _c(eo_bits, np.uint16)
+    gates_f32 = _c(gates_f32, np.float32)
+    dst_row = _c(dst_row, np.int32)
+    tokens = _c(tokens, np.int64)
+    H = dy_bits.shape[1]
+    d_eo = np.zeros((tokens.size * k, H), np.uint16)
+    d_g = np.empty((tokens.size, k), np.float64)
+    _lib().oracle_combine_backward_tokens(_p(dy_bits), _p(eo_bits), H, k, _p(gates_f32), _p(dst_row),
+                                          _p(tokens), tokens.size, _p(d_eo), _p(d_g))
+    return d_eo, d_g
+
+
+def dispatch_backward(d_packed_bits, dst_row, tokens, k):
+    """(dx bf16 bits [n, H] in the pinned fp32 order, dx fp64 [n, H])."""
+    d_packed_bits = _c(d_packed_bits, np.uint16)
+    dst_row = _c(dst_row, np.int32)
+    tokens = _c(tokens, np.int64)
+    H = d_packed_bits.shape[1]
+    dx = np.empty((tokens.size, H), np.uint16)
+    dx64 = np.empty((tokens.size, H), np.float64)
+    _lib().oracle_dispatch_backward_tokens(_p(d_packed_bits), H, k, _p(dst_row), _p(tokens), tokens.size,
+                                           _p(dx), _p(dx64))
+    return dx, dx64
+
+
+def gate_backward(logits, topk_idx, d_gates, mode):
+    """d_logits fp64 [T, E] for L = sum d_gates * gates(logits)."""
+    logits = _c(logits, np.float32)
+    topk_idx = _c(topk_idx, np.int32)
+    d_gates = _c(d_gates, np.float64)
+    T, E = logits.shape
+    k = topk_idx.shape[1]
+    out = np.empty((T, E), np.float64)
+    rc = _lib().oracle_gate_backward(_p(logits), _p(topk_idx), _p(d_gates), T, E, k, mode, _p(out))
+    if rc != 0:
+        raise ValueError("oracle_gate_backward failed")
+    return out
 
 
 def bf16_bits_from_float(v: np.ndarray) -> np.ndarray:

@@ -465,3 +465,101 @@ void oracle_combine_ref64_tokens(const uint16_t *eo, int64_t H, int k, const flo
         }
     }
 }
+
+/* ------------------------------------------------------------------ */
+/* Backward of the path: the gradient retraces the forward routing     */
+/* with the saved indices ([P1] sec. 2.4: the backward all-to-all      */
+/* mirrors the forward one using cached routing indices; [P4] sec. 7,  */
+/* detail item 3: the combine stage is also the backward gradient     */
+/* dispatch).                                                          */
+/* ------------------------------------------------------------------ */
+
+/* Combine backward, for the listed tokens:
+ *   d_eo[dst_row[t,j]] = bf16 RNE(fp32(g[t,j] * dy[t]))  for kept j
+ *   d_gates[t,j]       = sum_h dy[t,h] * eo[dst_row[t,j],h]  (fp64), 0 if dropped
+ * d_eo rows are written to d_eo_rows[i*k + j] (row-major [n*k, H]); rows of
+ * dropped slots are left as they are. */
+void oracle_combine_backward_tokens(const uint16_t *dy, const uint16_t *eo, int64_t H, int k,
+                                    const float *gates, const int32_t *dst_row,
+                                    const int64_t *tokens, int64_t n, uint16_t *d_eo_rows,
+                                    double *d_gates)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t t = tokens[i];
+        for (int j = 0; j < k; ++j) {
+            int32_t r = dst_row[t * k + j];
+            double dot = 0.0;
+            if (r >= 0) {
+                float g = gates[t * k + j];
+                for (int64_t h = 0; h < H; ++h) {
+                    float d = bf16_bits_to_float(dy[t * H + h]);
+                    float prod = g * d; /* one fp32 rounding */
+                    d_eo_rows[(i * k + j) * H + h] = float_to_bf16_bits_rne(prod);
+                    dot += (double)d * (double)bf16_bits_to_float(eo[(int64_t)r * H + h]);
+                }
+            }
+            d_gates[i * k + j] = dot;
+        }
+    }
+}
+
+/* Dispatch backward (bf16 gradients), for the listed tokens, pinned fp32
+ * order: acc = 0; acc = acc + d_packed[dst_row[t,j]] over kept j ascending;
+ * dx[t] = bf16 RNE(acc).  Also the fp64 sum. */
+void oracle_dispatch_backward_tokens(const uint16_t *d_packed, int64_t H, int k,
+                                     const int32_t *dst_row, const int64_t *tokens, int64_t n,
+                                     uint16_t *dx, double *dx64)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t t = tokens[i];
+        for (int64_t h = 0; h < H; ++h) {
+            float acc = 0.0f;
+            double acc64 = 0.0;
+            for (int j = 0; j < k; ++j) {
+                int32_t r = dst_row[t * k + j];
+                if (r < 0) continue;
+                float v = bf16_bits_to_float(d_packed[(int64_t)r * H + h]);
+                acc = acc + v;
+                acc64 += (double)v;
+            }
+            dx[i * H + h] = float_to_bf16_bits_rne(acc);
+            dx64[i * H + h] = acc64;
+        }
+    }
+}
+
+/* Gate backward in fp64: gradient of L = sum_j d_gates[t,j] * g[t,j] with
+ * respect to the logits, the gates g recomputed from logits and topk_idx as
+ * oracle_gates does.
+ *   TOPK_SOFTMAX: g = softmax(l_sel):  dl_sel[j] = g_j (dg_j - sum_i g_i dg_i),
+ *                 other experts 0.
+ *   SOFTMAX_TOPK: g_j = p[sel_j], p = softmax(l):  dl_e = p_e (dp_e - sum_j g_j dg_j)
+ *                 with dp_e = dg_j at e = sel_j, else 0.
+ * (The aux loss depends on the indices only and has no gradient.) */
+int oracle_gate_backward(const float *logits, const int32_t *topk_idx, const double *d_gates,
+                         int64_t T, int E, int k, int mode, double *d_logits)
+{
+    double *g = (double *)malloc(sizeof(double) * (size_t)k);
+    if (!g) return -2;
+    for (int64_t t = 0; t < T; ++t) {
+        const float *l = logits + t * E;
+        const int32_t *ix = topk_idx + t * k;
+        const double *dg = d_gates + t * k;
+        double *dl = d_logits + t * E;
+        if (oracle_gates(l, ix, 1, E, k, mode, g) != 0) { free(g); return -1; }
+        double s = 0.0;
+        for (int j = 0; j < k; ++j) s += g[j] * dg[j];
+        for (int e = 0; e < E; ++e) dl[e] = 0.0;
+        if (mode == 0) {
+            for (int j = 0; j < k; ++j) dl[ix[j]] = g[j] * (dg[j] - s);
+        } else {
+            double m = (double)l[ix[0]];
+            double denom = 0.0;
+            for (int e = 0; e < E; ++e) denom += exp((double)l[e] - m);
+            for (int e = 0; e < E; ++e) dl[e] = -exp((double)l[e] - m) / denom * s;
+            for (int j = 0; j < k; ++j) dl[ix[j]] += g[j] * dg[j];
+        }
+    }
+    free(g);
+    return 0;
+}
