@@ -45,6 +45,8 @@ def parse_args():
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--backward-steps", type=int, default=500,
+                    help="passes of the backward calls timed after the forward (0: skip)")
     return ap.parse_args()
 
 
@@ -476,6 +478,10 @@ def run_ours(args):
                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / K2, "steps": K2,
                "path": "pinned host -> device copies, the four C-ABI calls, y/aux/entropy back, one stream"}
 
+    bwd = None
+    if args.backward_steps > 0:
+        bwd = time_backward(plan, w, inputs, eo_arg, args.backward_steps, world, dev, stream, peak)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, host_inputs(w, inputs, eo), args.cpu_seconds)
@@ -501,12 +507,61 @@ def run_ours(args):
             "clocks": clocks,
             "e2e": e2e,
             "cpu_baseline": cpu,
+            "backward": bwd,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def time_backward(plan, w, inputs, eo_arg, steps, world, dev, stream, peak):
+    """The backward calls on the forward's layout, timed after the forward
+    (not part of the headline step): combine backward (d_expert_out,
+    d_gates), gate backward (d_logits) and dispatch backward (dx).  Returns
+    per-kernel times, algorithmic-byte throughput and roofline fractions."""
+    import torch
+
+    from combine_moe_gate_warp_gb300 import workloads
+    R = int(plan.layout.offsets[w.E].item())
+    dy = workloads.make_dy(w, dev)
+    dp = workloads.make_d_packed(w, max(R, 1), dev)
+    for _ in range(3):
+        plan.backward(inputs["logits"], dy, eo_arg, dp)
+    torch.cuda.synchronize(dev)
+    names = ["combine_backward", "gate_backward", "dispatch_backward"]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    for e in ev:
+        e[0].record(stream)
+        plan.combine_backward(dy, eo_arg)
+        e[1].record(stream)
+        plan.gate_backward(inputs["logits"])
+        e[2].record(stream)
+        plan.dispatch_backward(dp)
+        e[3].record(stream)
+    torch.cuda.synchronize(dev)
+    per = {n: statistics.fmean(e[j].elapsed_time(e[j + 1]) for e in ev) for j, n in enumerate(names)}
+    # whole backward without events between the kernels
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        plan.backward(inputs["logits"], dy, eo_arg, dp)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    total_ms = max_over_ranks(a.elapsed_time(b) / steps, world, dev)
+    st = plan.status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} during the backward passes")
+    by = workloads.nbytes_backward(w, R)
+    gbs = {n: by[n] / (per[n] * 1e-3) / 1e9 for n in names}
+    return {"steps": steps, "ms_per_pass": total_ms,
+            "tokens_per_s": world * w.T / (total_ms * 1e-3),
+            "kernels_ms": per, "kernels_gbs": gbs,
+            "kernels_frac": {n: gbs[n] / peak for n in names},
+            "algorithmic_bytes": by, "gpu_launches": 3 * steps * 2}
 
 
 def main():

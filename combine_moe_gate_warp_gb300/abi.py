@@ -88,6 +88,12 @@ def lib():
     L.moe_dispatch.restype = I
     L.moe_combine.argtypes = [P, ctypes.POINTER(moe_layout), P, P, I, I, I, P, P]
     L.moe_combine.restype = I
+    L.moe_combine_backward.argtypes = [P, P, ctypes.POINTER(moe_layout), P, I, I, P, P, P]
+    L.moe_combine_backward.restype = I
+    L.moe_dispatch_backward.argtypes = [P, ctypes.POINTER(moe_layout), I, I, P, P]
+    L.moe_dispatch_backward.restype = I
+    L.moe_gate_backward.argtypes = [P, P, P, I, I, I, I, P, P, SZ, P]
+    L.moe_gate_backward.restype = I
     L.moe_get_status.argtypes = [P, P]
     L.moe_get_status.restype = I
     L.moe_status_string.argtypes = [I]
@@ -196,6 +202,30 @@ def moe_combine(expert_out, layout: "Layout", gates, shared_out, Ks: int, T: int
                              _ptr(gates, torch.float32, "gates"),
                              _ptr(shared_out, torch.bfloat16, "shared_out"), Ks, T, H,
                              _ptr(y, torch.bfloat16, "y"), _stream(stream)), "moe_combine")
+
+
+def moe_combine_backward(dy, expert_out, layout: "Layout", gates, T: int, H: int, d_expert_out, d_gates,
+                         stream=None) -> None:
+    _check(lib().moe_combine_backward(_ptr(dy, torch.bfloat16, "dy"),
+                                      _ptr(expert_out, torch.bfloat16, "expert_out"), ctypes.byref(layout.c),
+                                      _ptr(gates, torch.float32, "gates"), T, H,
+                                      _ptr(d_expert_out, torch.bfloat16, "d_expert_out"),
+                                      _ptr(d_gates, torch.float32, "d_gates"), _stream(stream)),
+           "moe_combine_backward")
+
+
+def moe_dispatch_backward(d_packed, layout: "Layout", T: int, H: int, dx, stream=None) -> None:
+    _check(lib().moe_dispatch_backward(_ptr(d_packed, torch.bfloat16, "d_packed"), ctypes.byref(layout.c), T, H,
+                                       _ptr(dx, torch.bfloat16, "dx"), _stream(stream)), "moe_dispatch_backward")
+
+
+def moe_gate_backward(logits, topk_idx, d_gates, mode: int, d_logits, ws, stream=None) -> None:
+    T, E = logits.shape
+    k = topk_idx.shape[1]
+    _check(lib().moe_gate_backward(_ptr(logits, torch.float32, "logits"), _ptr(topk_idx, torch.int32, "topk_idx"),
+                                   _ptr(d_gates, torch.float32, "d_gates"), T, E, k, mode,
+                                   _ptr(d_logits, torch.float32, "d_logits"), _ptr(ws, name="ws"), _nbytes(ws),
+                                   _stream(stream)), "moe_gate_backward")
 
 
 def moe_get_status(ws, stream=None) -> int:

@@ -161,6 +161,44 @@ moe_status moe_combine(const void *expert_out, const moe_layout *L, const float 
                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 
+moe_status moe_combine_backward(const void *dy, const void *expert_out, const moe_layout *L, const float *gates,
+                                int T, int H, void *d_expert_out, float *d_gates, moe_stream_t stream)
+{
+    moe_status st = check_layout(L, T);
+    if (st != MOE_OK) return st;
+    if (H < 8 || H % 8 != 0) return MOE_ERR_UNSUPPORTED;
+    if (T > 0 && (!dy || !expert_out || !gates || !d_expert_out || !d_gates)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(dy) || !aligned16(expert_out) || !aligned16(d_expert_out)) return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_combine_backward(dy, expert_out, L, gates, T, H, d_expert_out, d_gates,
+                                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_dispatch_backward(const void *d_packed, const moe_layout *L, int T, int H, void *dx,
+                                 moe_stream_t stream)
+{
+    moe_status st = check_layout(L, T);
+    if (st != MOE_OK) return st;
+    if (H < 8 || H % 8 != 0) return MOE_ERR_UNSUPPORTED;
+    if (T > 0 && (!d_packed || !dx)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(d_packed) || !aligned16(dx)) return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_combine(d_packed, L, nullptr, nullptr, 0, T, H, dx,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_gate_backward(const float *logits, const int32_t *topk_idx, const float *d_gates, int T, int E,
+                             int k, int mode, float *d_logits, void *ws, size_t ws_bytes, moe_stream_t stream)
+{
+    moe_status st = check_sizes(T, E, k);
+    if (st != MOE_OK) return st;
+    if (mode != MOE_TOPK_SOFTMAX && mode != MOE_SOFTMAX_TOPK) return MOE_ERR_INVALID_ARG;
+    if (!ws) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!logits || !topk_idx || !d_gates || !d_logits)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(ws)) return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < moe::kWsHeaderBytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    return from_cuda(moe::launch_gate_backward(logits, topk_idx, d_gates, T, E, k, mode, d_logits, ws,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
 moe_status moe_get_status(void *ws, moe_stream_t stream)
 {
     if (!ws) return MOE_ERR_INVALID_ARG;

@@ -1,0 +1,317 @@
+// backward.cu -- the backward of the routing path: moe_combine_backward and
+// moe_gate_backward (moe_dispatch_backward reuses the combine kernel with
+// unit weights, see combine.cu).
+//
+// "Deepseek-MoE sync-tax essence and four-layer optimisation guide" sec. 2.4
+// (the backward exchange mirrors the forward one, driven by the routing
+// indices cached in the forward pass: nothing is re-routed);
+// "MoE data traits ... DeepEP and MoE all-to-all data handling" sec. 7,
+// detail item 3 (the combine stage carries the gradients back in the
+// backward pass; gradient sums want fp32 accumulation).
+//
+// Combine backward, per token t and kept slot j (row r = dst_row[t,j]):
+//   d_expert_out[r] = bf16 RNE(fp32(g[t,j] * dy[t]))   -- a dispatch of g*dy
+//   d_gates[t,j]    = sum_h dy[t,h] * expert_out[r,h]   -- fp32, 0 if dropped
+// Design (sm_103a): scatter form like the forward dispatch.  One block per
+// token; each thread owns V 16-byte column vectors of the row.  It loads its
+// dy vectors and the matching vectors of all K expert-output rows up front
+// (a dropped slot reads the dy row again, an L2 hit, so the loads stay
+// unconditional and all in flight together), writes the K scaled rows with
+// 16-byte stores, and accumulates the K dot products with FMA (a bf16 x
+// bf16 product is exact in fp32, so each step rounds once).  The K partial
+// sums are reduced by a warp xor tree and then across warps in warp order:
+// fixed order, deterministic.  Summation depth: each thread adds 8*V*passes
+// products (<= 32 when one pass covers the row, else <= H/256 + 32), then 5
+// shuffle levels and <= 7 warp partials: <= H/256 + 44 in all.
+//
+// Gate backward, per token (gates recomputed from the logits in fp32):
+//   TOPK_SOFTMAX: g = softmax over the k selected logits;
+//                 d_logits[sel_j] = g_j (dg_j - s), s = sum_i g_i dg_i, other experts 0
+//   SOFTMAX_TOPK: p = softmax over all E, g_j = p[sel_j];
+//                 d_logits[e] = (e == sel_j ? g_j dg_j : 0) - p_e s
+// One warp per token, lanes striding the E experts (coalesced row loads and
+// stores), warp xor trees for max and sums.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kBwdMaxThreads = 256;
+
+__device__ __forceinline__ unsigned pack_bf16x2_rn(float lo, float hi)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<unsigned *>(&h);
+}
+
+__device__ __forceinline__ uint4 scale_row_vec(float g, const uint4 &d)
+{
+    uint4 o;
+    o.x = pack_bf16x2_rn(__fmul_rn(g, bf16lo(d.x)), __fmul_rn(g, bf16hi(d.x)));
+    o.y = pack_bf16x2_rn(__fmul_rn(g, bf16lo(d.y)), __fmul_rn(g, bf16hi(d.y)));
+    o.z = pack_bf16x2_rn(__fmul_rn(g, bf16lo(d.z)), __fmul_rn(g, bf16hi(d.z)));
+    o.w = pack_bf16x2_rn(__fmul_rn(g, bf16lo(d.w)), __fmul_rn(g, bf16hi(d.w)));
+    return o;
+}
+
+__device__ __forceinline__ float dot_vec(float acc, const uint4 &d, const uint4 &e)
+{
+    acc = __fmaf_rn(bf16lo(d.x), bf16lo(e.x), acc);
+    acc = __fmaf_rn(bf16hi(d.x), bf16hi(e.x), acc);
+    acc = __fmaf_rn(bf16lo(d.y), bf16lo(e.y), acc);
+    acc = __fmaf_rn(bf16hi(d.y), bf16hi(e.y), acc);
+    acc = __fmaf_rn(bf16lo(d.z), bf16lo(e.z), acc);
+    acc = __fmaf_rn(bf16hi(d.z), bf16hi(e.z), acc);
+    acc = __fmaf_rn(bf16lo(d.w), bf16lo(e.w), acc);
+    acc = __fmaf_rn(bf16hi(d.w), bf16hi(e.w), acc);
+    return acc;
+}
+
+template <int K, int V>
+__global__ void __launch_bounds__(kBwdMaxThreads)
+combine_bwd_kernel(const uint4 *__restrict__ dy, const uint4 *__restrict__ eo, const float *__restrict__ gates,
+                   const int32_t *__restrict__ dst_row, int r_max, const int32_t *__restrict__ R_ptr, long long T,
+                   int nvec, uint4 *__restrict__ d_eo, float *__restrict__ d_gates, void *ws)
+{
+    __shared__ int s_row[K];
+    __shared__ float s_g[K];
+    __shared__ float s_part[kBwdMaxThreads / 32][K];
+    pdl_wait();
+    pdl_launch_dependents();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nthr = blockDim.x, nwarps = nthr >> 5;
+    const int rows_valid = min(r_max, __ldg(R_ptr));
+    for (long long t = blockIdx.x; t < T; t += gridDim.x) {
+        if (tid < K) {
+            int r = __ldg(dst_row + t * K + tid);
+            if (r >= rows_valid) {
+                record_status(ws, MOE_ERR_DEVICE_DATA);
+                r = -1;
+            }
+            s_row[tid] = r;
+            s_g[tid] = __ldg(gates + t * K + tid);
+        }
+        __syncthreads();
+        const uint4 *dyrow = dy + t * nvec;
+        float dot[K];
+#pragma unroll
+        for (int j = 0; j < K; ++j) dot[j] = 0.0f;
+        for (int c0 = 0; c0 < nvec; c0 += nthr * V) {
+            uint4 d[V];
+            uint4 e[K][V];
+#pragma unroll
+            for (int u = 0; u < V; ++u) {
+                const int c = c0 + u * nthr + tid;
+                d[u] = c < nvec ? ld_stream_v4(dyrow + c) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int j = 0; j < K; ++j) {
+                const int r = s_row[j];
+                const uint4 *src = r >= 0 ? eo + (long long)r * nvec : dyrow;
+#pragma unroll
+                for (int u = 0; u < V; ++u) {
+                    const int c = c0 + u * nthr + tid;
+                    e[j][u] = c < nvec ? ld_stream_v4(src + c) : make_uint4(0, 0, 0, 0);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < K; ++j) {
+                const int r = s_row[j];
+                if (r < 0) continue;
+                uint4 *dst = d_eo + (long long)r * nvec;
+                const float g = s_g[j];
+#pragma unroll
+                for (int u = 0; u < V; ++u) {
+                    const int c = c0 + u * nthr + tid;
+                    if (c < nvec) st_v4(dst + c, scale_row_vec(g, d[u]));
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < K; ++j)
+#pragma unroll
+                for (int u = 0; u < V; ++u) dot[j] = dot_vec(dot[j], d[u], e[j][u]);
+        }
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) dot[j] += __shfl_xor_sync(0xffffffffu, dot[j], o);
+        }
+        if (lane == 0) {
+#pragma unroll
+            for (int j = 0; j < K; ++j) s_part[warp][j] = dot[j];
+        }
+        __syncthreads();
+        if (tid < K) {
+            float acc = s_part[0][tid];
+            for (int w = 1; w < nwarps; ++w) acc += s_part[w][tid];
+            d_gates[t * K + tid] = s_row[tid] >= 0 ? acc : 0.0f;
+        }
+        __syncthreads();  // s_row / s_part are rewritten for the next token
+    }
+}
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+constexpr int kGateBwdThreads = 256;
+
+// EPL = experts per lane (ceil(E / 32)).
+template <int MODE, int EPL>
+__global__ void __launch_bounds__(kGateBwdThreads)
+gate_bwd_kernel(const float *__restrict__ logits, const int32_t *__restrict__ topk_idx,
+                const float *__restrict__ d_gates, long long T, int E, int k, float *__restrict__ d_logits, void *ws)
+{
+    pdl_wait();
+    pdl_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const long long wpb = kGateBwdThreads / 32;
+    for (long long t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += (long long)gridDim.x * wpb) {
+        const float *l = logits + t * E;
+        // slot lanes: lane j < k holds slot j
+        int sel = -1;
+        float dg = 0.0f;
+        if (lane < k) {
+            sel = __ldg(topk_idx + t * k + lane);
+            dg = __ldg(d_gates + t * k + lane);
+            if (sel < 0 || sel >= E) {
+                record_status(ws, MOE_ERR_DEVICE_DATA);
+                sel = -1;
+            }
+        }
+        const float lsel = sel >= 0 ? __ldg(l + sel) : -INFINITY;
+        float vals[EPL];
+        float m;
+        if (MODE == MOE_TOPK_SOFTMAX) {
+            m = warp_max(lsel);
+        } else {
+            float lm = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) {
+                const int e = lane + 32 * i;
+                vals[i] = e < E ? __ldg(l + e) : -INFINITY;
+                lm = fmaxf(lm, vals[i]);
+            }
+            m = warp_max(lm);
+        }
+        float z;
+        if (MODE == MOE_TOPK_SOFTMAX) {
+            z = warp_sum(sel >= 0 ? expf(__fsub_rn(lsel, m)) : 0.0f);
+        } else {
+            float zs = 0.0f;
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) {
+                vals[i] = (lane + 32 * i) < E ? expf(__fsub_rn(vals[i], m)) : 0.0f;
+                zs += vals[i];
+            }
+            z = warp_sum(zs);
+        }
+        const float g = sel >= 0 ? __fdiv_rn(expf(__fsub_rn(lsel, m)), z) : 0.0f;
+        const float gdg = __fmul_rn(g, dg);
+        const float s = warp_sum(gdg);
+        // slot contribution to its expert's gradient
+        const float own = MODE == MOE_TOPK_SOFTMAX ? __fmul_rn(g, __fsub_rn(dg, s)) : gdg;
+        float out[EPL];
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            out[i] = MODE == MOE_TOPK_SOFTMAX ? 0.0f : -__fmul_rn(__fdiv_rn(vals[i], z), s);
+        }
+        for (int j = 0; j < k; ++j) {
+            const int ej = __shfl_sync(0xffffffffu, sel, j);
+            const float oj = __shfl_sync(0xffffffffu, own, j);
+            if (ej >= 0 && (ej & 31) == lane) {
+#pragma unroll
+                for (int i = 0; i < EPL; ++i)
+                    if (ej == lane + 32 * i) out[i] = __fadd_rn(out[i], oj);
+            }
+        }
+        float *dl = d_logits + t * E;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E) dl[e] = out[i];
+        }
+    }
+}
+
+long long grid_tokens(long long n)
+{
+    return n < 0x7FFFFFFFll ? (n < 1 ? 1 : n) : 0x7FFFFFFFll;
+}
+
+template <int K>
+cudaError_t launch_cbwd_k(const void *dy, const void *eo, const moe_layout *L, const float *gates, int T, int H,
+                          void *d_eo, float *d_gates, cudaStream_t s)
+{
+    const int nvec = H / 8;
+    // V vectors per thread, chosen so the (K+1)*V vectors of a pass fit in
+    // registers; threads cover one row pass (warp multiple, <= 256).
+    constexpr int V = K <= 3 ? 4 : (K <= 8 ? 2 : 1);
+    int nthr = (nvec + V - 1) / V;
+    nthr = (nthr + 31) / 32 * 32;
+    if (nthr > kBwdMaxThreads) nthr = kBwdMaxThreads;
+    const unsigned grid = (unsigned)grid_tokens(T);
+    return launch_pdl(combine_bwd_kernel<K, V>, dim3(grid), dim3(nthr), 0, s, static_cast<const uint4 *>(dy),
+                      static_cast<const uint4 *>(eo), gates, (const int32_t *)L->dst_row, (int)L->r_max,
+                      (const int32_t *)(L->offsets + L->E), (long long)T, nvec, static_cast<uint4 *>(d_eo), d_gates,
+                      L->ws);
+}
+
+template <int MODE>
+cudaError_t launch_gbwd_m(const float *logits, const int32_t *topk_idx, const float *d_gates, int T, int E, int k,
+                          float *d_logits, void *ws, cudaStream_t s)
+{
+    const long long blocks = ((long long)T + kGateBwdThreads / 32 - 1) / (kGateBwdThreads / 32);
+    const unsigned grid = (unsigned)grid_tokens(blocks);
+    const int epl = (E + 31) / 32;
+#define MOE_GBWD_CASE(N)                                                                                          \
+    case N:                                                                                                       \
+        return launch_pdl(gate_bwd_kernel<MODE, N>, dim3(grid), dim3(kGateBwdThreads), 0, s, logits, topk_idx,   \
+                          d_gates, (long long)T, E, k, d_logits, ws);
+    switch (epl) {
+        MOE_GBWD_CASE(1) MOE_GBWD_CASE(2) MOE_GBWD_CASE(3) MOE_GBWD_CASE(4)
+        MOE_GBWD_CASE(5) MOE_GBWD_CASE(6) MOE_GBWD_CASE(7) MOE_GBWD_CASE(8)
+    default: return cudaErrorInvalidValue;
+    }
+#undef MOE_GBWD_CASE
+}
+
+}  // namespace
+
+cudaError_t launch_combine_backward(const void *dy, const void *eo, const moe_layout *L, const float *gates, int T,
+                                   int H, void *d_eo, float *d_gates, cudaStream_t s)
+{
+    if (T == 0) return cudaSuccess;
+    switch (L->k) {
+#define MOE_CBWD_CASE(KK) \
+    case KK: return launch_cbwd_k<KK>(dy, eo, L, gates, T, H, d_eo, d_gates, s);
+        MOE_CBWD_CASE(1) MOE_CBWD_CASE(2) MOE_CBWD_CASE(3) MOE_CBWD_CASE(4)
+        MOE_CBWD_CASE(5) MOE_CBWD_CASE(6) MOE_CBWD_CASE(7) MOE_CBWD_CASE(8)
+        MOE_CBWD_CASE(9) MOE_CBWD_CASE(10) MOE_CBWD_CASE(11) MOE_CBWD_CASE(12)
+        MOE_CBWD_CASE(13) MOE_CBWD_CASE(14) MOE_CBWD_CASE(15) MOE_CBWD_CASE(16)
+#undef MOE_CBWD_CASE
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_gate_backward(const float *logits, const int32_t *topk_idx, const float *d_gates, int T, int E,
+                                 int k, int mode, float *d_logits, void *ws, cudaStream_t s)
+{
+    if (T == 0) return cudaSuccess;
+    return mode == MOE_TOPK_SOFTMAX
+               ? launch_gbwd_m<MOE_TOPK_SOFTMAX>(logits, topk_idx, d_gates, T, E, k, d_logits, ws, s)
+               : launch_gbwd_m<MOE_SOFTMAX_TOPK>(logits, topk_idx, d_gates, T, E, k, d_logits, ws, s);
+}
+
+}  // namespace moe

@@ -29,6 +29,11 @@
 // mbarrier wait is bounded; on expiry the waiter records MOE_ERR_TIMEOUT,
 // and the producer always waits (bounded) for its copies still in flight
 // before it returns.
+//
+// With no gates (weight 1 for every kept slot, no shared experts) the same
+// kernel is the dispatch backward: dx[t] = bf16 RNE of the fp32 sum, in slot
+// order, of the gradient rows of t's kept copies (an FMA with weight 1
+// rounds exactly like the plain fp32 add).
 #include <cuda_bf16.h>
 
 #include <mutex>
@@ -59,7 +64,7 @@ constexpr int kRingBytes = MOE_COMBINE_RING_KB * 1024;     // byte ring per bloc
 
 struct CombineArgs {
     const char *eo;        // [rows, H] bf16
-    const float *gates;    // [T, K]
+    const float *gates;    // [T, K], or null: every weight 1 (dispatch backward)
     const int32_t *dst_row;
     const int32_t *R_ptr;  // offsets + E: rows the layout produced
     const char *shared;    // [Ks, T, H] bf16 or null
@@ -174,7 +179,7 @@ __global__ void __launch_bounds__(kCombThreads + 32) combine_tma_kernel(CombineA
 #pragma unroll
                 for (int j = 0; j < K; ++j) {
                     rows[j] = __ldg(a.dst_row + t * K + j);
-                    g[j] = __ldg(a.gates + t * K + j);
+                    g[j] = a.gates ? __ldg(a.gates + t * K + j) : 1.0f;
                 }
             }
             for (int b = 0; b < 32 && i < n_units; ++b, ++i) {

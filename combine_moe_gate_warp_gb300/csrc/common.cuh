@@ -142,6 +142,10 @@ cudaError_t launch_dispatch_fp8(const void *x, int T, int H, const moe_layout *L
                                 float *scales, cudaStream_t s);
 cudaError_t launch_combine(const void *eo, const moe_layout *L, const float *gates,
                            const void *shared, int Ks, int T, int H, void *y, cudaStream_t s);
+cudaError_t launch_combine_backward(const void *dy, const void *eo, const moe_layout *L, const float *gates, int T,
+                                   int H, void *d_eo, float *d_gates, cudaStream_t s);
+cudaError_t launch_gate_backward(const float *logits, const int32_t *topk_idx, const float *d_gates, int T, int E,
+                                 int k, int mode, float *d_logits, void *ws, cudaStream_t s);
 int device_sm_count();
 
 // Allow `fn` up to `bytes` of dynamic shared memory on the current device

@@ -115,5 +115,55 @@ class RoutePlan:
 
     KERNELS_PER_STEP = 4
 
+    # backward through the same layout -------------------------------------
+    def _bwd_buffers(self):
+        if getattr(self, "d_expert_out", None) is None:
+            s = self.shape
+            dev = self.device
+            self.d_expert_out = torch.empty((max(self.r_max, 1), s.H), dtype=torch.bfloat16, device=dev)
+            self.d_gates = torch.empty((max(s.T, 1), s.k), dtype=torch.float32, device=dev)
+            self.dx = torch.empty((max(s.T, 1), s.H), dtype=torch.bfloat16, device=dev)
+            self.d_logits = torch.empty((max(s.T, 1), s.E), dtype=torch.float32, device=dev)
+
+    def combine_backward(self, dy: torch.Tensor, expert_out: torch.Tensor):
+        """d_expert_out (rows of g*dy) and d_gates (<dy, expert row>)."""
+        s = self.shape
+        self._bwd_buffers()
+        _check_input(dy, torch.bfloat16, (s.T, s.H), "dy")
+        _check_input(expert_out, torch.bfloat16, (), "expert_out")
+        if expert_out.shape[-1] != s.H:
+            raise ValueError("expert_out: last dimension must be H")
+        abi._check(self._lib.moe_combine_backward(dy.data_ptr(), expert_out.data_ptr(), self._Lref,
+                                                  self.gates.data_ptr(), s.T, s.H, self.d_expert_out.data_ptr(),
+                                                  self.d_gates.data_ptr(), self._s), "moe_combine_backward")
+
+    def dispatch_backward(self, d_packed: torch.Tensor):
+        """dx = sum of the gradients of each token's packed copies (fp32)."""
+        s = self.shape
+        self._bwd_buffers()
+        _check_input(d_packed, torch.bfloat16, (), "d_packed")
+        if d_packed.shape[-1] != s.H:
+            raise ValueError("d_packed: last dimension must be H")
+        abi._check(self._lib.moe_dispatch_backward(d_packed.data_ptr(), self._Lref, s.T, s.H, self.dx.data_ptr(),
+                                                   self._s), "moe_dispatch_backward")
+
+    def gate_backward(self, logits: torch.Tensor, d_gates: torch.Tensor | None = None):
+        """d_logits from d_gates (default: the combine backward's d_gates)."""
+        s = self.shape
+        self._bwd_buffers()
+        _check_input(logits, torch.float32, (s.T, s.E), "logits")
+        dg = self.d_gates[:s.T] if d_gates is None else d_gates
+        _check_input(dg, torch.float32, (s.T, s.k), "d_gates")
+        abi._check(self._lib.moe_gate_backward(logits.data_ptr(), self.topk_idx.data_ptr(), dg.data_ptr(), s.T, s.E,
+                                               s.k, s.mode, self.d_logits.data_ptr(), self.ws.data_ptr(),
+                                               self._ws_bytes, self._s), "moe_gate_backward")
+
+    def backward(self, logits, dy, expert_out, d_packed):
+        """combine backward -> gate backward, and the dispatch backward of the
+        expert-side gradient d_packed (3 kernel launches)."""
+        self.combine_backward(dy, expert_out)
+        self.gate_backward(logits)
+        self.dispatch_backward(d_packed)
+
     def status(self) -> int:
         return abi.moe_get_status(self.ws, self.stream)

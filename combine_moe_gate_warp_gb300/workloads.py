@@ -141,6 +141,17 @@ def make_expert_out(w: Workload, rows: int, device="cuda") -> torch.Tensor:
     return _randn_bf16(rows, w.H, _gen(device, w.seed + 303), device)
 
 
+def make_dy(w: Workload, device="cuda") -> torch.Tensor:
+    """Seeded stand-in for the gradient of the combine output y."""
+    return _randn_bf16(w.T, w.H, _gen(device, w.seed + 404), device)
+
+
+def make_d_packed(w: Workload, rows: int, device="cuda") -> torch.Tensor:
+    """Seeded stand-in for the gradient of the packed rows (what the expert
+    FFN's backward hands to the dispatch backward)."""
+    return _randn_bf16(rows, w.H, _gen(device, w.seed + 505), device)
+
+
 def make_inputs(w: Workload, device="cuda") -> dict:
     return dict(logits=make_logits(w, device), x=make_x(w, device), shared=make_shared(w, device))
 
@@ -150,6 +161,18 @@ def nbytes_roofline(w: Workload, R: int) -> int:
     written, expert outputs read, y written."""
     bt = 1 if w.fp8 else 2
     return w.T * w.H * 2 + R * w.H * bt + R * w.H * 2 + w.T * w.H * 2
+
+
+def nbytes_backward(w: Workload, R: int) -> dict:
+    """Roofline bytes of each backward call: combine backward reads dy and
+    the kept expert rows and writes their gradients (+ the gate gradients);
+    dispatch backward reads the kept row gradients and writes dx; gate
+    backward reads the logits and writes their gradients (+ ids, d_gates)."""
+    return {
+        "combine_backward": w.T * w.H * 2 + 2 * R * w.H * 2 + w.T * w.k * 4 * 3,
+        "dispatch_backward": R * w.H * 2 + w.T * w.H * 2 + w.T * w.k * 4,
+        "gate_backward": 2 * w.T * w.E * 4 + w.T * w.k * 8,
+    }
 
 
 def gib(n: int) -> float:
@@ -163,5 +186,6 @@ def describe(w: Workload) -> str:
 
 
 __all__ = ["Workload", "WORKLOADS", "ORDER", "make_inputs", "make_logits", "make_x",
-           "make_shared", "make_expert_out", "zipf_bias", "nbytes_roofline", "describe",
+           "make_shared", "make_expert_out", "make_dy", "make_d_packed", "zipf_bias", "nbytes_roofline",
+           "nbytes_backward", "describe",
            "TOPK_SOFTMAX", "SOFTMAX_TOPK", "gib", "math"]

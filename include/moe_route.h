@@ -4,6 +4,11 @@
  *
  *     moe_gate -> moe_dispatch_layout -> moe_dispatch -> (expert FFN) -> moe_combine
  *
+ * and its backward through the same layout:
+ *
+ *     moe_combine_backward -> (expert FFN backward) -> moe_dispatch_backward
+ *     moe_gate_backward (gate gradients -> router-logit gradients)
+ *
  * Source pages cited below:
  *   [P1] "Deepseek-MoE sync-tax essence and four-layer optimisation guide"
  *        (gsyq.cn news 1572160)
@@ -228,6 +233,72 @@ moe_status moe_dispatch(const void *x, int T, int H, const moe_layout *L, int fp
 moe_status moe_combine(const void *expert_out, const moe_layout *L, const float *gates,
                        const void *shared_out, int Ks, int T, int H, void *y,
                        moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Backward of the path.  The gradients retrace the forward routing through
+ * the same layout; nothing is re-routed ([P1] sec. 2.4: the backward
+ * exchange mirrors the forward one using the routing indices cached in the
+ * forward pass; [P4] sec. 7, detail item 3: the combine stage carries the
+ * gradients back, with fp32 accumulation of the gradient sums).  The shared
+ * experts' output gradient is dy itself (weight 1) and needs no call.
+ * ------------------------------------------------------------------------ */
+
+/*
+ * moe_combine_backward -- gradients of moe_combine with respect to the
+ * expert outputs and the gates.
+ *
+ *   dy            [T, H] bf16, gradient of y.
+ *   expert_out    [r_max, H] bf16, the combine's input.
+ *   gates         [T, k] fp32, the combine's gates.
+ *   d_expert_out out [r_max, H] bf16: for every kept slot (t, j) with
+ *                 r = dst_row[t,j]: row r = bf16 RNE(fp32(gates[t,j] * dy[t]))
+ *                 (one fp32 rounding per element); rows >= R are not written.
+ *   d_gates   out [T, k] fp32: sum_h dy[t,h] * expert_out[r,h] accumulated in
+ *                 fp32 (each bf16 x bf16 product is exact) in a fixed order of
+ *                 summation depth <= H/256 + 44, so |error| <= (H/256 + 44) *
+ *                 2^-24 * sum_h |dy[t,h] * expert_out[r,h]|; 0 for dropped
+ *                 slots.  Deterministic for fixed (H, k).
+ * dst_row entries >= R are recorded as MOE_ERR_DEVICE_DATA and treated as dropped.
+ */
+moe_status moe_combine_backward(const void *dy, const void *expert_out, const moe_layout *L,
+                                const float *gates, int T, int H, void *d_expert_out,
+                                float *d_gates, moe_stream_t stream);
+
+/*
+ * moe_dispatch_backward -- gradient of moe_dispatch (bf16 transport; for
+ * the FP8 transport the quantiser is passed straight through) with respect
+ * to x: each token's gradient is the sum of the gradients of its packed
+ * copies.
+ *
+ *   d_packed  [r_max, H] bf16, gradient of the packed rows.
+ *   dx    out [T, H] bf16:
+ *     acc = 0; for kept j ascending: acc = acc + d_packed[dst_row[t,j]] (fp32);
+ *     dx = bf16 RNE(acc).  A token with no kept slot gets 0.
+ */
+moe_status moe_dispatch_backward(const void *d_packed, const moe_layout *L, int T, int H,
+                                 void *dx, moe_stream_t stream);
+
+/*
+ * moe_gate_backward -- gradient of the gates with respect to the router
+ * logits, the gates recomputed from (logits, topk_idx) in fp32 ([P3] ch.1:
+ * softmax of the selected logits; [P2] sec. 4.1: softmax over all experts
+ * then top-k).  The selection itself and the aux loss (a function of the
+ * counts only) carry no gradient.
+ *
+ *   logits        [T, E] fp32, the gate's input.
+ *   topk_idx      [T, k] int32 from moe_gate (ids outside [0, E) are recorded
+ *                 as MOE_ERR_DEVICE_DATA and ignored).
+ *   d_gates       [T, k] fp32, gradient of the gates.
+ *   d_logits  out [T, E] fp32, with s = sum_j g_j d_gates[t,j]:
+ *     MOE_TOPK_SOFTMAX: g = softmax of the selected logits;
+ *                       d_logits[sel_j] = g_j (d_gates[t,j] - s), others 0.
+ *     MOE_SOFTMAX_TOPK: p = softmax of all E logits, g_j = p[sel_j];
+ *                       d_logits[e] = (e == sel_j ? g_j d_gates[t,j] : 0) - p_e s.
+ *   ws, ws_bytes  any workspace of >= 4096 bytes (only its status word is used).
+ */
+moe_status moe_gate_backward(const float *logits, const int32_t *topk_idx, const float *d_gates,
+                             int T, int E, int k, int mode, float *d_logits,
+                             void *ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Synchronise `stream`, return the device status recorded in `ws` since the
  * last call (MOE_OK if none) and clear it. */
