@@ -12,17 +12,16 @@
 // Combine backward, per token t and kept slot j (row r = dst_row[t,j]):
 //   d_expert_out[r] = bf16 RNE(fp32(g[t,j] * dy[t]))   -- a dispatch of g*dy
 //   d_gates[t,j]    = sum_h dy[t,h] * expert_out[r,h]   -- fp32, 0 if dropped
-// Design (sm_103a): scatter form like the forward dispatch.  One block per
-// token; each thread owns V 16-byte column vectors of the row.  It loads its
-// dy vectors and the matching vectors of all K expert-output rows up front
+// Design (sm_103a): scatter form like the forward dispatch.  One warp per
+// token; each lane owns 16-byte column vectors of the row.  It loads V dy
+// vectors and the matching vectors of all K expert-output rows up front
 // (a dropped slot reads the dy row again, an L2 hit, so the loads stay
 // unconditional and all in flight together), writes the K scaled rows with
-// 16-byte stores, and accumulates the K dot products with FMA (a bf16 x
-// bf16 product is exact in fp32, so each step rounds once).  The K partial
-// sums are reduced by a warp xor tree and then across warps in warp order:
-// fixed order, deterministic.  Summation depth: each thread adds 8*V*passes
-// products (<= 32 when one pass covers the row, else <= H/256 + 32), then 5
-// shuffle levels and <= 7 warp partials: <= H/256 + 44 in all.
+// 16-byte stores, and accumulates the K dot products: the 8 products of a
+// vector with FMA from 0 (a bf16 x bf16 product is exact in fp32, so each
+// step rounds once), that partial added to the slot's running sum, and the
+// 32 lane sums reduced by a warp xor tree.  Fixed order, deterministic;
+// summation depth 8 + ceil(H/256) + 5 <= H/256 + 14.
 //
 // Gate backward, per token (gates recomputed from the logits in fp32):
 //   TOPK_SOFTMAX: g = softmax over the k selected logits;
@@ -38,7 +37,7 @@
 namespace moe {
 namespace {
 
-constexpr int kBwdMaxThreads = 256;
+constexpr int kBwdThreads = 256;  // combine backward: 8 token warps per block
 
 __device__ __forceinline__ unsigned pack_bf16x2_rn(float lo, float hi)
 {
@@ -69,86 +68,86 @@ __device__ __forceinline__ float dot_vec(float acc, const uint4 &d, const uint4 
     return acc;
 }
 
+// One warp per token (persistent warps striding over the tokens): lane l
+// owns the 16-byte column vectors l, l+32, ... of the row, V of them per
+// pass.  No block-wide barrier, so the warps of an SM drift apart and one
+// warp's reduction overlaps the others' loads.
 template <int K, int V>
-__global__ void __launch_bounds__(kBwdMaxThreads)
+__global__ void __launch_bounds__(kBwdThreads)
 combine_bwd_kernel(const uint4 *__restrict__ dy, const uint4 *__restrict__ eo, const float *__restrict__ gates,
                    const int32_t *__restrict__ dst_row, int r_max, const int32_t *__restrict__ R_ptr, long long T,
                    int nvec, uint4 *__restrict__ d_eo, float *__restrict__ d_gates, void *ws)
 {
-    __shared__ int s_row[K];
-    __shared__ float s_g[K];
-    __shared__ float s_part[kBwdMaxThreads / 32][K];
     pdl_wait();
     pdl_launch_dependents();
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int nthr = blockDim.x, nwarps = nthr >> 5;
+    const int lane = threadIdx.x & 31;
+    const long long nwarps = (long long)gridDim.x * (kBwdThreads / 32);
     const int rows_valid = min(r_max, __ldg(R_ptr));
-    for (long long t = blockIdx.x; t < T; t += gridDim.x) {
-        if (tid < K) {
-            int r = __ldg(dst_row + t * K + tid);
-            if (r >= rows_valid) {
+    for (long long t = (long long)blockIdx.x * (kBwdThreads / 32) + (threadIdx.x >> 5); t < T; t += nwarps) {
+        // lane j < K reads slot j; broadcast below
+        int rl = -1;
+        float gl = 0.0f;
+        if (lane < K) {
+            rl = __ldg(dst_row + t * K + lane);
+            gl = __ldg(gates + t * K + lane);
+            if (rl >= rows_valid) {
                 record_status(ws, MOE_ERR_DEVICE_DATA);
-                r = -1;
+                rl = -1;
             }
-            s_row[tid] = r;
-            s_g[tid] = __ldg(gates + t * K + tid);
         }
-        __syncthreads();
+        int row[K];
+        float g[K];
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            row[j] = __shfl_sync(0xffffffffu, rl, j);
+            g[j] = __shfl_sync(0xffffffffu, gl, j);
+        }
         const uint4 *dyrow = dy + t * nvec;
         float dot[K];
 #pragma unroll
         for (int j = 0; j < K; ++j) dot[j] = 0.0f;
-        for (int c0 = 0; c0 < nvec; c0 += nthr * V) {
+        for (int c0 = lane; c0 < nvec; c0 += 32 * V) {
             uint4 d[V];
             uint4 e[K][V];
 #pragma unroll
             for (int u = 0; u < V; ++u) {
-                const int c = c0 + u * nthr + tid;
+                const int c = c0 + 32 * u;
                 d[u] = c < nvec ? ld_stream_v4(dyrow + c) : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
             for (int j = 0; j < K; ++j) {
-                const int r = s_row[j];
-                const uint4 *src = r >= 0 ? eo + (long long)r * nvec : dyrow;
+                const uint4 *src = row[j] >= 0 ? eo + (long long)row[j] * nvec : dyrow;
 #pragma unroll
                 for (int u = 0; u < V; ++u) {
-                    const int c = c0 + u * nthr + tid;
+                    const int c = c0 + 32 * u;
                     e[j][u] = c < nvec ? ld_stream_v4(src + c) : make_uint4(0, 0, 0, 0);
                 }
             }
 #pragma unroll
             for (int j = 0; j < K; ++j) {
-                const int r = s_row[j];
-                if (r < 0) continue;
-                uint4 *dst = d_eo + (long long)r * nvec;
-                const float g = s_g[j];
+                if (row[j] < 0) continue;
+                uint4 *dst = d_eo + (long long)row[j] * nvec;
 #pragma unroll
                 for (int u = 0; u < V; ++u) {
-                    const int c = c0 + u * nthr + tid;
-                    if (c < nvec) st_v4(dst + c, scale_row_vec(g, d[u]));
+                    const int c = c0 + 32 * u;
+                    if (c < nvec) st_v4(dst + c, scale_row_vec(g[j], d[u]));
                 }
             }
+            // per vector: its 8 products summed from 0, then added to the slot's sum
 #pragma unroll
             for (int j = 0; j < K; ++j)
 #pragma unroll
-                for (int u = 0; u < V; ++u) dot[j] = dot_vec(dot[j], d[u], e[j][u]);
+                for (int u = 0; u < V; ++u) dot[j] = __fadd_rn(dot[j], dot_vec(0.0f, d[u], e[j][u]));
         }
+        float mine = 0.0f;
 #pragma unroll
         for (int j = 0; j < K; ++j) {
+            float v = dot[j];
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) dot[j] += __shfl_xor_sync(0xffffffffu, dot[j], o);
+            for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+            if (lane == j) mine = row[j] >= 0 ? v : 0.0f;
         }
-        if (lane == 0) {
-#pragma unroll
-            for (int j = 0; j < K; ++j) s_part[warp][j] = dot[j];
-        }
-        __syncthreads();
-        if (tid < K) {
-            float acc = s_part[0][tid];
-            for (int w = 1; w < nwarps; ++w) acc += s_part[w][tid];
-            d_gates[t * K + tid] = s_row[tid] >= 0 ? acc : 0.0f;
-        }
-        __syncthreads();  // s_row / s_part are rewritten for the next token
+        if (lane < K) d_gates[t * K + lane] = mine;
     }
 }
 
@@ -250,19 +249,29 @@ long long grid_tokens(long long n)
     return n < 0x7FFFFFFFll ? (n < 1 ? 1 : n) : 0x7FFFFFFFll;
 }
 
+int resident_blocks(const void *fn, int threads)
+{
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, 0) != cudaSuccess || n < 1) n = 1;
+    return n * device_sm_count();
+}
+
 template <int K>
 cudaError_t launch_cbwd_k(const void *dy, const void *eo, const moe_layout *L, const float *gates, int T, int H,
                           void *d_eo, float *d_gates, cudaStream_t s)
 {
     const int nvec = H / 8;
-    // V vectors per thread, chosen so the (K+1)*V vectors of a pass fit in
-    // registers; threads cover one row pass (warp multiple, <= 256).
+    // V vectors per lane and pass, chosen so the (K+1)*V vectors of a pass
+    // fit in registers next to each other.
     constexpr int V = K <= 3 ? 4 : (K <= 8 ? 2 : 1);
-    int nthr = (nvec + V - 1) / V;
-    nthr = (nthr + 31) / 32 * 32;
-    if (nthr > kBwdMaxThreads) nthr = kBwdMaxThreads;
-    const unsigned grid = (unsigned)grid_tokens(T);
-    return launch_pdl(combine_bwd_kernel<K, V>, dim3(grid), dim3(nthr), 0, s, static_cast<const uint4 *>(dy),
+    static int resident[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int &res = resident[dev & 63];
+    if (res == 0) res = resident_blocks(reinterpret_cast<const void *>(combine_bwd_kernel<K, V>), kBwdThreads);
+    const long long need = ((long long)T + kBwdThreads / 32 - 1) / (kBwdThreads / 32);
+    const unsigned grid = (unsigned)(need < res ? need : res);
+    return launch_pdl(combine_bwd_kernel<K, V>, dim3(grid), dim3(kBwdThreads), 0, s, static_cast<const uint4 *>(dy),
                       static_cast<const uint4 *>(eo), gates, (const int32_t *)L->dst_row, (int)L->r_max,
                       (const int32_t *)(L->offsets + L->E), (long long)T, nvec, static_cast<uint4 *>(d_eo), d_gates,
                       L->ws);

@@ -255,7 +255,7 @@ moe_status moe_combine(const void *expert_out, const moe_layout *L, const float 
  *                 (one fp32 rounding per element); rows >= R are not written.
  *   d_gates   out [T, k] fp32: sum_h dy[t,h] * expert_out[r,h] accumulated in
  *                 fp32 (each bf16 x bf16 product is exact) in a fixed order of
- *                 summation depth <= H/256 + 44, so |error| <= (H/256 + 44) *
+ *                 summation depth <= H/256 + 14, so |error| <= (H/256 + 14) *
  *                 2^-24 * sum_h |dy[t,h] * expert_out[r,h]|; 0 for dropped
  *                 slots.  Deterministic for fixed (H, k).
  * dst_row entries >= R are recorded as MOE_ERR_DEVICE_DATA and treated as dropped.
