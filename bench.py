@@ -175,14 +175,15 @@ def kernel_bytes(w, R):
     }
 
 
-KERNEL_SOURCES = {"dispatch": "dispatch.cu", "combine": "combine.cu", "gate": "gate.cu",
-                  "layout": "layout.cu"}
+KERNEL_SOURCES = {"dispatch": ("dispatch.cu",), "combine": ("combine.cu",), "gate": ("gate.cu",),
+                  "layout": ("layout.cu",), "combine_backward": ("backward.cu",),
+                  "gate_backward": ("backward.cu",), "dispatch_backward": ("combine.cu",)}
 
 
 def source_digest(name: str) -> str:
     csrc = os.path.join(ROOT, "combine_moe_gate_warp_gb300", "csrc")
     h = hashlib.sha256()
-    for f in (KERNEL_SOURCES[name], "common.cuh"):
+    for f in KERNEL_SOURCES[name] + ("common.cuh",):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -558,6 +559,7 @@ def time_backward(plan, w, inputs, eo_arg, steps, world, dev, stream, peak):
     by = workloads.nbytes_backward(w, R)
     gbs = {n: by[n] / (per[n] * 1e-3) / 1e9 for n in names}
     return {"steps": steps, "ms_per_pass": total_ms,
+            "traffic": {n: measured_traffic(n, w.name) for n in names},
             "tokens_per_s": world * w.T / (total_ms * 1e-3),
             "kernels_ms": per, "kernels_gbs": gbs,
             "kernels_frac": {n: gbs[n] / peak for n in names},
