@@ -66,6 +66,14 @@ def _lib():
         lib.oracle_combine_f32order_tokens.restype = None
         lib.oracle_combine_ref64_tokens.argtypes = [P, I64, I, P, P, P, I, I64, P, I64, P, P]
         lib.oracle_combine_ref64_tokens.restype = None
+        lib.oracle_fp8_group_params.argtypes = [P, I64, P, P, I64, I64, P]
+        lib.oracle_fp8_group_params.restype = I
+        lib.oracle_quantize_rows_with_params.argtypes = [P, I64, P, P, I64, P, P, P]
+        lib.oracle_quantize_rows_with_params.restype = None
+        lib.oracle_combine_fp8_f32order_tokens.argtypes = [P, P, I64, I, P, P, P, I, I64, P, I64, P]
+        lib.oracle_combine_fp8_f32order_tokens.restype = None
+        lib.oracle_combine_fp8_ref64_tokens.argtypes = [P, P, I64, I, P, P, P, I, I64, P, I64, P, P]
+        lib.oracle_combine_fp8_ref64_tokens.restype = None
         lib.oracle_combine_backward_tokens.argtypes = [P, P, I64, I, P, P, P, I64, P, P]
         lib.oracle_combine_backward_tokens.restype = None
         lib.oracle_dispatch_backward_tokens.argtypes = [P, I64, I, P, P, I64, P, P]
@@ -222,6 +230,89 @@ def dispatch_fp8_rows(x_bits: np.ndarray, k: int, src_pos: np.ndarray, rows):
     _lib().oracle_dispatch_fp8_rows(_p(x_bits), H, k, _p(src_pos), _p(rows), rows.size,
                                     _p(codes), _p(scales))
     return codes, scales
+
+
+FP8_PER_TOKEN, FP8_PER_EXPERT, FP8_GLOBAL = 1, 2, 3
+
+
+def fp8_group_params(src_bits, src_row, group, ngroups):
+    """(scale, zero) float32 [ngroups, 2] over the rows of each group."""
+    src_bits = _c(src_bits, np.uint16)
+    src_row = _c(src_row, np.int64)
+    group = _c(group, np.int32)
+    params = np.empty((max(int(ngroups), 1), 2), np.float32)
+    rc = _lib().oracle_fp8_group_params(_p(src_bits), src_bits.shape[1], _p(src_row), _p(group), src_row.size,
+                                        int(ngroups), _p(params))
+    if rc != 0:
+        raise ValueError("oracle_fp8_group_params failed")
+    return params[:ngroups]
+
+
+def quantize_rows_with_params(src_bits, src_row, group, params):
+    """(codes uint8 [n, H], scales float32 [n, 2]) of the listed rows."""
+    src_bits = _c(src_bits, np.uint16)
+    src_row = _c(src_row, np.int64)
+    group = _c(group, np.int32)
+    params = _c(params, np.float32)
+    H = src_bits.shape[1]
+    codes = np.empty((src_row.size, H), np.uint8)
+    scales = np.empty((src_row.size, 2), np.float32)
+    _lib().oracle_quantize_rows_with_params(_p(src_bits), H, _p(src_row), _p(group), src_row.size, _p(params),
+                                            _p(codes), _p(scales))
+    return codes, scales
+
+
+def quantize_rows_grouped(src_bits, src_row, group, ngroups):
+    """Group parameters over all listed rows, then every row encoded."""
+    params = fp8_group_params(src_bits, src_row, group, ngroups)
+    return quantize_rows_with_params(src_bits, src_row, group, params)
+
+
+def row_groups(mode, offsets, rows):
+    """(group id per packed row, number of groups) for a quantiser mode:
+    per-token = the row itself, per-expert = the row's expert (from the
+    layout offsets), global = one group."""
+    rows = np.asarray(rows, np.int64)
+    offsets = np.asarray(offsets, np.int64)
+    if mode == FP8_PER_TOKEN:
+        return rows.astype(np.int32), int(rows.max()) + 1 if rows.size else 0
+    if mode == FP8_PER_EXPERT:
+        E = offsets.size - 1
+        return (np.searchsorted(offsets, rows, side="right") - 1).astype(np.int32), E
+    if mode == FP8_GLOBAL:
+        return np.zeros(rows.size, np.int32), 1
+    raise ValueError("unknown FP8 mode")
+
+
+def combine_fp8_f32order(codes, scales, gates_f32, dst_row, tokens, T, k, shared_bits=None):
+    """bf16 bits [n, H] of y from FP8 expert-output rows, pinned fp32 order."""
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.float32)
+    gates_f32 = _c(gates_f32, np.float32)
+    dst_row = _c(dst_row, np.int32)
+    tokens = _c(tokens, np.int64)
+    H = codes.shape[1]
+    sh, Ks = _shared_args(shared_bits, T, H)
+    y = np.empty((tokens.size, H), np.uint16)
+    _lib().oracle_combine_fp8_f32order_tokens(_p(codes), _p(scales), H, k, _p(gates_f32), _p(dst_row), _p(sh), Ks,
+                                              T, _p(tokens), tokens.size, _p(y))
+    return y
+
+
+def combine_fp8_ref64(codes, scales, gates_f32, dst_row, tokens, T, k, shared_bits=None):
+    """(fp64 reference [n, H], sum of |terms| [n, H]) of the FP8 combine."""
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.float32)
+    gates_f32 = _c(gates_f32, np.float32)
+    dst_row = _c(dst_row, np.int32)
+    tokens = _c(tokens, np.int64)
+    H = codes.shape[1]
+    sh, Ks = _shared_args(shared_bits, T, H)
+    ref = np.empty((tokens.size, H), np.float64)
+    mag = np.empty((tokens.size, H), np.float64)
+    _lib().oracle_combine_fp8_ref64_tokens(_p(codes), _p(scales), H, k, _p(gates_f32), _p(dst_row), _p(sh), Ks, T,
+                                           _p(tokens), tokens.size, _p(ref), _p(mag))
+    return ref, mag
 
 
 def _shared_args(shared_bits, T, H):

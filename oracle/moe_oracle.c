@@ -404,6 +404,72 @@ void oracle_dispatch_fp8_rows(const uint16_t *x, int64_t H, int k, const int32_t
     }
 }
 
+/* Grouped variants of the same affine map ([P1] sec. 5.2: the FP8
+ * quantiser offers per-token, per-expert and global modes).  One (scale,
+ * zero) pair per group, from the max and min over every element of the
+ * group's rows, with the per-token formula above; each row is encoded with
+ * its group's pair.  Per-token: a row is its own group; per-expert: the
+ * rows sent to one expert; global: every transported row.
+ *
+ * Rows are given as src [*, H] bf16 with row i = src row src_row[i] in
+ * group group[i] (0 <= group < ngroups). */
+
+/* params [ngroups, 2] = (scale, zero) per group; a group without rows gets
+ * (0, 0).  Returns 0, or -1 on a bad group id / allocation failure. */
+int oracle_fp8_group_params(const uint16_t *src, int64_t H, const int64_t *src_row,
+                            const int32_t *group, int64_t n, int64_t ngroups, float *params)
+{
+    float *gmx = (float *)malloc(sizeof(float) * (size_t)(ngroups > 0 ? ngroups : 1));
+    float *gmn = (float *)malloc(sizeof(float) * (size_t)(ngroups > 0 ? ngroups : 1));
+    unsigned char *seen = (unsigned char *)calloc((size_t)(ngroups > 0 ? ngroups : 1), 1);
+    int rc = 0;
+    if (!gmx || !gmn || !seen) { rc = -1; goto done; }
+    for (int64_t i = 0; i < n; ++i) {
+        if (group[i] < 0 || group[i] >= ngroups) { rc = -1; goto done; }
+        const uint16_t *row = src + src_row[i] * H;
+        int32_t g = group[i];
+        for (int64_t h = 0; h < H; ++h) {
+            float v = bf16_bits_to_float(row[h]);
+            if (!seen[g]) { gmx[g] = v; gmn[g] = v; seen[g] = 1; continue; }
+            if (total_less(gmx[g], v)) gmx[g] = v;
+            if (total_less(v, gmn[g])) gmn[g] = v;
+        }
+    }
+    for (int64_t g = 0; g < ngroups; ++g) {
+        if (!seen[g]) { params[2 * g] = 0.0f; params[2 * g + 1] = 0.0f; continue; }
+        params[2 * g] = (gmx[g] == gmn[g]) ? 0.0f : (gmx[g] - gmn[g]) / 896.0f;
+        params[2 * g + 1] = (gmx[g] + gmn[g]) * 0.5f;
+    }
+done:
+    free(gmx);
+    free(gmn);
+    free(seen);
+    return rc;
+}
+
+/* codes [n, H] and scales [n, 2] of the listed rows, encoded with their
+ * group's (scale, zero) from params. */
+void oracle_quantize_rows_with_params(const uint16_t *src, int64_t H, const int64_t *src_row,
+                                      const int32_t *group, int64_t n, const float *params,
+                                      uint8_t *codes, float *scales)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        float scale = params[2 * (int64_t)group[i]];
+        float zero = params[2 * (int64_t)group[i] + 1];
+        const uint16_t *row = src + src_row[i] * H;
+        for (int64_t h = 0; h < H; ++h) {
+            if (scale == 0.0f) {
+                codes[i * H + h] = 0x00u;
+            } else {
+                float q = (bf16_bits_to_float(row[h]) - zero) / scale;
+                codes[i * H + h] = oracle_e4m3_satfinite(q);
+            }
+        }
+        scales[2 * i] = scale;
+        scales[2 * i + 1] = zero;
+    }
+}
+
 /* ------------------------------------------------------------------ */
 /* a7: combine                                                          */
 /* [P4] sec. 7 "Combine": per token, the weighted sum of its top-k      */
@@ -452,6 +518,69 @@ void oracle_combine_ref64_tokens(const uint16_t *eo, int64_t H, int k, const flo
                 int32_t r = dst_row[t * k + j];
                 if (r < 0) continue;
                 double term = (double)gates[t * k + j] * (double)bf16_bits_to_float(eo[(int64_t)r * H + h]);
+                acc += term;
+                mag += fabs(term);
+            }
+            for (int s = 0; s < Ks; ++s) {
+                double term = (double)bf16_bits_to_float(shared[((int64_t)s * T + t) * H + h]);
+                acc += term;
+                mag += fabs(term);
+            }
+            ref[i * H + h] = acc;
+            abs_terms[i * H + h] = mag;
+        }
+    }
+}
+
+/* Combine of FP8 expert outputs ([P1] sec. 3.1: the per-token affine
+ * FP8 map is applied to each token's expert output vector, i.e. on the
+ * combine side of the exchange too).  Each packed row r carries codes and
+ * (scale, zero); its value is dequantised in fp32 with one rounding,
+ *   v = fmaf(scale, e4m3_value(code), zero),
+ * and then combined in the pinned order of the bf16 combine:
+ *   acc = 0; acc = fmaf(g, v, acc) over kept slots ascending;
+ *   acc = acc + shared (bf16) over s ascending; y = bf16 RNE(acc).
+ * (e4m3 values are exact in fp32.) */
+void oracle_combine_fp8_f32order_tokens(const uint8_t *codes, const float *scales, int64_t H, int k,
+                                        const float *gates, const int32_t *dst_row,
+                                        const uint16_t *shared, int Ks, int64_t T,
+                                        const int64_t *tokens, int64_t n, uint16_t *y)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t t = tokens[i];
+        for (int64_t h = 0; h < H; ++h) {
+            float acc = 0.0f;
+            for (int j = 0; j < k; ++j) {
+                int32_t r = dst_row[t * k + j];
+                if (r < 0) continue;
+                float val = (float)oracle_e4m3_decode(codes[(int64_t)r * H + h]);
+                float v = fmaf(scales[2 * (int64_t)r], val, scales[2 * (int64_t)r + 1]);
+                acc = fmaf(gates[t * k + j], v, acc);
+            }
+            for (int s = 0; s < Ks; ++s)
+                acc = acc + bf16_bits_to_float(shared[((int64_t)s * T + t) * H + h]);
+            y[i * H + h] = float_to_bf16_bits_rne(acc);
+        }
+    }
+}
+
+/* fp64 reference of the FP8 combine: sum g * (zero + scale * value) (+
+ * shared), and sum |term|. */
+void oracle_combine_fp8_ref64_tokens(const uint8_t *codes, const float *scales, int64_t H, int k,
+                                     const float *gates, const int32_t *dst_row,
+                                     const uint16_t *shared, int Ks, int64_t T,
+                                     const int64_t *tokens, int64_t n, double *ref, double *abs_terms)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t t = tokens[i];
+        for (int64_t h = 0; h < H; ++h) {
+            double acc = 0.0, mag = 0.0;
+            for (int j = 0; j < k; ++j) {
+                int32_t r = dst_row[t * k + j];
+                if (r < 0) continue;
+                double v = (double)scales[2 * (int64_t)r + 1] +
+                           (double)scales[2 * (int64_t)r] * oracle_e4m3_decode(codes[(int64_t)r * H + h]);
+                double term = (double)gates[t * k + j] * v;
                 acc += term;
                 mag += fabs(term);
             }
