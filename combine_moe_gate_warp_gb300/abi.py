@@ -27,6 +27,10 @@ MOE_ERR_DEVICE_DATA = 6
 MOE_TOPK_SOFTMAX = 0
 MOE_SOFTMAX_TOPK = 1
 
+MOE_FP8_PER_TOKEN = 1
+MOE_FP8_PER_EXPERT = 2
+MOE_FP8_GLOBAL = 3
+
 MOE_MAX_EXPERTS = 256
 MOE_MAX_TOPK = 16
 MOE_MAX_SHARED = 8
@@ -88,6 +92,10 @@ def lib():
     L.moe_dispatch.restype = I
     L.moe_combine.argtypes = [P, ctypes.POINTER(moe_layout), P, P, I, I, I, P, P]
     L.moe_combine.restype = I
+    L.moe_quantize_rows.argtypes = [P, ctypes.POINTER(moe_layout), I, I, P, P, P]
+    L.moe_quantize_rows.restype = I
+    L.moe_combine_fp8.argtypes = [P, P, ctypes.POINTER(moe_layout), P, P, I, I, I, P, P]
+    L.moe_combine_fp8.restype = I
     L.moe_combine_backward.argtypes = [P, P, ctypes.POINTER(moe_layout), P, I, I, P, P, P]
     L.moe_combine_backward.restype = I
     L.moe_dispatch_backward.argtypes = [P, ctypes.POINTER(moe_layout), I, I, P, P]
@@ -202,6 +210,20 @@ def moe_combine(expert_out, layout: "Layout", gates, shared_out, Ks: int, T: int
                              _ptr(gates, torch.float32, "gates"),
                              _ptr(shared_out, torch.bfloat16, "shared_out"), Ks, T, H,
                              _ptr(y, torch.bfloat16, "y"), _stream(stream)), "moe_combine")
+
+
+def moe_quantize_rows(rows, layout: "Layout", H: int, mode: int, codes, scales, stream=None) -> None:
+    _check(lib().moe_quantize_rows(_ptr(rows, torch.bfloat16, "rows"), ctypes.byref(layout.c), H, int(mode),
+                                   _ptr(codes, torch.uint8, "codes"), _ptr(scales, torch.float32, "scales"),
+                                   _stream(stream)), "moe_quantize_rows")
+
+
+def moe_combine_fp8(codes, scales, layout: "Layout", gates, shared_out, Ks: int, T: int, H: int, y,
+                    stream=None) -> None:
+    _check(lib().moe_combine_fp8(_ptr(codes, torch.uint8, "codes"), _ptr(scales, torch.float32, "scales"),
+                                 ctypes.byref(layout.c), _ptr(gates, torch.float32, "gates"),
+                                 _ptr(shared_out, torch.bfloat16, "shared_out"), Ks, T, H,
+                                 _ptr(y, torch.bfloat16, "y"), _stream(stream)), "moe_combine_fp8")
 
 
 def moe_combine_backward(dy, expert_out, layout: "Layout", gates, T: int, H: int, d_expert_out, d_gates,

@@ -138,14 +138,15 @@ moe_status moe_dispatch(const void *x, int T, int H, const moe_layout *L, int fp
 {
     moe_status st = check_layout(L, T);
     if (st != MOE_OK) return st;
-    if (fp8 != 0 && fp8 != 1) return MOE_ERR_INVALID_ARG;
+    if (fp8 < 0 || fp8 > MOE_FP8_GLOBAL) return MOE_ERR_INVALID_ARG;
     if (H < 8 || H % 8 != 0) return MOE_ERR_UNSUPPORTED;
     if (fp8 && (H % 16 != 0 || H > MOE_MAX_H_FP8)) return MOE_ERR_UNSUPPORTED;
     if (T > 0 && (!x || !packed || (fp8 && !scales))) return MOE_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(packed) || !aligned16(scales)) return MOE_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    return from_cuda(fp8 ? moe::launch_dispatch_fp8(x, T, H, L, packed, scales, s)
-                         : moe::launch_dispatch_bf16(x, T, H, L, packed, s));
+    if (fp8 == MOE_FP8_PER_TOKEN) return from_cuda(moe::launch_dispatch_fp8(x, T, H, L, packed, scales, s));
+    if (fp8 != 0) return from_cuda(moe::launch_dispatch_fp8_grouped(x, T, H, L, fp8, packed, scales, s));
+    return from_cuda(moe::launch_dispatch_bf16(x, T, H, L, packed, s));
 }
 
 moe_status moe_combine(const void *expert_out, const moe_layout *L, const float *gates,
@@ -159,6 +160,32 @@ moe_status moe_combine(const void *expert_out, const moe_layout *L, const float 
     if (!aligned16(expert_out) || !aligned16(y) || !aligned16(shared_out)) return MOE_ERR_INVALID_ARG;
     return from_cuda(moe::launch_combine(expert_out, L, gates, Ks > 0 ? shared_out : nullptr, Ks, T, H, y,
                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_quantize_rows(const void *rows, const moe_layout *L, int H, int mode, void *codes, float *scales,
+                             moe_stream_t stream)
+{
+    if (!L) return MOE_ERR_INVALID_ARG;
+    moe_status st = check_layout(L, L->T);
+    if (st != MOE_OK) return st;
+    if (mode < MOE_FP8_PER_TOKEN || mode > MOE_FP8_GLOBAL) return MOE_ERR_INVALID_ARG;
+    if (H < 16 || H % 16 != 0 || H > MOE_MAX_H_FP8) return MOE_ERR_UNSUPPORTED;
+    if (L->r_max > 0 && (!rows || !codes || !scales)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(rows) || !aligned16(codes) || !aligned16(scales)) return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_quantize_rows(rows, L, H, mode, codes, scales, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_combine_fp8(const void *codes, const float *scales, const moe_layout *L, const float *gates,
+                           const void *shared_out, int Ks, int T, int H, void *y, moe_stream_t stream)
+{
+    moe_status st = check_layout(L, T);
+    if (st != MOE_OK) return st;
+    if (H < 16 || H % 16 != 0) return MOE_ERR_UNSUPPORTED;
+    if (Ks < 0 || Ks > MOE_MAX_SHARED) return MOE_ERR_UNSUPPORTED;
+    if (T > 0 && (!codes || !scales || !gates || !y || (Ks > 0 && !shared_out))) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(codes) || !aligned16(y) || !aligned16(shared_out)) return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_combine_fp8(codes, scales, L, gates, Ks > 0 ? shared_out : nullptr, Ks, T, H, y,
+                                             reinterpret_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_combine_backward(const void *dy, const void *expert_out, const moe_layout *L, const float *gates,

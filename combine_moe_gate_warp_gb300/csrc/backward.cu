@@ -28,8 +28,8 @@
 //                 d_logits[sel_j] = g_j (dg_j - s), s = sum_i g_i dg_i, other experts 0
 //   SOFTMAX_TOPK: p = softmax over all E, g_j = p[sel_j];
 //                 d_logits[e] = (e == sel_j ? g_j dg_j : 0) - p_e s
-// One warp per token, lanes striding the E experts (coalesced row loads and
-// stores), warp xor trees for max and sums.
+// A group of lanes per token (a whole warp for E > 16), lanes striding the
+// E experts (coalesced row loads and stores), xor trees for max and sums.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -151,102 +151,132 @@ combine_bwd_kernel(const uint4 *__restrict__ dy, const uint4 *__restrict__ eo, c
     }
 }
 
-__device__ __forceinline__ float warp_max(float v)
+// Reductions over the G lanes of a group (G a power of two <= 32).
+template <int G>
+__device__ __forceinline__ float group_max(float v)
 {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    for (int o = G / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o, G));
     return v;
 }
-__device__ __forceinline__ float warp_sum(float v)
+template <int G>
+__device__ __forceinline__ float group_sum(float v)
 {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    for (int o = G / 2; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o, G));
     return v;
 }
 
 constexpr int kGateBwdThreads = 256;
 
-// EPL = experts per lane (ceil(E / 32)).
-template <int MODE, int EPL>
+// Gradient of one token's logits held by a group of G lanes: vals = the
+// lane's logits (experts sub, sub+G, ...; -inf past E or for an invalid
+// token), sel/dg = slot `sub`'s expert and gate gradient (sel < 0: none).
+// Returns the lane's d_logits in out.
+template <int MODE, int G, int EPL>
+__device__ __forceinline__ void token_logit_grad(float (&vals)[EPL], int sel, float dg, bool valid, int k, int E,
+                                                 int sub, float (&out)[EPL])
+{
+    // the selected expert's logit, from the lane of the group that holds it
+    float lsel = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+        const float v = __shfl_sync(0xffffffffu, vals[i], sel >= 0 ? sel & (G - 1) : 0, G);
+        if (sel >= 0 && sel / G == i) lsel = v;
+    }
+    float m, z;
+    if (MODE == MOE_TOPK_SOFTMAX) {
+        m = group_max<G>(lsel);
+        z = group_sum<G>(sel >= 0 ? expf(__fsub_rn(lsel, m)) : 0.0f);
+    } else {
+        float lm = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) lm = fmaxf(lm, vals[i]);
+        m = group_max<G>(lm);
+        float zs = 0.0f;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            vals[i] = (valid && sub + G * i < E) ? expf(__fsub_rn(vals[i], m)) : 0.0f;
+            zs = __fadd_rn(zs, vals[i]);
+        }
+        z = group_sum<G>(zs);
+    }
+    const float g = sel >= 0 ? __fdiv_rn(expf(__fsub_rn(lsel, m)), z) : 0.0f;
+    const float gdg = __fmul_rn(g, dg);
+    const float s = group_sum<G>(gdg);
+    // slot j's contribution to its expert's gradient
+    const float own = MODE == MOE_TOPK_SOFTMAX ? __fmul_rn(g, __fsub_rn(dg, s)) : gdg;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+        out[i] = MODE == MOE_TOPK_SOFTMAX ? 0.0f : -__fmul_rn(__fdiv_rn(vals[i], z), s);
+    for (int j = 0; j < k; ++j) {
+        const int ej = __shfl_sync(0xffffffffu, sel, j, G);
+        const float oj = __shfl_sync(0xffffffffu, own, j, G);
+#pragma unroll
+        for (int i = 0; i < EPL; ++i)
+            if (ej == sub + G * i) out[i] = __fadd_rn(out[i], oj);
+    }
+}
+
+// A group of G lanes per token (G = E rounded up to a power of two, at most
+// 32), 32/G tokens per warp, so the row loads and stores of a warp stay
+// contiguous for small E.  Lane i of a group holds experts i, i+G, ...
+// (EPL = ceil(E/G) of them); lane j < k also holds slot j.  Each warp takes
+// U token groups per iteration and issues all their loads (logits rows,
+// ids, gate gradients) before any arithmetic; the selected logits come
+// from the rows through shuffles, not from a dependent second load.
+template <int MODE, int G, int EPL, int U>
 __global__ void __launch_bounds__(kGateBwdThreads)
 gate_bwd_kernel(const float *__restrict__ logits, const int32_t *__restrict__ topk_idx,
                 const float *__restrict__ d_gates, long long T, int E, int k, float *__restrict__ d_logits, void *ws)
 {
     pdl_wait();
     pdl_launch_dependents();
+    constexpr int TPW = 32 / G;
     const int lane = threadIdx.x & 31;
-    const long long wpb = kGateBwdThreads / 32;
-    for (long long t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += (long long)gridDim.x * wpb) {
-        const float *l = logits + t * E;
-        // slot lanes: lane j < k holds slot j
-        int sel = -1;
-        float dg = 0.0f;
-        if (lane < k) {
-            sel = __ldg(topk_idx + t * k + lane);
-            dg = __ldg(d_gates + t * k + lane);
-            if (sel < 0 || sel >= E) {
+    const int sub = lane & (G - 1), grp = lane / G;
+    const long long nwarps = (long long)gridDim.x * (kGateBwdThreads / 32);
+    for (long long base = ((long long)blockIdx.x * (kGateBwdThreads / 32) + (threadIdx.x >> 5)) * TPW * U;
+         base < T; base += nwarps * TPW * U) {
+        float vals[U][EPL];
+        int sel[U];
+        float dg[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const long long t = base + u * TPW + grp;
+            const bool valid = t < T;
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) {
+                const int e = sub + G * i;
+                vals[u][i] = (valid && e < E) ? __ldg(logits + t * E + e) : -INFINITY;
+            }
+            sel[u] = -1;
+            dg[u] = 0.0f;
+            if (valid && sub < k) {
+                sel[u] = __ldg(topk_idx + t * k + sub);
+                dg[u] = __ldg(d_gates + t * k + sub);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const long long t = base + u * TPW + grp;
+            const bool valid = t < T;
+            if (sel[u] >= E || (valid && sub < k && sel[u] < 0)) {
                 record_status(ws, MOE_ERR_DEVICE_DATA);
-                sel = -1;
+                sel[u] = -1;
             }
-        }
-        const float lsel = sel >= 0 ? __ldg(l + sel) : -INFINITY;
-        float vals[EPL];
-        float m;
-        if (MODE == MOE_TOPK_SOFTMAX) {
-            m = warp_max(lsel);
-        } else {
-            float lm = -INFINITY;
+            float out[EPL];
+            token_logit_grad<MODE, G, EPL>(vals[u], sel[u], dg[u], valid, k, E, sub, out);
+            if (valid) {
+                float *dl = d_logits + t * E;
 #pragma unroll
-            for (int i = 0; i < EPL; ++i) {
-                const int e = lane + 32 * i;
-                vals[i] = e < E ? __ldg(l + e) : -INFINITY;
-                lm = fmaxf(lm, vals[i]);
+                for (int i = 0; i < EPL; ++i) {
+                    const int e = sub + G * i;
+                    if (e < E) dl[e] = out[i];
+                }
             }
-            m = warp_max(lm);
-        }
-        float z;
-        if (MODE == MOE_TOPK_SOFTMAX) {
-            z = warp_sum(sel >= 0 ? expf(__fsub_rn(lsel, m)) : 0.0f);
-        } else {
-            float zs = 0.0f;
-#pragma unroll
-            for (int i = 0; i < EPL; ++i) {
-                vals[i] = (lane + 32 * i) < E ? expf(__fsub_rn(vals[i], m)) : 0.0f;
-                zs += vals[i];
-            }
-            z = warp_sum(zs);
-        }
-        const float g = sel >= 0 ? __fdiv_rn(expf(__fsub_rn(lsel, m)), z) : 0.0f;
-        const float gdg = __fmul_rn(g, dg);
-        const float s = warp_sum(gdg);
-        // slot contribution to its expert's gradient
-        const float own = MODE == MOE_TOPK_SOFTMAX ? __fmul_rn(g, __fsub_rn(dg, s)) : gdg;
-        float out[EPL];
-#pragma unroll
-        for (int i = 0; i < EPL; ++i) {
-            out[i] = MODE == MOE_TOPK_SOFTMAX ? 0.0f : -__fmul_rn(__fdiv_rn(vals[i], z), s);
-        }
-        for (int j = 0; j < k; ++j) {
-            const int ej = __shfl_sync(0xffffffffu, sel, j);
-            const float oj = __shfl_sync(0xffffffffu, own, j);
-            if (ej >= 0 && (ej & 31) == lane) {
-#pragma unroll
-                for (int i = 0; i < EPL; ++i)
-                    if (ej == lane + 32 * i) out[i] = __fadd_rn(out[i], oj);
-            }
-        }
-        float *dl = d_logits + t * E;
-#pragma unroll
-        for (int i = 0; i < EPL; ++i) {
-            const int e = lane + 32 * i;
-            if (e < E) dl[e] = out[i];
         }
     }
-}
-
-long long grid_tokens(long long n)
-{
-    return n < 0x7FFFFFFFll ? (n < 1 ? 1 : n) : 0x7FFFFFFFll;
 }
 
 int resident_blocks(const void *fn, int threads)
@@ -277,23 +307,45 @@ cudaError_t launch_cbwd_k(const void *dy, const void *eo, const moe_layout *L, c
                       L->ws);
 }
 
+template <int MODE, int G, int EPL, int U = (EPL <= 2 ? 4 : (EPL <= 4 ? 2 : 1))>
+cudaError_t launch_gbwd(const float *logits, const int32_t *topk_idx, const float *d_gates, int T, int E, int k,
+                        float *d_logits, void *ws, cudaStream_t s)
+{
+    static int resident[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int &res = resident[dev & 63];
+    if (res == 0)
+        res = resident_blocks(reinterpret_cast<const void *>(gate_bwd_kernel<MODE, G, EPL, U>), kGateBwdThreads);
+    const long long per_block = (long long)(kGateBwdThreads / 32) * (32 / G) * U;
+    const long long need = ((long long)T + per_block - 1) / per_block;
+    const unsigned grid = (unsigned)(need < res ? need : res);
+    return launch_pdl(gate_bwd_kernel<MODE, G, EPL, U>, dim3(grid), dim3(kGateBwdThreads), 0, s, logits, topk_idx,
+                      d_gates, (long long)T, E, k, d_logits, ws);
+}
+
 template <int MODE>
 cudaError_t launch_gbwd_m(const float *logits, const int32_t *topk_idx, const float *d_gates, int T, int E, int k,
                           float *d_logits, void *ws, cudaStream_t s)
 {
-    const long long blocks = ((long long)T + kGateBwdThreads / 32 - 1) / (kGateBwdThreads / 32);
-    const unsigned grid = (unsigned)grid_tokens(blocks);
-    const int epl = (E + 31) / 32;
-#define MOE_GBWD_CASE(N)                                                                                          \
-    case N:                                                                                                       \
-        return launch_pdl(gate_bwd_kernel<MODE, N>, dim3(grid), dim3(kGateBwdThreads), 0, s, logits, topk_idx,   \
-                          d_gates, (long long)T, E, k, d_logits, ws);
-    switch (epl) {
-        MOE_GBWD_CASE(1) MOE_GBWD_CASE(2) MOE_GBWD_CASE(3) MOE_GBWD_CASE(4)
-        MOE_GBWD_CASE(5) MOE_GBWD_CASE(6) MOE_GBWD_CASE(7) MOE_GBWD_CASE(8)
+#define MOE_GBWD(G, EPL) return launch_gbwd<MODE, G, EPL>(logits, topk_idx, d_gates, T, E, k, d_logits, ws, s)
+    if (E <= 1) MOE_GBWD(1, 1);
+    if (E <= 2) MOE_GBWD(2, 1);
+    if (E <= 4) MOE_GBWD(4, 1);
+    if (E <= 8) MOE_GBWD(8, 1);
+    if (E <= 16) MOE_GBWD(16, 1);
+    switch ((E + 31) / 32) {
+    case 1: MOE_GBWD(32, 1);
+    case 2: MOE_GBWD(32, 2);
+    case 3: MOE_GBWD(32, 3);
+    case 4: MOE_GBWD(32, 4);
+    case 5: MOE_GBWD(32, 5);
+    case 6: MOE_GBWD(32, 6);
+    case 7: MOE_GBWD(32, 7);
+    case 8: MOE_GBWD(32, 8);
     default: return cudaErrorInvalidValue;
     }
-#undef MOE_GBWD_CASE
+#undef MOE_GBWD
 }
 
 }  // namespace

@@ -11,7 +11,7 @@
 namespace moe {
 
 // ---------------------------------------------------------------------------
-// Workspace.  A fixed 4 KiB header of counters followed by the decoupled
+// Workspace.  A fixed 8 KiB header of counters followed by the decoupled
 // look-back flag words of the layout scan (one 64-bit word per tile and
 // expert).  Every counter is returned to zero by the kernel that used it, so
 // a zeroed workspace stays valid from call to call.
@@ -29,12 +29,17 @@ struct WsHeader {
     // block learns both with a single atomic; the epoch tags flag words and
     // is bumped by the block that draws the last tile id of a call
     unsigned long long tile_epoch;
-    unsigned pad0[26];
+    unsigned quant_ticket;         // grouped FP8 encode: finished blocks
+    unsigned pad0[25];
     unsigned gate_counts[MOE_MAX_EXPERTS];  // gate: per-expert totals
     unsigned part_tok[MOE_MAX_EXPERTS];     // layout: per-partition token totals
+    // grouped FP8 quantiser: per group (expert, or group 0 for global) the
+    // max key (max_word) and min key (min_word) of its rows, zero = empty
+    unsigned quant_max[MOE_MAX_EXPERTS];
+    unsigned quant_min[MOE_MAX_EXPERTS];
 };
-static_assert(sizeof(WsHeader) <= 4096, "workspace header must fit 4 KiB");
-constexpr size_t kWsHeaderBytes = 4096;
+static_assert(sizeof(WsHeader) <= 8192, "workspace header must fit 8 KiB");
+constexpr size_t kWsHeaderBytes = 8192;
 
 __host__ __device__ inline unsigned long long *ws_flags(void *ws)
 {
@@ -142,6 +147,12 @@ cudaError_t launch_dispatch_fp8(const void *x, int T, int H, const moe_layout *L
                                 float *scales, cudaStream_t s);
 cudaError_t launch_combine(const void *eo, const moe_layout *L, const float *gates,
                            const void *shared, int Ks, int T, int H, void *y, cudaStream_t s);
+cudaError_t launch_dispatch_fp8_grouped(const void *x, int T, int H, const moe_layout *L, int mode, void *packed,
+                                        float *scales, cudaStream_t s);
+cudaError_t launch_quantize_rows(const void *rows, const moe_layout *L, int H, int mode, void *codes, float *scales,
+                                 cudaStream_t s);
+cudaError_t launch_combine_fp8(const void *codes, const float *scales, const moe_layout *L, const float *gates,
+                               const void *shared, int Ks, int T, int H, void *y, cudaStream_t s);
 cudaError_t launch_combine_backward(const void *dy, const void *eo, const moe_layout *L, const float *gates, int T,
                                    int H, void *d_eo, float *d_gates, cudaStream_t s);
 cudaError_t launch_gate_backward(const float *logits, const int32_t *topk_idx, const float *d_gates, int T, int E,

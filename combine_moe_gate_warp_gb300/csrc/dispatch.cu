@@ -18,9 +18,8 @@
 // the hardware e4m3 satfinite conversion, and writes 16 codes per store.
 #include <climits>
 
-#include <cuda_fp8.h>
-
 #include "common.cuh"
+#include "fp8.cuh"
 
 namespace moe {
 namespace {
@@ -82,30 +81,6 @@ dispatch_bf16_kernel(const uint4 *__restrict__ x, long long T, int nvec, int k,
         }
         __syncthreads();
     }
-}
-
-// fp32 bit pattern -> int key with numeric order and -0 < +0.
-__device__ __forceinline__ int f32_order_key(unsigned b)
-{
-    return (b & 0x80000000u) ? (int)(b ^ 0x7FFFFFFFu) : (int)b;
-}
-__device__ __forceinline__ float key_to_f32(int key)
-{
-    unsigned b = (unsigned)key;
-    return __uint_as_float(key < 0 ? (b ^ 0x7FFFFFFFu) : b);
-}
-
-__device__ __forceinline__ unsigned short e4m3x2(float lo, float hi)
-{
-    return (unsigned short)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
-}
-
-// Quantise one bf16 pair word into two codes (low code = low element).
-__device__ __forceinline__ unsigned quant_pair(unsigned w, float zero, float scale)
-{
-    const float a = __fdiv_rn(__fsub_rn(bf16lo(w), zero), scale);
-    const float b = __fdiv_rn(__fsub_rn(bf16hi(w), zero), scale);
-    return (unsigned)e4m3x2(a, b);
 }
 
 // One block per token.  Thread c handles chunk pairs p = c + i*128 (a pair

@@ -22,9 +22,10 @@ class RouteShape:
     k: int
     P: int
     mode: int = abi.MOE_TOPK_SOFTMAX
-    fp8: bool = False
+    fp8: int = 0          # dispatch transport: 0 bf16, else a MOE_FP8_* quantiser mode
     Ks: int = 0
     capacity: int = 0
+    fp8_combine: int = 0  # expert outputs: 0 bf16, else quantised with this MOE_FP8_* mode
 
 
 def _check_input(t, dtype, shape, name):
@@ -62,6 +63,9 @@ class RoutePlan:
             self.packed = torch.empty((rows, s.H), dtype=torch.bfloat16, device=self.device)
             self.scales = None
         self.y = torch.empty((max(T, 1), s.H), dtype=torch.bfloat16, device=self.device)
+        if s.fp8_combine:
+            self.eo_codes = torch.empty((rows, s.H), dtype=torch.uint8, device=self.device)
+            self.eo_scales = torch.empty((rows, 2), dtype=torch.float32, device=self.device)
         self._bind()
 
     def _bind(self):
@@ -106,14 +110,47 @@ class RoutePlan:
         abi._check(self._lib.moe_combine(expert_out.data_ptr(), self._Lref, self.gates.data_ptr(), sh, s.Ks, s.T,
                                          s.H, self.y.data_ptr(), self._s), "moe_combine")
 
+    def quantize_expert_out(self, expert_out: torch.Tensor):
+        """FP8-encode the expert-output rows (the expert side of the return
+        transport) into eo_codes / eo_scales."""
+        s = self.shape
+        _check_input(expert_out, torch.bfloat16, (), "expert_out")
+        if expert_out.shape[-1] != s.H:
+            raise ValueError("expert_out: last dimension must be H")
+        abi._check(self._lib.moe_quantize_rows(expert_out.data_ptr(), self._Lref, s.H, s.fp8_combine,
+                                               self.eo_codes.data_ptr(), self.eo_scales.data_ptr(), self._s),
+                   "moe_quantize_rows")
+
+    def combine_fp8(self, shared_out: torch.Tensor | None = None):
+        """Combine from eo_codes / eo_scales."""
+        s = self.shape
+        sh = None
+        if s.Ks:
+            _check_input(shared_out, torch.bfloat16, (s.Ks, s.T, s.H), "shared_out")
+            sh = shared_out.data_ptr()
+        abi._check(self._lib.moe_combine_fp8(self.eo_codes.data_ptr(), self.eo_scales.data_ptr(), self._Lref,
+                                             self.gates.data_ptr(), sh, s.Ks, s.T, s.H, self.y.data_ptr(), self._s),
+                   "moe_combine_fp8")
+
     def step(self, logits, x, expert_out, shared_out=None):
-        """gate -> layout -> dispatch -> combine (4 kernel launches)."""
+        """gate -> layout -> dispatch -> combine; with FP8 expert outputs the
+        combine is quantise (expert side) -> FP8 combine."""
         self.gate(logits)
         self.dispatch_layout()
         self.dispatch(x)
-        self.combine(expert_out, shared_out)
+        if self.shape.fp8_combine:
+            self.quantize_expert_out(expert_out)
+            self.combine_fp8(shared_out)
+        else:
+            self.combine(expert_out, shared_out)
 
-    KERNELS_PER_STEP = 4
+    def launches_per_step(self) -> int:
+        """Kernel launches of one step (the grouped FP8 modes take two)."""
+        s = self.shape
+        n = 3 + (2 if s.fp8 in (abi.MOE_FP8_PER_EXPERT, abi.MOE_FP8_GLOBAL) else 1)
+        if s.fp8_combine:
+            n += 1 + (2 if s.fp8_combine in (abi.MOE_FP8_PER_EXPERT, abi.MOE_FP8_GLOBAL) else 1)
+        return n
 
     # backward through the same layout -------------------------------------
     def _bwd_buffers(self):

@@ -21,6 +21,10 @@ Workloads (shapes taken from the workloads the source pages discuss):
   prefill_cap T=262144 (batch 128 x seq 2048), H=4096, E=64, k=8, P=8,
               logits N(0, 1.5^2) + the same Zipf-like bias, capacity
               ceil(1.25*T*k/E) per expert, bf16 transport
+  fp8_expert, fp8_global, fp8_both
+              fp8_skewed's shape and inputs with per-expert / global FP8
+              groups for the dispatch, or per-token FP8 both ways (the
+              expert outputs quantised per row and combined from FP8)
 
 Distributions: x ~ N(0,1) drawn in fp32 and rounded to bf16; router logits
 fp32 as above; expert outputs (the FFN is not part of this path) and shared
@@ -46,12 +50,13 @@ class Workload:
     k: int
     P: int
     mode: int = TOPK_SOFTMAX
-    fp8: bool = False
+    fp8: int = 0           # dispatch: 0 bf16, 1 per-token, 2 per-expert, 3 global FP8
     Ks: int = 0
     logit_std: float = 1.0
     zipf_bias: bool = False
     capacity_factor: float = 0.0  # 0: no capacity limit
     identity_experts: bool = False
+    fp8_combine: int = 0   # expert outputs: 0 bf16, else FP8 with this quantiser mode
     seed: int = 1234
     note: str = field(default="", compare=False)
 
@@ -82,12 +87,18 @@ WORKLOADS = {
     "v2_top2": Workload("v2_top2", T=16384, H=5120, E=16, k=2, P=4, seed=1235),
     "fine_shared": Workload("fine_shared", T=8192, H=2048, E=32, k=8, P=8, mode=SOFTMAX_TOPK,
                             Ks=2, seed=1236),
-    "fp8_skewed": Workload("fp8_skewed", T=65536, H=4096, E=64, k=2, P=8, fp8=True,
+    "fp8_skewed": Workload("fp8_skewed", T=65536, H=4096, E=64, k=2, P=8, fp8=1,
                            zipf_bias=True, seed=1237),
     "prefill_cap": Workload("prefill_cap", T=262144, H=4096, E=64, k=8, P=8, logit_std=1.5,
                             zipf_bias=True, capacity_factor=1.25, seed=1238),
 }
-ORDER = ["tiny", "v2_top2", "fine_shared", "fp8_skewed", "prefill_cap"]
+# The other quantiser modes on the fp8_skewed shape and inputs (same seed):
+# per-expert and global groups for the dispatch, and FP8 both ways (per-token
+# dispatch, per-token expert outputs into an FP8 combine).
+for _name, _kw in (("fp8_expert", dict(fp8=2)), ("fp8_global", dict(fp8=3)),
+                   ("fp8_both", dict(fp8=1, fp8_combine=1))):
+    WORKLOADS[_name] = Workload(**{**WORKLOADS["fp8_skewed"].__dict__, "name": _name, **_kw})
+ORDER = ["tiny", "v2_top2", "fine_shared", "fp8_skewed", "prefill_cap", "fp8_expert", "fp8_global", "fp8_both"]
 
 
 def _gen(device, seed: int) -> torch.Generator:
@@ -152,6 +163,11 @@ def make_d_packed(w: Workload, rows: int, device="cuda") -> torch.Tensor:
     return _randn_bf16(rows, w.H, _gen(device, w.seed + 505), device)
 
 
+def make_d_gates(w: Workload, device="cuda") -> torch.Tensor:
+    """Seeded stand-in for the gradient of the gate weights [T, k] fp32."""
+    return torch.randn((w.T, w.k), generator=_gen(device, w.seed + 606), device=device, dtype=torch.float32)
+
+
 def make_inputs(w: Workload, device="cuda") -> dict:
     return dict(logits=make_logits(w, device), x=make_x(w, device), shared=make_shared(w, device))
 
@@ -182,10 +198,11 @@ def gib(n: int) -> float:
 def describe(w: Workload) -> str:
     c = w.capacity
     return (f"{w.name}: T={w.T} H={w.H} E={w.E} k={w.k} P={w.P} mode={w.mode} fp8={int(w.fp8)} "
+            f"fp8_combine={w.fp8_combine} "
             f"Ks={w.Ks} capacity={c if c else 'none'}")
 
 
 __all__ = ["Workload", "WORKLOADS", "ORDER", "make_inputs", "make_logits", "make_x",
-           "make_shared", "make_expert_out", "make_dy", "make_d_packed", "zipf_bias", "nbytes_roofline",
+           "make_shared", "make_expert_out", "make_dy", "make_d_packed", "make_d_gates", "zipf_bias", "nbytes_roofline",
            "nbytes_backward", "describe",
            "TOPK_SOFTMAX", "SOFTMAX_TOPK", "gib", "math"]

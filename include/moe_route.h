@@ -71,6 +71,14 @@ typedef int moe_status;
 #define MOE_SOFTMAX_TOPK 1  /* softmax over all E logits, keep the k selected, no renormalisation
                                (DeepSeekMoE fine-grained routing, [P2] sec. 2.1 and 4.1) */
 
+/* FP8 quantiser modes ([P1] sec. 5.2: per-token, per-expert and global),
+ * for moe_dispatch's `fp8` argument and moe_quantize_rows.  One affine
+ * (scale, zero) pair per group, from the max and min over every element of
+ * the group's rows ([P1] sec. 3.1's per-token formula). */
+#define MOE_FP8_PER_TOKEN 1   /* each packed row is its own group */
+#define MOE_FP8_PER_EXPERT 2  /* the rows sent to one expert */
+#define MOE_FP8_GLOBAL 3      /* every transported row */
+
 #define MOE_MAX_EXPERTS 256
 #define MOE_MAX_TOPK 16
 #define MOE_MAX_SHARED 8
@@ -200,17 +208,23 @@ moe_status moe_dispatch_layout_noalloc(const int32_t *topk_idx, const int32_t *e
 /*
  * moe_dispatch -- permute and pack token hidden states into the
  * expert-contiguous send buffer ([P4] sec. 7 Dispatch detail), optionally
- * as per-token affine FP8 ([P1] sec. 3.1: per-token min/max, affine map).
+ * as affine FP8 ([P1] sec. 3.1: per-token min/max, affine map; sec. 5.2:
+ * per-token, per-expert or global groups).
  *
  *   x       [T, H] bf16.
  *   fp8 = 0: packed [r_max, H] bf16; row r = x[src_pos[r] / k] bit-exactly.
- *   fp8 = 1: packed [r_max, H] uint8 e4m3 codes, scales [r_max, 2] fp32
- *            (scale, zero) of the row's token, with (fp32, in this order)
- *            mx, mn = max and min of the row (-0 < +0),
+ *   fp8 = MOE_FP8_PER_TOKEN (1): packed [r_max, H] uint8 e4m3 codes, scales
+ *            [r_max, 2] fp32 (scale, zero) of the row's token, with (fp32, in
+ *            this order) mx, mn = max and min of the row (-0 < +0),
  *            zero = (mx + mn) * 0.5, scale = (mx - mn) / 896,
  *            code = e4m3 satfinite RNE((x - zero) / scale);
  *            a constant row has scale 0 and all-zero codes.
  *            Dequantise as zero + scale * e4m3_value(code).  x must be finite.
+ *   fp8 = MOE_FP8_PER_EXPERT (2) / MOE_FP8_GLOBAL (3): the same, with mx, mn
+ *            taken over every element of the rows sent to the row's expert /
+ *            of every transported row; scales still holds the pair per row.
+ *            Two kernels (extremes, then codes), which use the workspace L->ws
+ *            and leave it clean.
  *   Rows >= R are not written.
  */
 moe_status moe_dispatch(const void *x, int T, int H, const moe_layout *L, int fp8,
@@ -233,6 +247,36 @@ moe_status moe_dispatch(const void *x, int T, int H, const moe_layout *L, int fp
 moe_status moe_combine(const void *expert_out, const moe_layout *L, const float *gates,
                        const void *shared_out, int Ks, int T, int H, void *y,
                        moe_stream_t stream);
+
+/*
+ * moe_quantize_rows -- affine FP8 encode of packed bf16 rows, e.g. the
+ * expert outputs before they travel back to the combine ([P1] sec. 3.1: the
+ * per-token map applies to each token's expert output vector; sec. 5.2:
+ * per-token, per-expert or global groups).
+ *
+ *   rows      [r_max, H] bf16 in the packed-row layout of L (rows >= R are
+ *             neither read nor written).
+ *   mode      MOE_FP8_PER_TOKEN (each row its own group), MOE_FP8_PER_EXPERT
+ *             (rows offsets[e] .. offsets[e+1]-1), MOE_FP8_GLOBAL (rows 0..R-1).
+ *   codes out [r_max, H] uint8 e4m3, scales out [r_max, 2] fp32 (scale, zero),
+ *             with the formulas of moe_dispatch.  H % 16 == 0, H <= 16384.
+ *   The grouped modes use the workspace L->ws and leave it clean.
+ */
+moe_status moe_quantize_rows(const void *rows, const moe_layout *L, int H, int mode,
+                             void *codes, float *scales, moe_stream_t stream);
+
+/*
+ * moe_combine_fp8 -- moe_combine over FP8 expert outputs (codes and
+ * (scale, zero) per packed row, as written by moe_quantize_rows):
+ *     acc = 0; for kept j ascending:
+ *         acc = fmaf(g[t,j], fmaf(scale_r, e4m3_value(code_r), zero_r), acc);
+ *     for s ascending: acc = acc + shared[s,t]; y = bf16 RNE(acc)
+ * (r = dst_row[t,j]; every operation fp32 round-to-nearest).  Arguments as
+ * moe_combine; H % 16 == 0.
+ */
+moe_status moe_combine_fp8(const void *codes, const float *scales, const moe_layout *L,
+                           const float *gates, const void *shared_out, int Ks, int T, int H,
+                           void *y, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Backward of the path.  The gradients retrace the forward routing through
@@ -294,7 +338,7 @@ moe_status moe_dispatch_backward(const void *d_packed, const moe_layout *L, int 
  *                       d_logits[sel_j] = g_j (d_gates[t,j] - s), others 0.
  *     MOE_SOFTMAX_TOPK: p = softmax of all E logits, g_j = p[sel_j];
  *                       d_logits[e] = (e == sel_j ? g_j d_gates[t,j] : 0) - p_e s.
- *   ws, ws_bytes  any workspace of >= 4096 bytes (only its status word is used).
+ *   ws, ws_bytes  any workspace of >= 8192 bytes (only its status word is used).
  */
 moe_status moe_gate_backward(const float *logits, const int32_t *topk_idx, const float *d_gates,
                              int T, int E, int k, int mode, float *d_logits,

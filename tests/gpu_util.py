@@ -1,12 +1,20 @@
 """Helpers for the GPU parity tests: run the CUDA path through the C ABI,
-run the oracle on the same inputs, and compare."""
+run the oracle on the same inputs, and compare.
+
+Every oracle input is either a seeded input (from `workloads`) or an oracle
+output; nothing the CUDA path computed is fed to the oracle.  Where a later
+call of the path consumes an earlier call's result (the combine reads the
+gate weights), the test hands that call the oracle's value instead, so both
+sides start from the same bits: after the gate has been compared, the
+oracle's fp32 gate weights replace the GPU's in the plan before the layout
+runs."""
 from __future__ import annotations
 
 import numpy as np
 import torch
 
 import oracle
-from combine_moe_gate_warp_gb300 import RoutePlan, RouteShape, workloads
+from combine_moe_gate_warp_gb300 import RoutePlan, RouteShape, abi, workloads
 
 
 def bits(t: torch.Tensor) -> np.ndarray:
@@ -19,17 +27,28 @@ def f_of_bits(b: np.ndarray) -> np.ndarray:
 
 
 def shape_of(w: workloads.Workload) -> RouteShape:
-    return RouteShape(T=w.T, H=w.H, E=w.E, k=w.k, P=w.P, mode=w.mode, fp8=w.fp8, Ks=w.Ks,
-                      capacity=w.capacity)
+    return RouteShape(T=w.T, H=w.H, E=w.E, k=w.k, P=w.P, mode=w.mode, fp8=int(w.fp8), Ks=w.Ks,
+                      capacity=w.capacity, fp8_combine=int(w.fp8_combine))
+
+
+def gate_with_oracle(w, plan, logits: torch.Tensor):
+    """moe_gate on the GPU, the oracle's gate on the same logits, then the
+    oracle's fp32 gates written into the plan for the calls that follow.
+    Returns (GPU gates before the swap, oracle (idx, g64, counts, aux, ent))."""
+    plan.gate(logits)
+    gates_pre = plan.gates.clone()
+    og = oracle.gate(logits.cpu().numpy(), w.k, w.mode)
+    if w.T:
+        plan.gates[:w.T].copy_(torch.from_numpy(og[1].astype(np.float32)).to(plan.gates.device))
+    return gates_pre, og
 
 
 def run_gpu(w: workloads.Workload, inputs: dict, device="cuda"):
-    """The four calls on the GPU.  Returns the plan, host snapshots of the
-    gate outputs taken before the layout zeroes dropped gates, R, and the
-    expert outputs used by the combine."""
+    """The path on the GPU.  Returns the plan, the GPU's gate weights, the
+    oracle's gate outputs, R, the expert outputs used by the combine and the
+    device status."""
     plan = RoutePlan(shape_of(w), device)
-    plan.gate(inputs["logits"])
-    gates_pre = plan.gates.clone()
+    gates_pre, og = gate_with_oracle(w, plan, inputs["logits"])
     plan.dispatch_layout()
     plan.dispatch(inputs["x"])
     R = int(plan.layout.offsets[w.E].item())
@@ -37,13 +56,17 @@ def run_gpu(w: workloads.Workload, inputs: dict, device="cuda"):
         eo = plan.packed
     else:
         eo = workloads.make_expert_out(w, max(R, 1), device)
-    plan.combine(eo, inputs["shared"])
+    if w.fp8_combine:
+        plan.quantize_expert_out(eo)
+        plan.combine_fp8(inputs["shared"])
+    else:
+        plan.combine(eo, inputs["shared"])
     status = plan.status()
-    return plan, gates_pre, R, eo, status
+    return plan, gates_pre, og, R, eo, status
 
 
-def check_gate(w, plan, gates_pre, logits_np, tol_gate=1e-6):
-    idx, g64, counts, aux, ent = oracle.gate(logits_np, w.k, w.mode)
+def check_gate(w, plan, gates_pre, og, tol_gate=1e-6):
+    idx, g64, counts, aux, ent = og
     T = w.T
     assert np.array_equal(plan.topk_idx.cpu().numpy()[:T], idx), "topk_idx differs from the oracle"
     assert np.array_equal(plan.expert_counts.cpu().numpy(), counts), "expert_counts differ"
@@ -56,9 +79,10 @@ def check_gate(w, plan, gates_pre, logits_np, tol_gate=1e-6):
     return idx, counts
 
 
-def check_layout(w, plan, idx, gates_pre):
-    gpre = gates_pre.cpu().numpy()[:w.T]
-    L = oracle.layout(idx, w.E, w.P, w.capacity, gates_f32=gpre)
+def check_layout(w, plan, og):
+    """The GPU layout (run on the oracle's gates) against the oracle's."""
+    idx, g64 = og[0], og[1]
+    L = oracle.layout(idx, w.E, w.P, w.capacity, gates_f32=g64.astype(np.float32))
     lay = plan.layout
     A = w.T * w.k
     assert np.array_equal(lay.counts.cpu().numpy(), L["counts"]), "kept counts"
@@ -84,6 +108,19 @@ def sample_rows(n: int, rng, m: int = 512) -> np.ndarray:
     return np.unique(pick).astype(np.int64)
 
 
+def oracle_fp8_rows(mode, src_bits, src_row_all, offsets, rows):
+    """The oracle's codes and scales of packed rows `rows` for a quantiser
+    mode: group extremes over every row (src_row_all[r] = source row of
+    packed row r), then the listed rows encoded."""
+    R = src_row_all.size
+    if mode == oracle.FP8_PER_TOKEN:
+        return oracle.quantize_rows_grouped(src_bits, src_row_all[rows], np.arange(rows.size, dtype=np.int32),
+                                            rows.size)
+    group_all, ng = oracle.row_groups(mode, offsets, np.arange(R))
+    params = oracle.fp8_group_params(src_bits, src_row_all, group_all, ng)
+    return oracle.quantize_rows_with_params(src_bits, src_row_all[rows], group_all[rows], params)
+
+
 def check_dispatch(w, plan, L, x_bits, rows):
     if rows.size == 0:
         return
@@ -91,7 +128,11 @@ def check_dispatch(w, plan, L, x_bits, rows):
     if w.fp8:
         got = plan.packed.index_select(0, rows_t).cpu().numpy()
         got_s = plan.scales.index_select(0, rows_t).cpu().numpy()
-        want, want_s = oracle.dispatch_fp8_rows(x_bits, w.k, L["src_pos"], rows)
+        if int(w.fp8) == oracle.FP8_PER_TOKEN:
+            want, want_s = oracle.dispatch_fp8_rows(x_bits, w.k, L["src_pos"], rows)
+        else:
+            src_row_all = (L["src_pos"].astype(np.int64) // w.k)
+            want, want_s = oracle_fp8_rows(int(w.fp8), x_bits, src_row_all, L["offsets"], rows)
         assert np.array_equal(got, want), f"fp8 codes differ in {np.sum(np.any(got != want, 1))} rows"
         assert np.array_equal(got_s.view(np.uint32), want_s.view(np.uint32)), "fp8 scales differ"
     else:
@@ -106,34 +147,80 @@ def _ulp_bf16(v):
     return 2.0 ** (np.maximum(e, -126) - 7)
 
 
-def check_combine(w, plan, L, eo, shared, tokens):
+def oracle_expert_rows(w, L, eo, x_bits, need):
+    """bf16 bits of expert-output rows `need` as the oracle sees them: the
+    seeded tensor, or, for identity experts, the oracle's own dispatch."""
+    if need.size == 0:
+        return np.zeros((1, w.H), np.uint16)
+    if w.identity_experts:
+        return oracle.dispatch_bf16_rows(x_bits, w.k, L["src_pos"], need)
+    return bits(eo.index_select(0, torch.from_numpy(need.astype(np.int64)).to(eo.device)))
+
+
+def check_combine(w, plan, L, eo, shared, tokens, x_bits=None):
     """Bit-exact against the oracle's pinned fp32 order, and within the
-    error bound of the fp64 reference; both fed the GPU's fp32 gates and
-    the oracle's layout (bit-equal to the GPU's)."""
+    error bound of the fp64 reference, both sides fed the oracle's gates
+    and layout and the seeded expert outputs."""
     if tokens.size == 0:
         return
     T, k = w.T, w.k
     dst = L["dst_row"].reshape(T, k)[tokens]
     need = np.unique(dst[dst >= 0])
-    eo_sub = bits(eo.index_select(0, torch.from_numpy(need.astype(np.int64)).to(eo.device))) \
-        if need.size else np.zeros((1, w.H), np.uint16)
     remap = np.full(T * k, -1, np.int32)
     flat = (tokens[:, None] * k + np.arange(k)[None, :]).ravel()
     sub = dst.ravel()
     remap[flat] = np.where(sub >= 0, np.searchsorted(need, sub), -1)
     n = tokens.size
-    g_c = plan.gates.cpu().numpy()[:T][tokens]
+    g_c = L["gates"][tokens]
     remap_c = remap.reshape(T, k)[tokens].ravel()
     sh_c = None
     if shared is not None:  # [Ks, T, H] -> [Ks, n, H], tokens renumbered 0..n-1
         sh_c = bits(shared.index_select(1, torch.from_numpy(tokens).to(shared.device)))
-    y_ref = oracle.combine_f32order(eo_sub, g_c, remap_c, np.arange(n), n, k, sh_c)
-    ref, mag = oracle.combine_ref64(eo_sub, g_c, remap_c, np.arange(n), n, k, sh_c)
     got = bits(plan.y.index_select(0, torch.from_numpy(tokens).to(plan.y.device)))
+    n_terms = k + w.Ks
+    if w.fp8_combine:
+        R = L["R"]
+        mode = int(w.fp8_combine)
+        if mode == oracle.FP8_PER_TOKEN:
+            eo_sub = oracle_expert_rows(w, L, eo, x_bits, need)
+            codes, scales = oracle.quantize_rows_grouped(eo_sub, np.arange(need.size), np.arange(need.size,
+                                                         dtype=np.int32), need.size)
+        else:
+            eo_all = oracle_expert_rows(w, L, eo, x_bits, np.arange(R))
+            codes, scales = oracle_fp8_rows(mode, eo_all, np.arange(R, dtype=np.int64), L["offsets"], need)
+        if need.size:
+            need_t = torch.from_numpy(need.astype(np.int64)).to(plan.eo_codes.device)
+            assert np.array_equal(plan.eo_codes.index_select(0, need_t).cpu().numpy(), codes), \
+                "expert-output FP8 codes differ"
+            assert np.array_equal(plan.eo_scales.index_select(0, need_t).cpu().numpy().view(np.uint32),
+                                  scales.view(np.uint32)), "expert-output FP8 scales differ"
+        else:
+            codes, scales = np.zeros((1, w.H), np.uint8), np.zeros((1, 2), np.float32)
+        y_ref = oracle.combine_fp8_f32order(codes, scales, g_c, remap_c, np.arange(n), n, k, sh_c)
+        ref, mag = oracle.combine_fp8_ref64(codes, scales, g_c, remap_c, np.arange(n), n, k, sh_c)
+        n_terms += 1  # the dequantisation rounding
+    else:
+        eo_sub = oracle_expert_rows(w, L, eo, x_bits, need)
+        y_ref = oracle.combine_f32order(eo_sub, g_c, remap_c, np.arange(n), n, k, sh_c)
+        ref, mag = oracle.combine_ref64(eo_sub, g_c, remap_c, np.arange(n), n, k, sh_c)
     assert np.array_equal(got, y_ref), f"combine differs from the pinned fp32 order in {np.sum(got != y_ref)} values"
     err = np.abs(f_of_bits(got).astype(np.float64) - ref)
-    n_terms = k + w.Ks
     bound = _ulp_bf16(ref) + n_terms * 2.0 ** -24 * mag
     assert np.all(err <= bound), "combine outside the fp64 error bound"
     within_ulp = float(np.mean(err <= _ulp_bf16(ref)))
     return within_ulp
+
+
+def route_checked(w, plan, logits):
+    """Gate (compared, then the oracle's gates swapped in) and layout
+    (compared) on an existing plan; returns the oracle layout."""
+    gates_pre, og = gate_with_oracle(w, plan, logits)
+    plan.dispatch_layout()
+    assert plan.status() == 0
+    check_gate(w, plan, gates_pre, og)
+    return check_layout(w, plan, og)
+
+
+__all__ = ["bits", "f_of_bits", "shape_of", "gate_with_oracle", "run_gpu", "check_gate", "check_layout",
+           "sample_rows", "oracle_fp8_rows", "check_dispatch", "oracle_expert_rows", "check_combine",
+           "route_checked", "abi"]

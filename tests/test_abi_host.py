@@ -39,8 +39,8 @@ def test_exports_every_declared_symbol(lib):
 
 def test_workspace_and_rows_queries(lib):
     from combine_moe_gate_warp_gb300 import abi
-    assert abi.moe_workspace_size(16384, 16, 2, 4) == 4096 + 32 * 16 * 8    # 1024-assignment tiles
-    assert abi.moe_workspace_size(262144, 64, 8, 8) == 4096 + 256 * 64 * 8   # 8192-assignment tiles
+    assert abi.moe_workspace_size(16384, 16, 2, 4) == 8192 + 32 * 16 * 8    # 1024-assignment tiles
+    assert abi.moe_workspace_size(262144, 64, 8, 8) == 8192 + 256 * 64 * 8   # 8192-assignment tiles
     assert abi.moe_workspace_size(100, 16, 2, 3) == 0   # P does not divide E
     assert abi.moe_workspace_size(100, 300, 2, 4) == 0  # E too large
     assert abi.moe_rows_max(262144, 64, 8, 40960) == 2097152

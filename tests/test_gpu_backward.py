@@ -14,7 +14,7 @@ import torch
 
 import oracle
 from combine_moe_gate_warp_gb300 import workloads
-from gpu_util import bits, f_of_bits, run_gpu, sample_rows
+from gpu_util import bits, check_gate, check_layout, f_of_bits, run_gpu, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -36,33 +36,43 @@ def _gather(t, rows):
 
 
 def _check_backward(w, token_sample=None, seed=11):
+    """Forward on the GPU (gate compared, oracle gates swapped in, layout
+    compared), then the backward calls on seeded gradients; the oracle gets
+    its own layout and gates and the same seeded tensors."""
     rng = np.random.default_rng(seed)
     inp = workloads.make_inputs(w, "cuda")
-    plan, gates_pre, R, eo, status = run_gpu(w, inp)
+    plan, gates_pre, og, R, eo, status = run_gpu(w, inp)
     assert status == 0
+    check_gate(w, plan, gates_pre, og)
+    L = check_layout(w, plan, og)
     dy = workloads.make_dy(w, "cuda")
     dp = workloads.make_d_packed(w, max(R, 1), "cuda")
-    plan.backward(inp["logits"], dy, eo, dp)
+    dg_in = workloads.make_d_gates(w, "cuda")
+    plan.combine_backward(dy, eo)
+    plan.gate_backward(inp["logits"], dg_in)
+    plan.dispatch_backward(dp)
     assert plan.status() == 0, "device status after the backward"
     T, k, H, E = w.T, w.k, w.H, w.E
     if T == 0:
         return plan
     toks = np.arange(T, dtype=np.int64) if token_sample is None else sample_rows(T, rng, token_sample)
     n = toks.size
-    dst = plan.layout.dst_row.cpu().numpy()[:T * k].reshape(T, k)[toks]
+    dst = L["dst_row"].reshape(T, k)[toks]
     need = np.unique(dst[dst >= 0])
     remap = np.where(dst >= 0, np.searchsorted(need, np.maximum(dst, 0)), -1).astype(np.int32).ravel()
     dy_c = _gather(dy, toks)
-    g_c = plan.gates.cpu().numpy()[:T][toks]
+    g_c = L["gates"][toks]
+    eo_rows = _gather(eo, need) if not w.identity_experts else \
+        (oracle.dispatch_bf16_rows(bits(inp["x"]), k, L["src_pos"], need) if need.size else _gather(eo, need))
 
     # combine backward
-    d_eo_ref, dg_ref = oracle.combine_backward(dy_c, _gather(eo, need), g_c, remap, np.arange(n), k)
+    d_eo_ref, dg_ref = oracle.combine_backward(dy_c, eo_rows, g_c, remap, np.arange(n), k)
     got_rows = _gather(plan.d_expert_out, need)
     kept = dst.ravel() >= 0
     assert np.array_equal(got_rows[remap[kept]], d_eo_ref[kept]), "d_expert_out differs from the oracle"
     dg = plan.d_gates.cpu().numpy()[:T][toks]
     assert np.all(dg.ravel()[~kept] == 0.0), "dropped slots must get a zero gate gradient"
-    eo_c = f_of_bits(_gather(eo, need)).astype(np.float64)
+    eo_c = f_of_bits(eo_rows).astype(np.float64)
     dyf = f_of_bits(dy_c).astype(np.float64)
     mag = np.zeros(n * k)
     for i in np.flatnonzero(kept):
@@ -78,16 +88,17 @@ def _check_backward(w, token_sample=None, seed=11):
     none_kept = ~kept.reshape(n, k).any(1)
     assert not np.any(dx[none_kept]), "a token with no kept slot has dx = 0"
 
-    # gate backward, fed the GPU's fp32 d_gates
+    # gate backward on the seeded gate gradients
     logits = inp["logits"].cpu().numpy()[toks]
-    idx = plan.topk_idx.cpu().numpy()[:T][toks]
-    dl_ref = oracle.gate_backward(logits, idx, dg.astype(np.float64), w.mode)
+    idx = og[0][toks]
+    dgs = dg_in.cpu().numpy()[toks].astype(np.float64)
+    dl_ref = oracle.gate_backward(logits, idx, dgs, w.mode)
     dl = plan.d_logits.cpu().numpy()[:T][toks].astype(np.float64)
     l64 = logits.astype(np.float64)
     sel = np.zeros((n, E), bool)
     np.put_along_axis(sel, idx, True, 1)
     dsel = np.zeros((n, E))
-    np.put_along_axis(dsel, idx, np.abs(dg.astype(np.float64)), 1)
+    np.put_along_axis(dsel, idx, np.abs(dgs), 1)
     if w.mode == workloads.TOPK_SOFTMAX:
         lm = np.where(sel, l64, -np.inf)
         m = lm.max(1, keepdims=True)
@@ -99,7 +110,7 @@ def _check_backward(w, token_sample=None, seed=11):
         rng_l = np.abs(l64 - m).max(1, keepdims=True)
     p /= p.sum(1, keepdims=True)
     g_sel = np.take_along_axis(p, idx, 1)
-    S1 = np.sum(g_sel * np.abs(dg.astype(np.float64)), 1, keepdims=True)
+    S1 = np.sum(g_sel * np.abs(dgs), 1, keepdims=True)
     mag_l = p * dsel + p * S1
     c = 2.0 * (rng_l + E + k + 8) * 2.0 ** -24
     err = np.abs(dl - dl_ref)
@@ -152,7 +163,7 @@ def test_backward_edge_cases(w):
 def test_backward_is_deterministic():
     w = W["fine_shared"].scaled(500)
     inp = workloads.make_inputs(w, "cuda")
-    plan, _, R, eo, _ = run_gpu(w, inp)
+    plan, _, _, R, eo, _ = run_gpu(w, inp)
     dy = workloads.make_dy(w, "cuda")
     dp = workloads.make_d_packed(w, max(R, 1), "cuda")
     plan.backward(inp["logits"], dy, eo, dp)

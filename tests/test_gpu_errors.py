@@ -10,7 +10,7 @@ import torch
 
 import oracle
 from combine_moe_gate_warp_gb300 import RoutePlan, RouteShape, abi, workloads
-from gpu_util import check_gate, check_layout, shape_of
+from gpu_util import route_checked, shape_of
 
 pytestmark = pytest.mark.gpu
 
@@ -91,12 +91,7 @@ def test_out_of_range_ids_and_count_mismatch_reported():
     p.dispatch_layout()
     assert p.status() == abi.MOE_ERR_DEVICE_DATA
     # a clean call afterwards is exact again
-    p.gate(inp["logits"])
-    gpre = p.gates.clone()
-    p.dispatch_layout()
-    assert p.status() == 0
-    idx, _ = check_gate(w, p, gpre, inp["logits"].cpu().numpy())
-    check_layout(w, p, idx, gpre)
+    route_checked(w, p, inp["logits"])
 
 
 def test_lookback_wait_expires_with_timeout_status():
@@ -112,9 +107,4 @@ def test_lookback_wait_expires_with_timeout_status():
     p.dispatch_layout()
     assert p.status() == abi.MOE_ERR_TIMEOUT
     # the hook is cleared and the workspace usable again
-    p.gate(inp["logits"])
-    gpre = p.gates.clone()
-    p.dispatch_layout()
-    assert p.status() == 0
-    idx, _ = check_gate(w, p, gpre, inp["logits"].cpu().numpy())
-    check_layout(w, p, idx, gpre)
+    route_checked(w, p, inp["logits"])

@@ -13,7 +13,7 @@ import torch
 
 import oracle
 from combine_moe_gate_warp_gb300 import workloads
-from gpu_util import (bits, check_combine, check_dispatch, check_gate, check_layout, run_gpu,
+from gpu_util import (bits, check_combine, check_dispatch, check_gate, check_layout, route_checked, run_gpu,
                       sample_rows)
 
 pytestmark = pytest.mark.gpu
@@ -32,18 +32,17 @@ def _built():
 def _full_check(w, rows_sample=None, token_sample=None, seed=7):
     rng = np.random.default_rng(seed)
     inp = workloads.make_inputs(w, "cuda")
-    plan, gates_pre, R, eo, status = run_gpu(w, inp)
+    plan, gates_pre, og, R, eo, status = run_gpu(w, inp)
     assert status == 0, f"device status {status}"
-    logits = inp["logits"].cpu().numpy()
-    idx, counts = check_gate(w, plan, gates_pre, logits)
+    idx, counts = check_gate(w, plan, gates_pre, og)
     assert counts.sum() == w.T * w.k
-    L = check_layout(w, plan, idx, gates_pre)
+    L = check_layout(w, plan, og)
     assert L["R"] == R
     x_bits = bits(inp["x"])
     rows = np.arange(R, dtype=np.int64) if rows_sample is None else sample_rows(R, rng, rows_sample)
     check_dispatch(w, plan, L, x_bits, rows)
     toks = np.arange(w.T, dtype=np.int64) if token_sample is None else sample_rows(w.T, rng, token_sample)
-    frac = check_combine(w, plan, L, eo, inp["shared"], toks)
+    frac = check_combine(w, plan, L, eo, inp["shared"], toks, x_bits)
     return plan, L, frac
 
 
@@ -101,7 +100,7 @@ def test_edge_shapes(w):
 def test_empty_batch():
     w = _custom(0, 64, 8, 2, 4)
     inp = workloads.make_inputs(w, "cuda")
-    plan, gates_pre, R, eo, status = run_gpu(w, inp)
+    plan, gates_pre, og, R, eo, status = run_gpu(w, inp)
     assert status == 0 and R == 0
     assert plan.expert_counts.cpu().tolist() == [0] * 8
     assert plan.aux_loss.item() == 0.0 and plan.entropy.item() == 0.0
@@ -111,12 +110,12 @@ def test_empty_batch():
 
 def _run_with_logits(w, logits):
     inp = dict(logits=logits.contiguous(), x=workloads.make_x(w, "cuda"), shared=None)
-    plan, gates_pre, R, eo, status = run_gpu(w, inp)
+    plan, gates_pre, og, R, eo, status = run_gpu(w, inp)
     assert status == 0
-    idx, _ = check_gate(w, plan, gates_pre, inp["logits"].cpu().numpy())
-    L = check_layout(w, plan, idx, gates_pre)
+    check_gate(w, plan, gates_pre, og)
+    L = check_layout(w, plan, og)
     check_dispatch(w, plan, L, bits(inp["x"]), np.arange(R, dtype=np.int64))
-    check_combine(w, plan, L, eo, None, np.arange(w.T, dtype=np.int64))
+    check_combine(w, plan, L, eo, None, np.arange(w.T, dtype=np.int64), bits(inp["x"]))
     return plan, L
 
 
@@ -126,6 +125,17 @@ def test_ties_and_signed_zeros():
     logits = torch.randint(-2, 3, (w.T, w.E), generator=g, device="cuda").float()
     logits[torch.rand((w.T, w.E), generator=g, device="cuda") < 0.2] = -0.0
     _run_with_logits(w, logits)
+
+
+class _with_capacity:
+    """A workload view with an explicit capacity (the capacity property of
+    Workload is derived from its factor)."""
+
+    def __init__(self, w, cap):
+        self._w, self.capacity = w, cap
+
+    def __getattr__(self, name):
+        return getattr(self._w, name)
 
 
 def test_all_tokens_one_expert_capacity_hit_exactly_and_exceeded():
@@ -142,19 +152,14 @@ def test_all_tokens_one_expert_capacity_hit_exactly_and_exceeded():
         shp = shape_of(w)
         shp.capacity = cap
         plan = RoutePlan(shp, "cuda")
-        plan.gate(logits)
-        gpre = plan.gates.clone()
-        plan.dispatch_layout()
+        idx = oracle.gate(logits.cpu().numpy(), 2, 0)[0]
+        assert np.all(idx == [5, 2])
+        # the capacity lives in the plan's shape; the oracle gets the same value
+        wc = workloads.Workload("hot", T=1000, H=32, E=8, k=2, P=4, seed=3)
+        L = route_checked(_with_capacity(wc, cap), plan, logits)
         plan.dispatch(x)
         assert plan.status() == 0
-        idx = plan.topk_idx.cpu().numpy()
-        assert np.all(idx == [5, 2])
-        L = oracle.layout(idx, 8, 4, cap, gates_f32=gpre.cpu().numpy())
-        assert np.array_equal(plan.layout.dst_row.cpu().numpy(), L["dst_row"])
-        assert np.array_equal(plan.layout.src_pos.cpu().numpy()[:L["R"]], L["src_pos"])
-        assert np.array_equal(plan.layout.part_tokens.cpu().numpy(), L["part_tokens"])
         assert int(plan.layout.dropped.item()) == 2 * 1000 - 2 * min(cap, 1000)
-        wc = workloads.Workload("hot", T=1000, H=32, E=8, k=2, P=4, seed=3)
         check_dispatch(wc, plan, L, bits(x), np.arange(L["R"], dtype=np.int64))
 
 
@@ -168,10 +173,10 @@ def test_fp8_constant_and_signed_zero_rows():
     x[2] = -0.0                       # all -0: zero word is -0
     x[3, :] = 1.0
     x[3, 7] = -448.0                  # min hits -448 exactly
-    plan, gates_pre, R, eo, status = run_gpu(w, inp)
+    plan, gates_pre, og, R, eo, status = run_gpu(w, inp)
     assert status == 0
-    idx, _ = check_gate(w, plan, gates_pre, inp["logits"].cpu().numpy())
-    L = check_layout(w, plan, idx, gates_pre)
+    check_gate(w, plan, gates_pre, og)
+    L = check_layout(w, plan, og)
     check_dispatch(w, plan, L, bits(x), np.arange(R, dtype=np.int64))
 
 
@@ -209,9 +214,10 @@ def test_fp8_bf16_pattern_sweep():
     w = _custom(T, H, 8, 1, 1, fp8=True)
     x = torch.from_numpy(rows.view(np.int16)).cuda().view(torch.bfloat16)
     inp = dict(logits=workloads.make_logits(w, "cuda"), x=x, shared=None)
-    plan, gates_pre, R, eo, status = run_gpu(w, inp)
+    plan, gates_pre, og, R, eo, status = run_gpu(w, inp)
     assert status == 0 and R == T
-    L = oracle.layout(plan.topk_idx.cpu().numpy(), 8, 1, 0)
+    check_gate(w, plan, gates_pre, og)
+    L = check_layout(w, plan, og)
     check_dispatch(w, plan, L, rows, np.arange(R, dtype=np.int64))
 
 
@@ -225,10 +231,6 @@ def test_repeated_calls_reuse_workspace():
     for rep in range(3):
         wr = workloads.Workload(**{**w.__dict__, "seed": 500 + rep})
         inp = workloads.make_inputs(wr, "cuda")
-        plan.gate(inp["logits"])
-        gpre = plan.gates.clone()
-        plan.dispatch_layout()
+        route_checked(wr, plan, inp["logits"])
         plan.dispatch(inp["x"])
         assert plan.status() == 0
-        idx, _ = check_gate(wr, plan, gpre, inp["logits"].cpu().numpy())
-        check_layout(wr, plan, idx, gpre)
