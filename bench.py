@@ -156,23 +156,35 @@ class ClockSampler:
 # byte accounting of the roofline (algorithmic bytes, not measured traffic)
 # ---------------------------------------------------------------------------
 def kernel_bytes(w, R):
+    """Algorithmic bytes per call of the step (and of the whole step)."""
     bt = 1 if w.fp8 else 2
     x = w.T * w.H * 2
+    grouped = int(w.fp8) in (2, 3)
+    # grouped FP8 modes read x once more for the group extremes
     packed = R * w.H * bt + (R * 8 if w.fp8 else 0)
-    eo = R * w.H * 2
     y = w.T * w.H * 2
     shared = w.Ks * w.T * w.H * 2
-    return {
+    by = {
         "gate": w.T * w.E * 4 + w.T * w.k * 8 + w.E * 4,
         "layout": w.T * w.k * (4 + 4 + 1 + 4) + R * 4,
-        "dispatch": x + packed,
-        "combine": eo + y + shared + w.T * w.k * 8,
-        "roofline_step": x + R * w.H * bt + eo + y,  # x read, packed written, eo read, y written
-        # every byte the step moves: the roofline bytes plus logits, shared
-        # experts, FP8 scales and the routing metadata
-        "all_step": (x + R * w.H * bt + eo + y + w.T * w.E * 4 + shared + (R * 8 if w.fp8 else 0)
-                     + w.T * w.k * (4 + 4) + w.T * w.k * (4 + 4 + 1 + 4) + w.T * w.k * 8),
+        "dispatch": x * (2 if grouped else 1) + packed,
     }
+    if w.fp8_combine:
+        # expert side: bf16 rows read (twice for grouped modes), codes and scales written;
+        # combine: codes and scales read
+        qgrouped = int(w.fp8_combine) in (2, 3)
+        by["quantize"] = R * w.H * 2 * (2 if qgrouped else 1) + R * (w.H + 8)
+        by["combine"] = R * (w.H + 8) + y + shared + w.T * w.k * 8
+        eo_metric = R * w.H * 2 + R * w.H + R * w.H  # bf16 read, codes written, codes read
+    else:
+        by["combine"] = R * w.H * 2 + y + shared + w.T * w.k * 8
+        eo_metric = R * w.H * 2
+    # the metric's bytes: x read, packed written, expert outputs read (for FP8
+    # expert outputs: read in bf16, codes written and read), y written
+    by["roofline_step"] = x + R * w.H * bt + eo_metric + y
+    # every byte the step moves
+    by["all_step"] = sum(v for k2, v in by.items() if k2 not in ("roofline_step",))
+    return by
 
 
 KERNEL_SOURCES = {"dispatch": ("dispatch.cu",), "combine": ("combine.cu",), "gate": ("gate.cu",),
@@ -231,15 +243,24 @@ def oracle_sample_run(w, inputs_host, T_s):
     idx, g64, counts, aux, ent = oracle.gate(logits, w.k, w.mode)
     L = oracle.layout(idx, w.E, w.P, cap, gates_f32=g64.astype(np.float32))
     rows = np.arange(L["R"], dtype=np.int64)
-    if w.fp8:
+    src_row = L["src_pos"].astype(np.int64) // w.k
+    if int(w.fp8) == 1:
         packed, scales = oracle.dispatch_fp8_rows(x_bits, w.k, L["src_pos"], rows)
+    elif w.fp8:
+        group, ng = oracle.row_groups(int(w.fp8), L["offsets"], rows)
+        packed, scales = oracle.quantize_rows_grouped(x_bits, src_row, group, ng)
     else:
         packed = oracle.dispatch_bf16_rows(x_bits, w.k, L["src_pos"], rows)
     t1 = time.perf_counter()
     eo = packed if w.identity_experts else inputs_host["eo"][:max(L["R"], 1)]
     sh = None if inputs_host.get("shared") is None else np.ascontiguousarray(inputs_host["shared"][:, :T_s])
     t2 = time.perf_counter()
-    oracle.combine_f32order(eo, L["gates"], L["dst_row"], np.arange(T_s), T_s, w.k, sh)
+    if w.fp8_combine:
+        group, ng = oracle.row_groups(int(w.fp8_combine), L["offsets"], rows)
+        codes, sc = oracle.quantize_rows_grouped(eo, rows, group, ng)
+        oracle.combine_fp8_f32order(codes, sc, L["gates"], L["dst_row"], np.arange(T_s), T_s, w.k, sh)
+    else:
+        oracle.combine_f32order(eo, L["gates"], L["dst_row"], np.arange(T_s), T_s, w.k, sh)
     t3 = time.perf_counter()
     return (t1 - t0) + (t3 - t2)
 
@@ -293,10 +314,12 @@ def rank_workload(base, rank: int):
 def config_of(w, world):
     return {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "P": w.P,
             "gate": "softmax_topk" if w.mode else "topk_softmax",
-            "transport": "e4m3" if w.fp8 else "bf16", "Ks": w.Ks,
+            "transport": (["bf16", "e4m3 per-token", "e4m3 per-expert", "e4m3 global"][int(w.fp8)]),
+            "expert_outputs": (["bf16", "e4m3 per-token", "e4m3 per-expert", "e4m3 global"][int(w.fp8_combine)]),
+            "Ks": w.Ks,
             "capacity": w.capacity or None,
             "l2": "no flush: each step touches ~%.2f GB, far above the 126 MB L2" % (
-                (w.T * w.H * 2 * 2 + 2 * w.T * w.k * w.H * (1 if w.fp8 else 2)) / 1e9),
+                (w.T * w.H * 2 * 2 + w.T * w.k * w.H * ((1 if w.fp8 else 2) + (1 if w.fp8_combine else 2))) / 1e9),
             "parallelism": f"dp{world}"}
 
 
@@ -361,8 +384,8 @@ def run_ours(args):
     w = rank_workload(base, rank)
 
     inputs = workloads.make_inputs(w, dev)
-    shape = RouteShape(T=w.T, H=w.H, E=w.E, k=w.k, P=w.P, mode=w.mode, fp8=w.fp8, Ks=w.Ks,
-                       capacity=w.capacity)
+    shape = RouteShape(T=w.T, H=w.H, E=w.E, k=w.k, P=w.P, mode=w.mode, fp8=int(w.fp8), Ks=w.Ks,
+                       capacity=w.capacity, fp8_combine=int(w.fp8_combine))
     plan = RoutePlan(shape, dev)
     eo = None if w.identity_experts else workloads.make_expert_out(w, max(plan.r_max, 1), dev)
     stream = torch.cuda.current_stream(dev)
@@ -388,11 +411,19 @@ def run_ours(args):
     time.sleep(0.3 if sampler else 0)
 
     K = args.steps
-    EV = 8  # per-kernel CUDA events on every EV-th step (events between kernels cost ~10 us/step)
+    EV = 8  # per-call CUDA events on every EV-th step (events between kernels cost ~10 us/step)
     sampled = list(range(0, K, EV))
-    ev = {i: [torch.cuda.Event(enable_timing=True) for _ in range(5)] for i in sampled}
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     eo_arg = plan.packed if eo is None else eo
+    calls = [("gate", lambda: plan.gate(inputs["logits"])), ("layout", plan.dispatch_layout),
+             ("dispatch", lambda: plan.dispatch(inputs["x"]))]
+    if w.fp8_combine:
+        calls += [("quantize", lambda: plan.quantize_expert_out(eo_arg)),
+                  ("combine", lambda: plan.combine_fp8(inputs["shared"]))]
+    else:
+        calls += [("combine", lambda: plan.combine(eo_arg, inputs["shared"]))]
+    names = [c[0] for c in calls]
+    ev = {i: [torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for i in sampled}
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize(dev)
     t_wall0 = time.time()
@@ -403,14 +434,9 @@ def run_ours(args):
             plan.step(inputs["logits"], inputs["x"], eo_arg, inputs["shared"])
             continue
         e[0].record(stream)
-        plan.gate(inputs["logits"])
-        e[1].record(stream)
-        plan.dispatch_layout()
-        e[2].record(stream)
-        plan.dispatch(inputs["x"])
-        e[3].record(stream)
-        plan.combine(eo_arg, inputs["shared"])
-        e[4].record(stream)
+        for j, (_, fn) in enumerate(calls):
+            fn()
+            e[j + 1].record(stream)
     stop.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
@@ -423,9 +449,9 @@ def run_ours(args):
     if sampler:
         time.sleep(0.25)
         sampler.stop()
-    names = ["gate", "layout", "dispatch", "combine"]
     per = {n: statistics.fmean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in sampled)
            for j, n in enumerate(names)}
+    step_samples = sorted(ev[i][0].elapsed_time(ev[i][len(calls)]) for i in sampled)
     by = kernel_bytes(w, R)
     peak, peak_kind = hbm_peak()
     dom = max(("dispatch", "combine"), key=lambda n: per[n])
@@ -504,7 +530,9 @@ def run_ours(args):
             "kernels_ms": per,
             "kernels_sampled_steps": len(sampled),
             "kernels_gbs": {n: by[n] / (per[n] * 1e-3) / 1e9 for n in names},
-            "gpu_launches": 4 * K,
+            "step_ms_evented": {"median": statistics.median(step_samples), "min": step_samples[0],
+                                "note": "sampled steps with events between the calls"},
+            "gpu_launches": plan.launches_per_step() * K,
             "clocks": clocks,
             "e2e": e2e,
             "cpu_baseline": cpu,

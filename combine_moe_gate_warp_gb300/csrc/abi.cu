@@ -144,7 +144,6 @@ moe_status moe_dispatch(const void *x, int T, int H, const moe_layout *L, int fp
     if (T > 0 && (!x || !packed || (fp8 && !scales))) return MOE_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(packed) || !aligned16(scales)) return MOE_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (fp8 == MOE_FP8_PER_TOKEN) return from_cuda(moe::launch_dispatch_fp8(x, T, H, L, packed, scales, s));
     if (fp8 != 0) return from_cuda(moe::launch_dispatch_fp8_grouped(x, T, H, L, fp8, packed, scales, s));
     return from_cuda(moe::launch_dispatch_bf16(x, T, H, L, packed, s));
 }

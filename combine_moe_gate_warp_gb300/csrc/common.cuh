@@ -143,8 +143,6 @@ cudaError_t launch_layout(const int32_t *topk_idx, const int32_t *counts_in, int
                           cudaStream_t s);
 cudaError_t launch_dispatch_bf16(const void *x, int T, int H, const moe_layout *L, void *packed,
                                  cudaStream_t s);
-cudaError_t launch_dispatch_fp8(const void *x, int T, int H, const moe_layout *L, void *packed,
-                                float *scales, cudaStream_t s);
 cudaError_t launch_combine(const void *eo, const moe_layout *L, const float *gates,
                            const void *shared, int Ks, int T, int H, void *y, cudaStream_t s);
 cudaError_t launch_dispatch_fp8_grouped(const void *x, int T, int H, const moe_layout *L, int mode, void *packed,

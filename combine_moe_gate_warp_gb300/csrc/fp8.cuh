@@ -3,6 +3,7 @@
 // encode of a bf16 pair, and the decode of 16 codes.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
@@ -34,23 +35,78 @@ __device__ __forceinline__ unsigned short e4m3x2(float lo, float hi)
     return (unsigned short)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
 }
 
-// Quantise one bf16 pair word into two codes (low code = low element).
-__device__ __forceinline__ unsigned quant_pair(unsigned w, float zero, float scale)
+// The quotient q = RN((v - zero) / scale) decides the code, and the code
+// must be the one the correctly rounded quotient gives.  Division is the
+// costliest step of the encode, so the quotients are formed as
+// q = RN(d * RN(1/scale)), which is within 4 fp32 ulp (relative 2^-21) of
+// RN(d / scale): two roundings of at most half an ulp each.  The codes of
+// q * (1 - 2^-20) and q * (1 + 2^-20) bracket the code of RN(d / scale),
+// because the e4m3 conversion is monotone; where the two agree, that is the
+// code, and only where they differ (q next to an e4m3 rounding boundary) is
+// the correctly rounded __fdiv_rn taken.  This is Ziv's rounding test
+// ("Fast evaluation of elementary mathematical functions with correctly
+// rounded last bit", ACM TOMS 17(3), 1991): an approximation plus an exact
+// fallback when the rounding is in doubt.  The arithmetic runs on packed
+// fp32 pairs (__fadd2_rn / __fmul2_rn), the test over 8 values at once,
+// and the fallback recomputes all 8 (a branch too long to be if-converted:
+// free when no lane needs it).  rcp = 0 forces the fallback.
+
+// 1 / scale for the fast quotient, or 0 (always fall back) where the
+// reciprocal would leave the normal range.
+__device__ __forceinline__ float e4m3_rcp(float scale)
 {
-    const float a = __fdiv_rn(__fsub_rn(bf16lo(w), zero), scale);
-    const float b = __fdiv_rn(__fsub_rn(bf16hi(w), zero), scale);
-    return (unsigned)e4m3x2(a, b);
+    return scale >= 1e-30f ? __frcp_rn(scale) : 0.0f;
+}
+
+// 8 bf16 (one 16-byte vector) -> 8 codes (two words), code i from element
+// i (low bytes first).
+__device__ __forceinline__ uint2 quant8(const uint4 &a, float zero, float scale, float rcp)
+{
+    const unsigned w[4] = {a.x, a.y, a.z, a.w};
+    const float2 nz = make_float2(-zero, -zero), r2 = make_float2(rcp, rcp);
+    const float2 dn = make_float2(1.0f - 0x1p-20f, 1.0f - 0x1p-20f), up = make_float2(1.0f + 0x1p-20f, 1.0f + 0x1p-20f);
+    unsigned lo[2], hi[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float2 q0 = __fmul2_rn(__fadd2_rn(make_float2(bf16lo(w[2 * i]), bf16hi(w[2 * i])), nz), r2);
+        const float2 q1 = __fmul2_rn(__fadd2_rn(make_float2(bf16lo(w[2 * i + 1]), bf16hi(w[2 * i + 1])), nz), r2);
+        const float2 l0 = __fmul2_rn(q0, dn), h0 = __fmul2_rn(q0, up);
+        const float2 l1 = __fmul2_rn(q1, dn), h1 = __fmul2_rn(q1, up);
+        lo[i] = (unsigned)e4m3x2(l0.x, l0.y) | ((unsigned)e4m3x2(l1.x, l1.y) << 16);
+        hi[i] = (unsigned)e4m3x2(h0.x, h0.y) | ((unsigned)e4m3x2(h1.x, h1.y) << 16);
+    }
+    if (__builtin_expect((lo[0] != hi[0]) | (lo[1] != hi[1]) | (rcp == 0.0f), 0)) {
+        float q[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            q[2 * i] = __fdiv_rn(__fsub_rn(bf16lo(w[i]), zero), scale);
+            q[2 * i + 1] = __fdiv_rn(__fsub_rn(bf16hi(w[i]), zero), scale);
+        }
+        lo[0] = (unsigned)e4m3x2(q[0], q[1]) | ((unsigned)e4m3x2(q[2], q[3]) << 16);
+        lo[1] = (unsigned)e4m3x2(q[4], q[5]) | ((unsigned)e4m3x2(q[6], q[7]) << 16);
+    }
+    return make_uint2(lo[0], lo[1]);
 }
 
 // 16 bf16 (two 16-byte vectors) -> 16 codes (one 16-byte vector).
-__device__ __forceinline__ uint4 quant16(const uint4 &a, const uint4 &b, float zero, float scale)
+__device__ __forceinline__ uint4 quant16(const uint4 &a, const uint4 &b, float zero, float scale, float rcp)
 {
-    uint4 c;
-    c.x = quant_pair(a.x, zero, scale) | (quant_pair(a.y, zero, scale) << 16);
-    c.y = quant_pair(a.z, zero, scale) | (quant_pair(a.w, zero, scale) << 16);
-    c.z = quant_pair(b.x, zero, scale) | (quant_pair(b.y, zero, scale) << 16);
-    c.w = quant_pair(b.z, zero, scale) | (quant_pair(b.w, zero, scale) << 16);
-    return c;
+    const uint2 l = quant8(a, zero, scale, rcp), h = quant8(b, zero, scale, rcp);
+    return make_uint4(l.x, l.y, h.x, h.y);
+}
+
+// Running max and min of bf16 pairs (packed, two lanes per word).  Signed
+// zeros are not ordered here; a caller whose extreme comes out as zero
+// recomputes it with the ordered keys below.
+__device__ __forceinline__ void hminmax8(const uint4 &a, __nv_bfloat162 &mx, __nv_bfloat162 &mn)
+{
+    const unsigned w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(&w[i]);
+        mx = __hmax2(mx, v);
+        mn = __hmin2(mn, v);
+    }
 }
 
 // Max and min keys of the 16 bf16 values of two 16-byte vectors.

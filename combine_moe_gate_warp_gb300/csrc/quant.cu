@@ -20,15 +20,18 @@
 //      group in shared memory (shared atomicMax on monotone key words) and
 //      merged into the workspace with one global atomicMax per (block,
 //      group): the global mode does not serialise on one address.
-//   2. fp8_group_encode_kernel: one block per source row; every block turns
-//      the workspace keys into the groups' (scale, zero) in shared memory
-//      first, then encodes its row with the pinned fp32 operations and the
-//      hardware e4m3x2 satfinite conversion; a completion ticket lets the
-//      last block reset the keys, so the workspace stays zeroed.
-// The dispatch side reads token rows of x and writes each kept copy (a
-// token sent to two experts is encoded once per expert in the per-expert
-// mode, once in total in the global mode); the expert side reads packed
-// expert-output rows and writes the same rows.
+//   2. fp8_encode_kernel: blocks walk the rows, every block first turning
+//      the workspace keys into the groups' (scale, zero) in shared memory;
+//      a completion ticket lets the last block reset the keys, so the
+//      workspace stays zeroed.
+// The per-token mode is the encode pass alone, with the row's extremes
+// reduced inside the block.  The encode does the pinned fp32 operations on
+// packed pairs with a rounding test that makes every code the one of the
+// correctly rounded division (fp8.cuh), and the hardware e4m3x2 satfinite
+// conversion.  The dispatch side reads token rows of x and writes each
+// kept copy (a token sent to two experts is encoded once per expert in the
+// per-expert mode, once in total in the other modes); the expert side reads
+// packed expert-output rows and writes the same rows.
 //
 // FP8 combine: per token y = bf16 RNE of, in fp32 and this order,
 //   acc = 0; acc = fmaf(g_j, fmaf(scale_r, e4m3(code), zero_r), acc) over kept
@@ -43,12 +46,12 @@
 
 #include "common.cuh"
 #include "fp8.cuh"
+#include "tma.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kStatThreads = 256;
-constexpr int kEncThreads = 128;
 
 // Expert of packed row `row` from the layout offsets held in shared memory:
 // the largest e with off[e] <= row (experts without rows are skipped).
@@ -129,132 +132,222 @@ fp8_group_stats_kernel(const uint4 *__restrict__ src, long long n_src, int nvec,
     }
 }
 
-// One block per source row.  Thread c handles 16-column groups c, c+128, ...
-// (CPT of them: 32 bytes of bf16 in, 16 codes out each).
-template <int CPT, int MODE, bool TOKENS>
-__global__ void __launch_bounds__(kEncThreads)
-fp8_group_encode_kernel(const uint4 *__restrict__ src, long long n_src, int npairs, int k,
-                        const int32_t *__restrict__ dst_row, const int32_t *__restrict__ offsets, int E, int r_max,
-                        uint4 *__restrict__ packed, float2 *__restrict__ scales, void *ws)
+// ---- encode pass ------------------------------------------------------------
+// Warp-specialised and TMA-staged, like the combine: a producer warp keeps
+// a ring of `stages` source rows in flight in shared memory (one 1-D bulk
+// copy per row, completing on the stage's "full" mbarrier), and eight
+// consumer warps each take every eighth row of the block: a warp reads its
+// row from shared memory, reduces the extremes with shuffles alone (per-
+// token mode; packed bf16 max/min, a zero extreme recomputed with the
+// ordered integer keys, which rank -0 below +0), encodes each run of
+// destinations with one group once (packed fp32 arithmetic with the
+// rounding test of fp8.cuh), stores the codes with 16-byte stores and
+// releases the stage on its "empty" mbarrier.  No block-wide barrier sits
+// in the loop: the rows in flight per SM are set by shared memory and the
+// rows being encoded by the consumer warps.  Every wait is bounded; on
+// expiry MOE_ERR_TIMEOUT is recorded, the block stops, and the producer
+// waits (bounded) for the copies it issued before the block exits.
+constexpr int kEncMaxConsumers = 8;
+constexpr int kEncMaxThreads = 32 * (kEncMaxConsumers + 1);
+constexpr int kEncRingBytes = 112 * 1024;  // per block at most
+constexpr int kEncMaxStages = 16;
+
+struct EncArgs {
+    const unsigned char *src;  // [n_src, H] bf16
+    long long n_src;           // T (tokens) or r_max (rows; R on the device bounds it)
+    int rowbytes;              // 2H
+    int npairs;                // H / 16
+    int k;
+    const int32_t *dst_row;
+    const int32_t *offsets;
+    int E;
+    int r_max;
+    uint4 *out;                // [r_max, H / 16] codes
+    float2 *scales;            // [r_max]
+    void *ws;
+    int stages;     // a multiple of `consumers`: stage st is always read by consumer warp st % consumers
+    int consumers;  // consumer warps (block = consumers + 1 warps)
+};
+
+__device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity)
 {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_timer_ns() - t0 > kSpinLimitNs) return false;
+    return true;
+}
+
+template <int MODE, bool TOKENS>
+__global__ void __launch_bounds__(kEncMaxThreads)
+fp8_encode_kernel(EncArgs a)
+{
+    extern __shared__ __align__(128) unsigned char s_ring[];
+    __shared__ uint64_t s_full[kEncMaxStages], s_empty[kEncMaxStages];
     __shared__ int s_off[MOE_MAX_EXPERTS + 1];
     __shared__ float2 s_par[MOE_MAX_EXPERTS];
-    __shared__ int s_rows[MOE_MAX_TOPK];
-    __shared__ int s_grp[MOE_MAX_TOPK];
-    __shared__ int s_n;
-    __shared__ int s_wmax[kEncThreads / 32], s_wmin[kEncThreads / 32];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int ngroups = MODE == MOE_FP8_GLOBAL ? 1 : (MODE == MOE_FP8_PER_EXPERT ? E : 0);
-    WsHeader *h = static_cast<WsHeader *>(ws);
+    __shared__ volatile int s_abort;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int ngroups = MODE == MOE_FP8_GLOBAL ? 1 : (MODE == MOE_FP8_PER_EXPERT ? a.E : 0);
+    WsHeader *h = static_cast<WsHeader *>(a.ws);
+    if (tid == 0) {
+        for (int st = 0; st < a.stages; ++st) {
+            mbar_init(&s_full[st], 1);
+            mbar_init(&s_empty[st], 1);
+        }
+        mbar_fence_init();
+        s_abort = 0;
+    }
     pdl_wait();
     pdl_launch_dependents();
-    for (int i = threadIdx.x; i <= E; i += kEncThreads) s_off[i] = __ldg(offsets + i);
-    for (int g = threadIdx.x; g < ngroups; g += kEncThreads) {
+    for (int i = tid; i <= a.E; i += blockDim.x) s_off[i] = __ldg(a.offsets + i);
+    for (int g = tid; g < ngroups; g += blockDim.x) {
         const unsigned wmx = *((volatile unsigned *)&h->quant_max[g]);
         const unsigned wmn = *((volatile unsigned *)&h->quant_min[g]);
         s_par[g] = wmx == 0u ? make_float2(0.0f, 0.0f) : affine_pair(key_of_max_word(wmx), key_of_min_word(wmn));
     }
     __syncthreads();
-    const int rows_valid = min(r_max, s_off[E]);
-    for (long long i = blockIdx.x; i < n_src; i += gridDim.x) {
-        // destination rows of this source row, compacted in slot order
-        if (threadIdx.x < 32) {
+    const int rows_valid = min(a.r_max, s_off[a.E]);
+    const long long n_src = TOKENS ? a.n_src : min(a.n_src, (long long)rows_valid);
+    const long long stride = gridDim.x;
+    const long long n_mine = n_src > blockIdx.x ? (n_src - blockIdx.x + stride - 1) / stride : 0;
+
+    if (warp == 0) {
+        // ---- producer: lane 0 keeps the ring full ---------------------------
+        if (lane == 0) {
+            long long i = 0;
+            for (; i < n_mine && !s_abort; ++i) {
+                const int st = (int)(i % a.stages);
+                if (i >= a.stages && !wait_phase(&s_empty[st], (uint32_t)(((i / a.stages) - 1) & 1))) {
+                    record_status(a.ws, MOE_ERR_TIMEOUT);
+                    s_abort = 1;
+                    break;
+                }
+                const long long r = blockIdx.x + i * stride;
+                mbar_arrive_expect_tx(&s_full[st], (uint32_t)a.rowbytes);
+                bulk_load(s_ring + (size_t)st * a.rowbytes, a.src + r * a.rowbytes, (uint32_t)a.rowbytes,
+                          &s_full[st]);
+            }
+            // never leave with copies still landing in shared memory: wait for
+            // the last copy issued into each stage
+            const long long first = i > a.stages ? i - a.stages : 0;
+            for (long long q = first; q < i; ++q)
+                wait_phase(&s_full[q % a.stages], (uint32_t)((q / a.stages) & 1));
+        }
+    } else {
+        // ---- consumers: warp c takes rows c-1, c-1+C, ... (C consumer warps).
+        // stages is a multiple of C, so every stage is read by one warp only,
+        // in order: a warp never waits on a phase two ahead of the last one it
+        // consumed there (the parity wait cannot alias).
+        for (long long i = warp - 1; i < n_mine; i += a.consumers) {
+            if (__any_sync(0xffffffffu, s_abort != 0)) break;  // the warp leaves together
+            const int st = (int)(i % a.stages);
+            const long long r_src = blockIdx.x + i * stride;
+            // destinations: lane j < k holds slot j's row (tokens), lane 0 the row itself
             int r = -1;
             if (TOKENS) {
-                if ((int)threadIdx.x < k) {
-                    r = __ldg(dst_row + i * k + threadIdx.x);
+                if (lane < a.k) {
+                    r = __ldg(a.dst_row + r_src * a.k + lane);
                     if (r >= rows_valid) {
-                        record_status(ws, MOE_ERR_DEVICE_DATA);
+                        record_status(a.ws, MOE_ERR_DEVICE_DATA);
                         r = -1;
                     }
                 }
-            } else if (threadIdx.x == 0 && i < rows_valid) {
-                r = (int)i;
+            } else if (lane == 0) {
+                r = (int)r_src;
             }
             const unsigned kept = __ballot_sync(0xffffffffu, r >= 0);
-            if (r >= 0) {
-                const int pos = __popc(kept & ((1u << threadIdx.x) - 1u));
-                s_rows[pos] = r;
-                s_grp[pos] = MODE == MOE_FP8_PER_EXPERT ? expert_of_row(s_off, E, r) : 0;
+            const int grp_mine = (r >= 0 && MODE == MOE_FP8_PER_EXPERT) ? expert_of_row(s_off, a.E, r) : 0;
+            // every lane waits (the wait makes the copy visible to it); the
+            // warp leaves together if any lane's bounded wait expired
+            const bool landed = wait_phase(&s_full[st], (uint32_t)((i / a.stages) & 1));
+            if (!__all_sync(0xffffffffu, landed)) {
+                if (lane == 0) record_status(a.ws, MOE_ERR_TIMEOUT);
+                s_abort = 1;
+                break;
             }
-            if (threadIdx.x == 0) s_n = __popc(kept);
-        }
-        __syncthreads();
-        const int n = s_n;
-        if (n > 0) {
-            const uint4 *row = src + i * (2LL * npairs);
-            uint4 v[CPT][2];
-#pragma unroll
-            for (int u = 0; u < CPT; ++u) {
-                const int p = u * kEncThreads + threadIdx.x;
-                if (p < npairs) {
-                    v[u][0] = ld_stream_v4(row + 2 * p);
-                    v[u][1] = ld_stream_v4(row + 2 * p + 1);
+            const unsigned char *row = s_ring + (size_t)st * a.rowbytes;
+            float2 par_tok = make_float2(0.0f, 0.0f);
+            if (MODE == MOE_FP8_PER_TOKEN && kept != 0u) {
+                __nv_bfloat162 mx2 = __float2bfloat162_rn(-INFINITY), mn2 = __float2bfloat162_rn(INFINITY);
+                for (int q = lane; q < a.npairs; q += 32) {
+                    hminmax8(lds_v4(row + 32 * q), mx2, mn2);
+                    hminmax8(lds_v4(row + 32 * q + 16), mx2, mn2);
                 }
-            }
-            if (MODE == MOE_FP8_PER_TOKEN) {
-                // the row is its own group: block-wide extremes first
-                int kmax = INT_MIN, kmin = INT_MAX;
-#pragma unroll
-                for (int u = 0; u < CPT; ++u)
-                    if (u * kEncThreads + (int)threadIdx.x < npairs) minmax16(v[u][0], v[u][1], kmax, kmin);
+                float mx = fmaxf(__low2float(mx2), __high2float(mx2));
+                float mn = fminf(__low2float(mn2), __high2float(mn2));
 #pragma unroll
                 for (int d = 16; d > 0; d >>= 1) {
-                    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, d));
-                    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, d));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, d));
+                    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, d));
                 }
-                if (lane == 0) {
-                    s_wmax[warp] = kmax;
-                    s_wmin[warp] = kmin;
-                }
-                __syncthreads();
-                if (threadIdx.x == 0) {
-                    int a = s_wmax[0], b = s_wmin[0];
-                    for (int w = 1; w < kEncThreads / 32; ++w) {
-                        a = max(a, s_wmax[w]);
-                        b = min(b, s_wmin[w]);
-                    }
-                    s_par[0] = affine_pair(a, b);
-                }
-                __syncthreads();
-            }
-            // rows of one group share their codes: encode once per run of
-            // equal groups (slot order), store to every row of the run
-            for (int j0 = 0; j0 < n;) {
-                const int g = s_grp[j0];
-                int j1 = j0 + 1;
-                while (j1 < n && s_grp[j1] == g) ++j1;
-                const float2 par = s_par[g];
+                int kmax = f32_order_key(__float_as_uint(mx)), kmin = f32_order_key(__float_as_uint(mn));
+                if (mx == 0.0f || mn == 0.0f) {
+                    // a zero extreme: its sign needs the ordered keys (-0 < +0)
+                    kmax = INT_MIN;
+                    kmin = INT_MAX;
+                    for (int q = lane; q < a.npairs; q += 32)
+                        minmax16(lds_v4(row + 32 * q), lds_v4(row + 32 * q + 16), kmax, kmin);
 #pragma unroll
-                for (int u = 0; u < CPT; ++u) {
-                    const int p = u * kEncThreads + threadIdx.x;
-                    if (p < npairs) {
-                        const uint4 c = par.x == 0.0f ? make_uint4(0u, 0u, 0u, 0u)
-                                                      : quant16(v[u][0], v[u][1], par.y, par.x);
-                        for (int j = j0; j < j1; ++j) st_v4(packed + (long long)s_rows[j] * npairs + p, c);
+                    for (int d = 16; d > 0; d >>= 1) {
+                        kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, d));
+                        kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, d));
                     }
                 }
-                if ((int)threadIdx.x >= j0 && (int)threadIdx.x < j1) scales[s_rows[threadIdx.x]] = par;
-                j0 = j1;
+                par_tok = affine_pair(kmax, kmin);
             }
+            // runs of destinations with one group share their codes (slot order)
+            unsigned rest = kept;
+            while (rest) {
+                const int j0 = __ffs(rest) - 1;
+                const int g = __shfl_sync(0xffffffffu, grp_mine, j0);
+                const unsigned same = __ballot_sync(0xffffffffu, (rest >> lane) & 1u && grp_mine == g);
+                rest &= ~same;
+                const float2 par = MODE == MOE_FP8_PER_TOKEN ? par_tok : s_par[g];
+                const float rcp = e4m3_rcp(par.x);
+                // the run's rows, gathered by every lane before the column loop
+                // (whose trip count differs between lanes: no warp collective in it)
+                int run[MOE_MAX_TOPK];
+                const int nr = __popc(same);
+                unsigned m = same;
+#pragma unroll
+                for (int j = 0; j < MOE_MAX_TOPK; ++j) {
+                    run[j] = __shfl_sync(0xffffffffu, r, m ? __ffs(m) - 1 : 0);
+                    m &= m - 1u;
+                }
+                for (int q = lane; q < a.npairs; q += 32) {
+                    const uint4 c = par.x == 0.0f
+                                        ? make_uint4(0u, 0u, 0u, 0u)
+                                        : quant16(lds_v4(row + 32 * q), lds_v4(row + 32 * q + 16), par.y, par.x, rcp);
+#pragma unroll
+                    for (int j = 0; j < MOE_MAX_TOPK; ++j)
+                        if (j < nr) st_v4(a.out + (long long)run[j] * a.npairs + q, c);
+                }
+                if ((same >> lane) & 1u) a.scales[r] = par;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_empty[st]);
         }
-        __syncthreads();  // s_rows / s_par[0] are rewritten for the next row
     }
+    // After the role split no block-wide barrier is used (the producer's
+    // lane 0 leaves its loop long after the other lanes): completion is
+    // counted per warp, each warp reconverged first.
+    __syncwarp();
     if (MODE != MOE_FP8_PER_TOKEN) {
-        // the last block to finish resets the group keys (every block read
-        // them at its start, before its ticket)
-        if (threadIdx.x == 0) {
+        // the last warp to finish resets the group keys (every block read
+        // them before its role split, so before any of its warps' tickets)
+        unsigned last = 0;
+        if (lane == 0) {
             __threadfence();
             const unsigned done = atomicAdd(&h->quant_ticket, 1u);
-            s_n = (done == gridDim.x - 1) ? 1 : 0;
+            last = (done == gridDim.x * (blockDim.x / 32) - 1) ? 1u : 0u;
         }
-        __syncthreads();
-        if (s_n) {
-            for (int g = threadIdx.x; g < ngroups; g += kEncThreads) {
+        if (__shfl_sync(0xffffffffu, last, 0)) {
+            for (int g = lane; g < ngroups; g += 32) {
                 h->quant_max[g] = 0u;
                 h->quant_min[g] = 0u;
             }
-            if (threadIdx.x == 0) h->quant_ticket = 0u;
+            if (lane == 0) h->quant_ticket = 0u;
         }
     }
 }
@@ -384,17 +477,49 @@ int resident_grid(const void *fn, int threads)
     return n * device_sm_count();
 }
 
-long long rows_grid(long long n)
+template <int MODE, bool TOKENS>
+cudaError_t launch_encode(const void *src, long long n_src, int H, const moe_layout *L, void *out, float *scales,
+                          cudaStream_t s)
 {
-    const long long cap = 1LL << 30;
-    return n < 1 ? 1 : (n < cap ? n : cap);
+    EncArgs a;
+    a.src = static_cast<const unsigned char *>(src);
+    a.n_src = n_src;
+    a.rowbytes = 2 * H;
+    a.npairs = H / 16;
+    a.k = L->k;
+    a.dst_row = L->dst_row;
+    a.offsets = L->offsets;
+    a.E = L->E;
+    a.r_max = L->r_max;
+    a.out = static_cast<uint4 *>(out);
+    a.scales = reinterpret_cast<float2 *>(scales);
+    a.ws = L->ws;
+    // consumer warps: 8 while 8 rows fit the ring, else fewer; stages: the
+    // largest multiple of the consumer count that fits (at most 16)
+    int c = kEncMaxConsumers;
+    while (c > 1 && (long long)c * a.rowbytes > kEncRingBytes) c >>= 1;
+    int stages = (int)(kEncRingBytes / a.rowbytes) / c * c;
+    if (stages > kEncMaxStages) stages = kEncMaxStages / c * c;
+    if (stages < c) stages = c;
+    a.consumers = c;
+    a.stages = stages;
+    const int threads = 32 * (c + 1);
+    const void *fn = reinterpret_cast<const void *>(fp8_encode_kernel<MODE, TOKENS>);
+    const size_t smem = (size_t)a.stages * a.rowbytes;
+    cudaError_t err = allow_dynamic_smem(fn, (int)smem);
+    if (err != cudaSuccess) return err;
+    int bps = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, fn, threads, smem) != cudaSuccess || bps < 1) bps = 1;
+    const long long resident = (long long)bps * device_sm_count();
+    const unsigned grid = (unsigned)(n_src < resident ? (n_src < 1 ? 1 : n_src) : resident);
+    return launch_pdl(fp8_encode_kernel<MODE, TOKENS>, dim3(grid), dim3(threads), smem, s, a);
 }
 
 template <int MODE, bool TOKENS>
 cudaError_t launch_grouped(const void *src, long long n_src, int H, const moe_layout *L, void *out, float *scales,
                            cudaStream_t s)
 {
-    const int nvec = H / 8, npairs = H / 16;
+    const int nvec = H / 8;
     cudaError_t err = cudaSuccess;
     if (MODE != MOE_FP8_PER_TOKEN) {
         static int res[64] = {0};
@@ -410,19 +535,7 @@ cudaError_t launch_grouped(const void *src, long long n_src, int H, const moe_la
                          (const int32_t *)L->offsets, L->E, L->r_max, L->ws);
         if (err != cudaSuccess) return err;
     }
-    const int per_thread = (npairs + kEncThreads - 1) / kEncThreads;
-    const unsigned grid = (unsigned)rows_grid(n_src);
-#define MOE_ENC(CC)                                                                                            \
-    return launch_pdl(fp8_group_encode_kernel<CC, MODE, TOKENS>, dim3(grid), dim3(kEncThreads), 0, s,          \
-                      static_cast<const uint4 *>(src), n_src, npairs, L->k, (const int32_t *)L->dst_row,       \
-                      (const int32_t *)L->offsets, L->E, L->r_max, static_cast<uint4 *>(out),                  \
-                      reinterpret_cast<float2 *>(scales), L->ws)
-    if (per_thread <= 1) MOE_ENC(1);
-    if (per_thread <= 2) MOE_ENC(2);
-    if (per_thread <= 4) MOE_ENC(4);
-    if (per_thread <= 8) MOE_ENC(8);
-#undef MOE_ENC
-    return cudaErrorInvalidValue;
+    return launch_encode<MODE, TOKENS>(src, n_src, H, L, out, scales, s);
 }
 
 template <int K>
@@ -449,6 +562,7 @@ cudaError_t launch_dispatch_fp8_grouped(const void *x, int T, int H, const moe_l
                                         float *scales, cudaStream_t s)
 {
     if (T == 0) return cudaSuccess;
+    if (mode == MOE_FP8_PER_TOKEN) return launch_grouped<MOE_FP8_PER_TOKEN, true>(x, T, H, L, packed, scales, s);
     if (mode == MOE_FP8_PER_EXPERT) return launch_grouped<MOE_FP8_PER_EXPERT, true>(x, T, H, L, packed, scales, s);
     if (mode == MOE_FP8_GLOBAL) return launch_grouped<MOE_FP8_GLOBAL, true>(x, T, H, L, packed, scales, s);
     return cudaErrorInvalidValue;

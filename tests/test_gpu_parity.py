@@ -221,6 +221,40 @@ def test_fp8_bf16_pattern_sweep():
     check_dispatch(w, plan, L, rows, np.arange(R, dtype=np.int64))
 
 
+@pytest.mark.parametrize("fp8", [1, 3])
+def test_fp8_odd_scale_sweep(fp8):
+    """Scales 3/128, 5/128, ..., 15/128 (not powers of two: the quotient is
+    formed through a reciprocal and checked by the rounding test): rows
+    headed by (M, -M) with M = 448 * scale carry every bf16 value in
+    [-M, M], so every quotient that lands on an e4m3 rounding midpoint
+    exactly, or next to one, is exercised.  Bit-exact against the oracle's
+    true division, per-token and global groups."""
+    H = 64
+    pats = np.arange(65536, dtype=np.uint32)
+    f = (pats << 16).view(np.float32)
+    rows = []
+    for num in (3, 5, 7, 9, 11, 13, 15):
+        M = np.float32(448.0 * num / 128.0)
+        Mb = np.uint32(M.view(np.uint32)) >> 16
+        assert (np.uint32(Mb) << 16).view(np.float32) == M
+        vals = pats[np.isfinite(f) & (np.abs(f) <= M)]
+        for c in range(0, vals.size, H - 2):
+            r = np.zeros(H, np.uint16)
+            r[0], r[1] = Mb, Mb | 0x8000
+            chunk = vals[c:c + H - 2]
+            r[2:2 + chunk.size] = chunk
+            rows.append(r)
+    rows = np.stack(rows)
+    w = _custom(rows.shape[0], H, 8, 1, 1, fp8=fp8)
+    x = torch.from_numpy(rows.view(np.int16)).cuda().view(torch.bfloat16)
+    inp = dict(logits=workloads.make_logits(w, "cuda"), x=x, shared=None)
+    plan, gates_pre, og, R, eo, status = run_gpu(w, inp)
+    assert status == 0 and R == w.T
+    check_gate(w, plan, gates_pre, og)
+    L = check_layout(w, plan, og)
+    check_dispatch(w, plan, L, rows, np.arange(R, dtype=np.int64))
+
+
 def test_repeated_calls_reuse_workspace():
     """The workspace returns to a clean state after every call: three passes
     over different inputs on one plan match fresh oracle runs."""
