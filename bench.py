@@ -45,6 +45,10 @@ def parse_args():
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-pipeline", action="store_true",
+                    help="time the step only as separate calls on one stream")
+    ap.add_argument("--route-priority", choices=["high", "same"], default="high",
+                    help="priority of the routing stream against the data stream")
     ap.add_argument("--backward-steps", type=int, default=500,
                     help="passes of the backward calls timed after the forward (0: skip)")
     return ap.parse_args()
@@ -446,6 +450,13 @@ def run_ours(args):
     st = plan.status()
     if st != 0:
         raise RuntimeError(f"device status {st} during the timed steps")
+    from combine_moe_gate_warp_gb300 import RoutePipeline
+    pipe = None
+    t_pw0 = t_pw1 = None
+    if not args.no_pipeline and RoutePipeline.overlaps(shape):
+        t_pw0 = time.time()
+        pipe = time_pipelined(w, shape, inputs, eo, dev, world, K, max(3, args.warmup), args.route_priority)
+        t_pw1 = time.time()
     if sampler:
         time.sleep(0.25)
         sampler.stop()
@@ -457,53 +468,19 @@ def run_ours(args):
     dom = max(("dispatch", "combine"), key=lambda n: per[n])
     achieved = by[dom] / (per[dom] * 1e-3) / 1e9
     traffic = measured_traffic(dom, w.name)
-    ms_step = elapsed_ms / K
-    tokens_per_s = world * w.T * K / (elapsed_ms * 1e-3)
+    ms_step_serial = elapsed_ms / K
+    unpipelined = {"ms_per_step": ms_step_serial,
+                   "tokens_per_s": world * w.T * K / (elapsed_ms * 1e-3),
+                   "hbm_frac": by["roofline_step"] / (ms_step_serial * 1e-3) / 1e9 / peak,
+                   "note": "the calls of each step on one stream, one batch after another"}
+    ms_step = pipe["ms_per_step"] if pipe else ms_step_serial
+    tokens_per_s = world * w.T / (ms_step * 1e-3)
     step_gbs = by["roofline_step"] / (ms_step * 1e-3) / 1e9
 
     # end to end through the public API: pinned host inputs copied in, result copied out
     e2e = None
     if not args.no_e2e:
-        pin = dict(logits=inputs["logits"].cpu().pin_memory(), x=inputs["x"].cpu().pin_memory())
-        eo_h = None if eo is None else eo.cpu().pin_memory()
-        sh_h = None if inputs["shared"] is None else inputs["shared"].cpu().pin_memory()
-        d_logits = torch.empty_like(inputs["logits"])
-        d_x = torch.empty_like(inputs["x"])
-        d_eo = None if eo is None else torch.empty_like(eo)
-        d_sh = None if sh_h is None else torch.empty_like(inputs["shared"])
-        y_h = torch.empty(plan.y.shape, dtype=plan.y.dtype, pin_memory=True)
-        stats_h = torch.empty(2, dtype=torch.float64, pin_memory=True)
-        h2d = sum(t.numel() * t.element_size() for t in (pin["logits"], pin["x"], eo_h, sh_h) if t is not None)
-        d2h = y_h.numel() * y_h.element_size() + 16
-
-        def e2e_step():
-            d_logits.copy_(pin["logits"], non_blocking=True)
-            d_x.copy_(pin["x"], non_blocking=True)
-            if d_eo is not None:
-                d_eo.copy_(eo_h, non_blocking=True)
-            if d_sh is not None:
-                d_sh.copy_(sh_h, non_blocking=True)
-            plan.step(d_logits, d_x, plan.packed if d_eo is None else d_eo, d_sh)
-            y_h.copy_(plan.y, non_blocking=True)
-            stats_h[0:1].copy_(plan.aux_loss, non_blocking=True)
-            stats_h[1:2].copy_(plan.entropy, non_blocking=True)
-
-        for _ in range(3):
-            e2e_step()
-        torch.cuda.synchronize(dev)
-        K2 = max(1, args.e2e_steps)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        barrier(world)
-        torch.cuda.synchronize(dev)
-        a.record(stream)
-        for _ in range(K2):
-            e2e_step()
-        b.record(stream)
-        torch.cuda.synchronize(dev)
-        e_ms = max_over_ranks(a.elapsed_time(b), world, dev)
-        e2e = {"value": world * w.T * K2 / (e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / K2, "steps": K2,
-               "path": "pinned host -> device copies, the four C-ABI calls, y/aux/entropy back, one stream"}
+        e2e = time_e2e(w, shape, plan, inputs, eo, dev, world, args.e2e_steps, pipe is not None)
 
     bwd = None
     if args.backward_steps > 0:
@@ -513,7 +490,7 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, host_inputs(w, inputs, eo), args.cpu_seconds)
 
-    clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
+    clocks = (sampler.summary(t_pw0, t_pw1) if pipe else sampler.summary(t_wall0, t_wall1)) if sampler else None
     if rank == 0:
         line = {
             "metric": METRIC, "value": tokens_per_s, "unit": UNIT, "n_gpus": world, "steps": K,
@@ -532,6 +509,8 @@ def run_ours(args):
             "kernels_gbs": {n: by[n] / (per[n] * 1e-3) / 1e9 for n in names},
             "step_ms_evented": {"median": statistics.median(step_samples), "min": step_samples[0],
                                 "note": "sampled steps with events between the calls"},
+            "execution": (pipe["note"] if pipe else unpipelined["note"]),
+            "unpipelined": unpipelined,
             "gpu_launches": plan.launches_per_step() * K,
             "clocks": clocks,
             "e2e": e2e,
@@ -543,6 +522,149 @@ def run_ours(args):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def time_e2e(w, shape, plan, inputs, eo, dev, world, steps, pipelined):
+    """The same metric end to end: every step copies its inputs (router
+    logits, x, expert outputs, shared-expert outputs) from pinned host memory
+    to the device and reads y, the aux loss and the entropy back.  With the
+    pipelined executor the copies of batch i+1 overlap the work of batch i
+    (a copy stream feeds each plan's own input buffers); otherwise the
+    copies and the calls run in order on one stream."""
+    import torch
+
+    from combine_moe_gate_warp_gb300 import RoutePipeline
+    pin = dict(logits=inputs["logits"].cpu().pin_memory(), x=inputs["x"].cpu().pin_memory())
+    eo_h = None if eo is None else eo.cpu().pin_memory()
+    sh_h = None if inputs["shared"] is None else inputs["shared"].cpu().pin_memory()
+    y_h = torch.empty((w.T, w.H), dtype=torch.bfloat16, pin_memory=True)
+    stats_h = torch.empty(2, dtype=torch.float64, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in (pin["logits"], pin["x"], eo_h, sh_h) if t is not None)
+    d2h = y_h.numel() * y_h.element_size() + 16
+
+    def dev_buffers():
+        return dict(logits=torch.empty_like(inputs["logits"]), x=torch.empty_like(inputs["x"]),
+                    eo=None if eo is None else torch.empty_like(eo),
+                    shared=None if inputs["shared"] is None else torch.empty_like(inputs["shared"]))
+
+    def copy_in(d):
+        d["logits"].copy_(pin["logits"], non_blocking=True)
+        d["x"].copy_(pin["x"], non_blocking=True)
+        if d["eo"] is not None:
+            d["eo"].copy_(eo_h, non_blocking=True)
+        if d["shared"] is not None:
+            d["shared"].copy_(sh_h, non_blocking=True)
+
+    K2 = max(1, steps)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if pipelined:
+        pipe = RoutePipeline(shape, dev)
+        bufs = [dev_buffers() for _ in pipe.plans]
+        copy_stream = torch.cuda.Stream(dev)
+        copied = [torch.cuda.Event() for _ in pipe.plans]
+
+        def one():
+            i = pipe.step_index
+            d = i % len(pipe.plans)
+            copy_stream.wait_event(pipe.release_event(i))
+            with torch.cuda.stream(copy_stream):
+                copy_in(bufs[d])
+            copied[d].record(copy_stream)
+            pipe.route_stream.wait_event(copied[d])
+            pipe.data_stream.wait_event(copied[d])
+            p = pipe.plan_for(i)
+            bd = bufs[d]
+            pipe.step(bd["logits"], bd["x"], p.packed if bd["eo"] is None else bd["eo"], bd["shared"],
+                      out=y_h, stats_out=stats_h)
+
+        for _ in range(3):
+            one()
+        pipe.synchronize()
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        a.record(copy_stream)
+        pipe.route_stream.wait_event(a)
+        pipe.data_stream.wait_event(a)
+        for _ in range(K2):
+            one()
+        b.record(pipe.data_stream)
+        torch.cuda.synchronize(dev)
+        st = pipe.status()
+        path = ("pinned host -> device copies on a copy stream into each plan's input buffers, the C-ABI "
+                "calls through RoutePipeline, y/aux/entropy back on the data stream; batch i+1's copies "
+                "and routing overlap batch i's data movement")
+    else:
+        stream = torch.cuda.current_stream(dev)
+        d = dev_buffers()
+
+        def one():
+            copy_in(d)
+            plan.step(d["logits"], d["x"], plan.packed if d["eo"] is None else d["eo"], d["shared"])
+            y_h.copy_(plan.y[:w.T], non_blocking=True)
+            stats_h[0:1].copy_(plan.aux_loss, non_blocking=True)
+            stats_h[1:2].copy_(plan.entropy, non_blocking=True)
+
+        for _ in range(3):
+            one()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        a.record(stream)
+        for _ in range(K2):
+            one()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        st = plan.status()
+        path = "pinned host -> device copies, the C-ABI calls, y/aux/entropy back, one stream"
+    if st != 0:
+        raise RuntimeError(f"device status {st} in the end-to-end steps")
+    e_ms = max_over_ranks(a.elapsed_time(b), world, dev)
+    return {"value": world * w.T * K2 / (e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / K2, "steps": K2, "path": path}
+
+
+def time_pipelined(w, shape, inputs, eo, dev, world, K, W, route_priority="high"):
+    """K back-to-back batches through RoutePipeline: two plans and two input
+    batches (the workload's seed and the next one) alternate, so every step
+    routes a batch while the previous batch's dispatch and combine run."""
+    import torch
+
+    from combine_moe_gate_warp_gb300 import RoutePipeline, workloads
+    w2 = workloads.Workload(**{**w.__dict__, "seed": w.seed + 1})
+    inputs2 = workloads.make_inputs(w2, dev)
+    pipe = RoutePipeline(shape, dev, route_priority=route_priority)
+    eo2 = None if eo is None else workloads.make_expert_out(w2, max(pipe.plans[0].r_max, 1), dev)
+    batches = [(inputs, eo), (inputs2, eo2)]
+
+    def one(i):
+        inp, e = batches[i % 2]
+        p = pipe.plan_for(pipe.step_index)
+        pipe.step(inp["logits"], inp["x"], p.packed if e is None else e, inp["shared"])
+
+    torch.cuda.synchronize(dev)
+    for i in range(W):
+        one(i)
+    torch.cuda.synchronize(dev)
+    st = pipe.status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the pipelined warm-up")
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    start.record(pipe.data_stream)
+    pipe.route_stream.wait_event(start)
+    for i in range(K):
+        one(W + i)
+    stop.record(pipe.data_stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    ms = max_over_ranks(start.elapsed_time(stop), world, dev) / K
+    st = pipe.status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} during the pipelined steps")
+    return {"ms_per_step": ms,
+            "note": "back-to-back batches (two alternating input batches and plans): gate + layout of "
+                    "batch i on a high-priority stream overlap dispatch + combine of batch i-1"}
 
 
 def time_backward(plan, w, inputs, eo_arg, steps, world, dev, stream, peak):
