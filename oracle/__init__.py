@@ -66,6 +66,8 @@ def _lib():
         lib.oracle_combine_f32order_tokens.restype = None
         lib.oracle_combine_ref64_tokens.argtypes = [P, I64, I, P, P, P, I, I64, P, I64, P, P]
         lib.oracle_combine_ref64_tokens.restype = None
+        lib.oracle_layout_reassign.argtypes = [P, I64, I, I, I, I64, P, P, P, P, P, P, P, P, P, P, P]
+        lib.oracle_layout_reassign.restype = I
         lib.oracle_fp8_group_params.argtypes = [P, I64, P, P, I64, I64, P]
         lib.oracle_fp8_group_params.restype = I
         lib.oracle_quantize_rows_with_params.argtypes = [P, I64, P, P, I64, P, P, P]
@@ -175,6 +177,45 @@ def layout(topk_idx: np.ndarray, E: int, P: int, capacity: int = 0, gates_f32=No
     R = int(out["offsets"][E])
     out["src_pos"] = out["src_pos"][:R]
     out["capacity_mask"] = out["capacity_mask"][:A]
+    out["dropped"] = int(dropped[0])
+    out["R"] = R
+    if g is not None:
+        out["gates"] = g
+    return out
+
+
+def layout_reassign(topk_idx: np.ndarray, E: int, P: int, capacity: int, gates_f32=None):
+    """Dispatch layout with capacity overflow re-assigned to the least-loaded
+    expert (capacity > 0).  Same keys as ``layout`` plus ``final_expert``;
+    capacity_mask is 1 kept, 2 re-assigned, 0 dropped."""
+    topk_idx = _c(topk_idx, np.int32)
+    T, k = topk_idx.shape
+    A = T * k
+    r_max = min(A, E * capacity)
+    g = None if gates_f32 is None else np.array(gates_f32, dtype=np.float32, copy=True, order="C")
+    out = dict(
+        counts=np.empty(E, np.int32),
+        offsets=np.empty(E + 1, np.int32),
+        dst_row=np.empty(max(A, 1), np.int32),
+        src_pos=np.full(max(r_max, 1), -7, np.int32),
+        capacity_mask=np.empty(max(A, 1), np.uint8),
+        final_expert=np.empty(max(A, 1), np.int32),
+        part_rows=np.empty(P, np.int32),
+        part_offsets=np.empty(P + 1, np.int32),
+        part_tokens=np.empty(P, np.int32),
+    )
+    dropped = np.zeros(1, np.int64)
+    rc = _lib().oracle_layout_reassign(
+        _p(topk_idx), T, E, k, P, capacity, _p(g),
+        _p(out["counts"]), _p(out["offsets"]), _p(out["dst_row"]), _p(out["src_pos"]),
+        _p(out["capacity_mask"]), _p(out["final_expert"]), _p(out["part_rows"]), _p(out["part_offsets"]),
+        _p(out["part_tokens"]), _p(dropped))
+    if rc != 0:
+        raise ValueError(f"oracle_layout_reassign failed ({rc})")
+    R = int(out["offsets"][E])
+    for key in ("dst_row", "capacity_mask", "final_expert"):
+        out[key] = out[key][:A]
+    out["src_pos"] = out["src_pos"][:R]
     out["dropped"] = int(dropped[0])
     out["R"] = R
     if g is not None:

@@ -280,6 +280,115 @@ int oracle_layout(const int32_t *topk_idx, int64_t T, int E, int k, int P, int64
     return 0;
 }
 
+/* Capacity overflow re-assigned instead of dropped ([P4] sec. 8.3.A:
+ * greedy top-k selection under a hard per-expert capacity, then a rolling
+ * fallback that sends the assignments an expert cannot take to the expert
+ * with the lowest load in the batch).  Read as two passes:
+ *   1. every expert keeps its first `capacity` assignments in token order
+ *      (exactly as oracle_layout);
+ *   2. the remaining ("overflow") assignments, in flat order a = t*k + j,
+ *      each go to the expert with the lowest current load (ties: lower id)
+ *      among experts below capacity, raising its load by one; with no such
+ *      expert the assignment is dropped.
+ * Rows: an expert's kept assignments in token order, then the ones it
+ * received in pass 2 in the order received.  capacity_mask: 1 kept where
+ * routed, 2 re-assigned, 0 dropped.  final_expert[a]: the expert that
+ * processes assignment a (-1 if dropped).  A re-assigned slot keeps its gate
+ * weight; only dropped slots get gate 0.  Partitions follow the final
+ * experts. */
+int oracle_layout_reassign(const int32_t *topk_idx, int64_t T, int E, int k, int P, int64_t capacity,
+                           float *gates_or_null, int32_t *counts, int32_t *offsets, int32_t *dst_row,
+                           int32_t *src_pos, uint8_t *capacity_mask, int32_t *final_expert,
+                           int32_t *part_rows, int32_t *part_offsets, int32_t *part_tokens, int64_t *dropped)
+{
+    if (P <= 0 || E % P != 0 || capacity <= 0) return -1;
+    const int64_t A = T * k;
+    routed_assignment *list = (routed_assignment *)malloc(sizeof(routed_assignment) * (size_t)(A > 0 ? A : 1));
+    int64_t *raw_start = (int64_t *)calloc((size_t)E + 1, sizeof(int64_t));
+    int64_t *load = (int64_t *)calloc((size_t)E, sizeof(int64_t));
+    int64_t *level = (int64_t *)malloc(sizeof(int64_t) * (size_t)(A > 0 ? A : 1));
+    if (!list || !raw_start || !load || !level) { free(list); free(raw_start); free(load); free(level); return -2; }
+    for (int64_t a = 0; a < A; ++a) {
+        int32_t e = topk_idx[a];
+        if (e < 0 || e >= E) { free(list); free(raw_start); free(load); free(level); return -1; }
+        list[a].e = e;
+        list[a].a = a;
+        raw_start[e + 1] += 1;
+    }
+    qsort(list, (size_t)A, sizeof(routed_assignment), by_expert_then_assignment);
+    for (int e = 0; e < E; ++e) raw_start[e + 1] += raw_start[e];
+
+    /* pass 1: the first `capacity` assignments of each expert, in token order */
+    for (int64_t a = 0; a < A; ++a) final_expert[a] = -1;
+    for (int64_t s = 0; s < A; ++s) {
+        int32_t e = list[s].e;
+        int64_t rank = s - raw_start[e];
+        if (rank < capacity) {
+            final_expert[list[s].a] = e;
+            level[list[s].a] = rank;
+            capacity_mask[list[s].a] = 1;
+            load[e] += 1;
+        }
+    }
+    /* pass 2: overflow assignments in flat order to the least-loaded expert */
+    for (int64_t a = 0; a < A; ++a) {
+        if (final_expert[a] >= 0) continue;
+        int best = -1;
+        for (int e = 0; e < E; ++e)
+            if (load[e] < capacity && (best < 0 || load[e] < load[best])) best = e;
+        if (best < 0) {
+            capacity_mask[a] = 0;
+            continue;
+        }
+        final_expert[a] = best;
+        level[a] = load[best];
+        load[best] += 1;
+        capacity_mask[a] = 2;
+    }
+    offsets[0] = 0;
+    for (int e = 0; e < E; ++e) {
+        counts[e] = (int32_t)load[e];
+        offsets[e + 1] = offsets[e] + counts[e];
+    }
+    const int32_t R = offsets[E];
+    for (int64_t a = 0; a < A; ++a) {
+        int32_t e = final_expert[a];
+        if (e < 0) {
+            dst_row[a] = -1;
+            if (gates_or_null) gates_or_null[a] = 0.0f;
+            continue;
+        }
+        int32_t row = offsets[e] + (int32_t)level[a];
+        dst_row[a] = row;
+        src_pos[row] = (int32_t)a;
+    }
+    const int per = E / P;
+    for (int p = 0; p < P; ++p) {
+        int32_t rows = 0;
+        for (int e = p * per; e < (p + 1) * per; ++e) rows += counts[e];
+        part_rows[p] = rows;
+        part_offsets[p] = offsets[p * per];
+        part_tokens[p] = 0;
+    }
+    part_offsets[P] = R;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int p = 0; p < P; ++p) {
+            int hit = 0;
+            for (int j = 0; j < k; ++j) {
+                int32_t e = final_expert[t * k + j];
+                if (e >= 0 && e / per == p) hit = 1;
+            }
+            part_tokens[p] += hit;
+        }
+    }
+    *dropped = A - (int64_t)R;
+    free(list);
+    free(raw_start);
+    free(load);
+    free(level);
+    return 0;
+}
+
 /* ------------------------------------------------------------------ */
 /* a5: dispatch (bf16 transport): packed row r is a bit copy of the     */
 /* hidden state of token src_pos[r] / k ([P4] sec. 7 Dispatch detail,   */
