@@ -245,7 +245,10 @@ def oracle_sample_run(w, inputs_host, T_s):
         cap = (5 * T_s * w.k + 4 * w.E - 1) // (4 * w.E)
     t0 = time.perf_counter()
     idx, g64, counts, aux, ent = oracle.gate(logits, w.k, w.mode)
-    L = oracle.layout(idx, w.E, w.P, cap, gates_f32=g64.astype(np.float32))
+    if w.reassign and cap:
+        L = oracle.layout_reassign(idx, w.E, w.P, cap, gates_f32=g64.astype(np.float32))
+    else:
+        L = oracle.layout(idx, w.E, w.P, cap, gates_f32=g64.astype(np.float32))
     rows = np.arange(L["R"], dtype=np.int64)
     src_row = L["src_pos"].astype(np.int64) // w.k
     if int(w.fp8) == 1:
@@ -322,6 +325,7 @@ def config_of(w, world):
             "expert_outputs": (["bf16", "e4m3 per-token", "e4m3 per-expert", "e4m3 global"][int(w.fp8_combine)]),
             "Ks": w.Ks,
             "capacity": w.capacity or None,
+            "overflow": ("re-assigned to the least-loaded expert" if w.reassign else "dropped") if w.capacity else None,
             "l2": "no flush: each step touches ~%.2f GB, far above the 126 MB L2" % (
                 (w.T * w.H * 2 * 2 + w.T * w.k * w.H * ((1 if w.fp8 else 2) + (1 if w.fp8_combine else 2))) / 1e9),
             "parallelism": f"dp{world}"}
@@ -389,7 +393,7 @@ def run_ours(args):
 
     inputs = workloads.make_inputs(w, dev)
     shape = RouteShape(T=w.T, H=w.H, E=w.E, k=w.k, P=w.P, mode=w.mode, fp8=int(w.fp8), Ks=w.Ks,
-                       capacity=w.capacity, fp8_combine=int(w.fp8_combine))
+                       capacity=w.capacity, fp8_combine=int(w.fp8_combine), reassign=bool(w.reassign))
     plan = RoutePlan(shape, dev)
     eo = None if w.identity_experts else workloads.make_expert_out(w, max(plan.r_max, 1), dev)
     stream = torch.cuda.current_stream(dev)

@@ -86,6 +86,8 @@ def lib():
     L.moe_gate.restype = I
     L.moe_dispatch_layout.argtypes = [P, P, I, I, I, I, I, P, ctypes.POINTER(moe_layout), P, SZ, P]
     L.moe_dispatch_layout.restype = I
+    L.moe_dispatch_layout_reassign.argtypes = [P, P, I, I, I, I, I, P, ctypes.POINTER(moe_layout), P, SZ, P]
+    L.moe_dispatch_layout_reassign.restype = I
     L.moe_dispatch_layout_noalloc.argtypes = [P, P, I, I, I, I, I, P, ctypes.POINTER(moe_layout), P]
     L.moe_dispatch_layout_noalloc.restype = I
     L.moe_dispatch.argtypes = [P, I, I, ctypes.POINTER(moe_layout), I, P, P, P]
@@ -183,6 +185,16 @@ def moe_dispatch_layout(topk_idx, expert_counts, T: int, E: int, k: int, P: int,
                                      _ptr(gates_or_null, torch.float32, "gates"),
                                      ctypes.byref(layout.c), _ptr(ws, name="ws"), _nbytes(ws),
                                      _stream(stream)), "moe_dispatch_layout")
+
+
+def moe_dispatch_layout_reassign(topk_idx, expert_counts, T: int, E: int, k: int, P: int, capacity: int,
+                                 gates_or_null, layout: "Layout", ws, stream=None) -> None:
+    _check(lib().moe_dispatch_layout_reassign(_ptr(topk_idx, torch.int32, "topk_idx"),
+                                              _ptr(expert_counts, torch.int32, "expert_counts"),
+                                              T, E, k, P, capacity,
+                                              _ptr(gates_or_null, torch.float32, "gates"),
+                                              ctypes.byref(layout.c), _ptr(ws, name="ws"), _nbytes(ws),
+                                              _stream(stream)), "moe_dispatch_layout_reassign")
 
 
 def moe_dispatch_layout_noalloc(topk_idx, expert_counts, T: int, E: int, k: int, P: int,

@@ -101,9 +101,9 @@ moe_status moe_gate(const float *logits, int T, int E, int k, int mode, int32_t 
                                       entropy, ws, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-moe_status moe_dispatch_layout(const int32_t *topk_idx, const int32_t *expert_counts, int T, int E,
-                               int k, int P, int capacity, float *gates_or_null, moe_layout *L,
-                               void *ws, size_t ws_bytes, moe_stream_t stream)
+static moe_status dispatch_layout_impl(const int32_t *topk_idx, const int32_t *expert_counts, int T, int E,
+                                       int k, int P, int capacity, float *gates_or_null, moe_layout *L,
+                                       void *ws, size_t ws_bytes, moe_stream_t stream, int reassign)
 {
     moe_status st = check_sizes(T, E, k);
     if (st != MOE_OK) return st;
@@ -123,7 +123,23 @@ moe_status moe_dispatch_layout(const int32_t *topk_idx, const int32_t *expert_co
     L->r_max = (int32_t)moe_rows_max(T, E, k, capacity);
     L->ws = ws;
     return from_cuda(moe::launch_layout(topk_idx, expert_counts, T, E, k, P, capacity, gates_or_null, L,
-                                        ws, reinterpret_cast<cudaStream_t>(stream)));
+                                        ws, reinterpret_cast<cudaStream_t>(stream), reassign));
+}
+
+moe_status moe_dispatch_layout(const int32_t *topk_idx, const int32_t *expert_counts, int T, int E,
+                               int k, int P, int capacity, float *gates_or_null, moe_layout *L,
+                               void *ws, size_t ws_bytes, moe_stream_t stream)
+{
+    return dispatch_layout_impl(topk_idx, expert_counts, T, E, k, P, capacity, gates_or_null, L, ws, ws_bytes,
+                                stream, 0);
+}
+
+moe_status moe_dispatch_layout_reassign(const int32_t *topk_idx, const int32_t *expert_counts, int T, int E,
+                                        int k, int P, int capacity, float *gates_or_null, moe_layout *L,
+                                        void *ws, size_t ws_bytes, moe_stream_t stream)
+{
+    return dispatch_layout_impl(topk_idx, expert_counts, T, E, k, P, capacity, gates_or_null, L, ws, ws_bytes,
+                                stream, 1);
 }
 
 static moe_status check_layout(const moe_layout *L, int T)

@@ -140,7 +140,7 @@ cudaError_t launch_gate(const float *logits, int T, int E, int k, int mode, int3
                         void *ws, cudaStream_t s);
 cudaError_t launch_layout(const int32_t *topk_idx, const int32_t *counts_in, int T, int E, int k,
                           int P, int capacity, float *gates, const moe_layout *L, void *ws,
-                          cudaStream_t s);
+                          cudaStream_t s, int reassign = 0);
 cudaError_t launch_dispatch_bf16(const void *x, int T, int H, const moe_layout *L, void *packed,
                                  cudaStream_t s);
 cudaError_t launch_combine(const void *eo, const moe_layout *L, const float *gates,

@@ -53,7 +53,49 @@ struct LayoutArgs {
     uint8_t *cmask;
     int64_t *dropped;
     void *ws;
+    int reassign;  // capacity overflow re-assigned to the least-loaded expert
 };
+
+// Water filling of the overflow (re-assign mode).  Experts are ranked by
+// (kept load L_e, id); the places left below capacity are the slots
+// (level, expert) with level in [L_e, C), taken in (level, expert) order.
+// Segment i of the levels, [L_(i), L_(i+1)) (L_(E) = C), has the i+1 lowest
+// ranked experts active; G_i = slots below level L_(i).
+struct WaterFill {
+    int Ls[MOE_MAX_EXPERTS + 1];          // sorted kept loads, Ls[E] = C
+    long long G[MOE_MAX_EXPERTS + 1];     // slots below segment i
+    unsigned mask[MOE_MAX_EXPERTS][8];    // experts of rank <= i (bit per id)
+    int rank[MOE_MAX_EXPERTS];            // rank of each expert
+};
+
+// j-th set bit (0-based) of a 256-bit mask.
+__device__ __forceinline__ int select_bit(const unsigned (&m)[8], int j)
+{
+    for (int w = 0; w < 8; ++w) {
+        const int c = __popc(m[w]);
+        if (j < c) {
+            unsigned v = m[w];
+            for (int q = 0; q < j; ++q) v &= v - 1u;
+            return w * 32 + __ffs(v) - 1;
+        }
+        j -= c;
+    }
+    return -1;
+}
+
+// Slot m (< G[E]) -> (level, expert).
+__device__ __forceinline__ void water_slot(const WaterFill &wf, int E, long long m, int &level, int &expert)
+{
+    int lo = 0, hi = E - 1;  // largest i with G[i] <= m
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (wf.G[mid] <= m) lo = mid;
+        else hi = mid - 1;
+    }
+    const long long off = m - wf.G[lo];
+    level = wf.Ls[lo] + (int)(off / (lo + 1));
+    expert = select_bit(wf.mask[lo], (int)(off % (lo + 1)));
+}
 
 __device__ __forceinline__ unsigned long long ld_volatile_u64(const unsigned long long *p)
 {
@@ -77,6 +119,9 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
     __shared__ unsigned s_warp_tot[kLayoutWarps];
     __shared__ unsigned s_tile, s_epoch;
     __shared__ int s_last, s_bad, s_skip, s_abort;
+    __shared__ WaterFill s_wf;               // re-assign mode only
+    __shared__ long long s_over, s_overbase;  // overflow before this tile / before the chunk
+    __shared__ int s_cscan[kLayoutWarps];
 
     WsHeader *ws = static_cast<WsHeader *>(a.ws);
     unsigned long long *flags = ws_flags(a.ws);
@@ -154,13 +199,91 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
         }
     }
 
-    // 1. packed offsets: exclusive scan of kept counts (block-wide, E <= 256).
+    // 1. packed offsets: exclusive scan of kept counts (block-wide, E <= 256);
+    // in re-assign mode of the final loads after the water filling.
+    long long total_slots = 0;
     {
         int c = 0;
         if (tid < E) {
             int raw = raw_count;
             if (raw < 0 || (long long)raw > (long long)a.T * k) { raw = 0; s_bad = 1; }
             c = ((unsigned)raw < a.cap) ? raw : (int)a.cap;
+        }
+        if (a.reassign) {
+            const int C = (int)a.cap;
+            // overflow total and the expert ranks by (kept load, id)
+            const long long over = tid < E ? (long long)(max(raw_count, 0) - c) : 0;
+            long long o = over;
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1) o += __shfl_xor_sync(0xffffffffu, o, d);
+            if (tid == 0) s_over = 0;
+            if (tid < E) s_wf.Ls[tid] = c;  // kept loads by id, for the ranking
+            __syncthreads();
+            if (lane == 0 && o) atomicAdd(reinterpret_cast<unsigned long long *>(&s_over), (unsigned long long)o);
+            int rk = 0;
+            if (tid < E)
+                for (int e2 = 0; e2 < E; ++e2) {
+                    const int l2 = s_wf.Ls[e2];
+                    rk += (l2 < c) || (l2 == c && e2 < tid);
+                }
+            __syncthreads();
+            if (tid < E) {
+                s_wf.rank[tid] = rk;
+                s_wf.Ls[rk] = c;
+                s_wf.G[rk] = tid;  // expert of rank rk (temporarily)
+            }
+            if (tid == 0) s_wf.Ls[E] = C;
+            __syncthreads();
+            if (tid < 8) {  // active-set masks, word tid
+                unsigned m = 0u;
+                for (int i = 0; i < E; ++i) {
+                    const int e2 = (int)s_wf.G[i];
+                    if ((e2 >> 5) == tid) m |= 1u << (e2 & 31);
+                    s_wf.mask[i][tid] = m;
+                }
+            }
+            __syncthreads();
+            if (tid == 0) {
+                long long g = 0;
+                for (int i = 0; i <= E; ++i) {
+                    const long long gi = g;
+                    if (i < E) g += (long long)(i + 1) * (s_wf.Ls[i + 1] - s_wf.Ls[i]);
+                    s_wf.G[i] = gi;
+                }
+                s_wf.G[E] = g;  // every place left below capacity
+            }
+            __syncthreads();
+            total_slots = s_wf.G[E];
+            if (tid < E) {
+                // final load: the slots of the first s_over places in (level, expert) order
+                const long long O = s_over;
+                if (O >= total_slots) {
+                    c = C;
+                } else {
+                    int lvO, eO;
+                    water_slot(s_wf, E, O, lvO, eO);
+                    (void)eO;
+                    // slot O is at (lvO, position pO among the active experts by id)
+                    int lo = 0, hi = E - 1;
+                    while (lo < hi) {
+                        const int mid = (lo + hi + 1) >> 1;
+                        if (s_wf.G[mid] <= O) lo = mid;
+                        else hi = mid - 1;
+                    }
+                    const int pO = (int)((O - s_wf.G[lo]) % (lo + 1));
+                    int cc = max(c, lvO);
+                    if (s_wf.rank[tid] <= lo) {
+                        int idpos = 0;
+                        for (int w2 = 0; w2 < 8; ++w2) {
+                            const unsigned mw = s_wf.mask[lo][w2];
+                            if (w2 < (tid >> 5)) idpos += __popc(mw);
+                            else if (w2 == (tid >> 5)) idpos += __popc(mw & ((1u << (tid & 31)) - 1u));
+                        }
+                        if (idpos < pO) ++cc;
+                    }
+                    c = min(cc, C);
+                }
+            }
         }
         int incl = c;
 #pragma unroll
@@ -284,6 +407,96 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
     // for every partition holding at least one of its kept slots (partition
     // bitmask when P <= 64, pairwise check otherwise).
     const int ntok = (int)max(0LL, tok1 - tok0);
+    if (a.reassign) {
+        // Overflow assignments (global rank >= C) are numbered in flat order
+        // across the batch: those of earlier tiles (per expert, its count
+        // before this tile beyond C), then this tile's in token order (a
+        // block scan per chunk of tokens).  Number m takes water-fill slot m
+        // if m < total_slots, else the assignment is dropped.
+        if (tid == 0) s_overbase = 0;
+        __syncthreads();
+        long long ob = (tid < E) ? max(0LL, (long long)s_excl[tid] - (long long)a.cap) : 0;
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) ob += __shfl_xor_sync(0xffffffffu, ob, d);
+        if (lane == 0 && ob) atomicAdd(reinterpret_cast<unsigned long long *>(&s_overbase), (unsigned long long)ob);
+        __syncthreads();
+        long long base = s_overbase;
+        for (int c0 = 0; c0 < ntok; c0 += kLayoutThreads) {
+            const int tl = c0 + tid;
+            int nov = 0;
+            if (tl < ntok) {
+                for (int j = 0; j < k; ++j) {
+                    const int i = tl * k + j;
+                    const int e = s_idx[i];
+                    if (e < E) {
+                        const unsigned pr = (unsigned)s_rank[i];
+                        const unsigned r = s_excl[e] + s_whist[pr >> 24][e] + (pr & 0xFFFFFFu);
+                        nov += r >= a.cap;
+                    }
+                }
+            }
+            // exclusive scan of nov over the chunk, in token order
+            int incl = nov;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int n = __shfl_up_sync(0xffffffffu, incl, d);
+                if (lane >= d) incl += n;
+            }
+            if (lane == 31) s_cscan[warp] = incl;
+            __syncthreads();
+            int wbase = 0, ctot = 0;
+            for (int w2 = 0; w2 < kLayoutWarps; ++w2) {
+                if (w2 < warp) wbase += s_cscan[w2];
+                ctot += s_cscan[w2];
+            }
+            long long m = base + wbase + incl - nov;
+            if (tl < ntok) {
+                int fe[MOE_MAX_TOPK];
+                for (int j = 0; j < k; ++j) {
+                    const int i = tl * k + j;
+                    const int e = s_idx[i];
+                    int row = -1, fin = -1;
+                    bool moved = false;
+                    if (e < E) {
+                        const unsigned pr = (unsigned)s_rank[i];
+                        const unsigned r = s_excl[e] + s_whist[pr >> 24][e] + (pr & 0xFFFFFFu);
+                        if (r < a.cap) {
+                            const int cand = s_off[e] + (int)r;
+                            if (cand < s_off[e + 1] && cand < a.r_max) { row = cand; fin = e; }
+                            else s_bad = 1;
+                        } else {
+                            if (m < total_slots) {
+                                int lv, e2;
+                                water_slot(s_wf, E, m, lv, e2);
+                                const int cand = s_off[e2] + lv;
+                                if (e2 >= 0 && cand < s_off[e2 + 1] && cand < a.r_max) {
+                                    row = cand;
+                                    fin = e2;
+                                    moved = true;
+                                } else {
+                                    s_bad = 1;
+                                }
+                            }
+                            ++m;
+                        }
+                    }
+                    fe[j] = fin;
+                    s_rank[i] = row < 0 ? -1 : (row | (moved ? 0x40000000 : 0));
+                }
+                // partitions reached through the final experts
+                for (int j = 0; j < k; ++j) {
+                    if (fe[j] < 0) continue;
+                    const int p = s_epart[fe[j]];
+                    bool first = true;
+                    for (int jj = 0; jj < j; ++jj)
+                        if (fe[jj] >= 0 && s_epart[fe[jj]] == p) { first = false; break; }
+                    if (first) atomicAdd(&s_ptok[p], 1u);
+                }
+            }
+            base += ctot;
+            __syncthreads();  // s_cscan is rewritten by the next chunk
+        }
+    } else
     for (int tl = tid; tl < ntok; tl += kLayoutThreads) {
         unsigned long long pmask = 0ull;
         for (int j = 0; j < k; ++j) {
@@ -344,9 +557,10 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
     // outputs of this tile (no block reads the workspace after this point)
     for (int i = tid; i < A; i += kLayoutThreads) {
         const long long as = a0 + i;
-        const int row = s_rank[i];
+        const int v = s_rank[i];
+        const int row = v < 0 ? -1 : (v & 0x3FFFFFFF);
         a.dst_row[as] = row;
-        a.cmask[as] = (uint8_t)(row >= 0);
+        a.cmask[as] = (uint8_t)(v < 0 ? 0 : ((v >> 30) ? 2 : 1));  // kept / re-assigned / dropped
         if (row >= 0) a.src_pos[row] = (int32_t)as;
         else if (a.gates) a.gates[as] = 0.0f;
     }
@@ -370,9 +584,10 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
 
 cudaError_t launch_layout(const int32_t *topk_idx, const int32_t *counts_in, int T, int E, int k,
                           int P, int capacity, float *gates, const moe_layout *L, void *ws,
-                          cudaStream_t s)
+                          cudaStream_t s, int reassign)
 {
     LayoutArgs a;
+    a.reassign = (reassign && capacity > 0) ? 1 : 0;
     a.idx = topk_idx;
     a.counts_in = counts_in;
     a.T = T;

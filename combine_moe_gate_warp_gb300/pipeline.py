@@ -26,6 +26,7 @@ class RouteShape:
     Ks: int = 0
     capacity: int = 0
     fp8_combine: int = 0  # expert outputs: 0 bf16, else quantised with this MOE_FP8_* mode
+    reassign: bool = False  # capacity overflow re-assigned to the least-loaded expert (not dropped)
 
 
 def _check_input(t, dtype, shape, name):
@@ -93,7 +94,10 @@ class RoutePlan:
         abi._check(self._lib.moe_gate(logits.data_ptr(), s.T, s.E, s.k, s.mode, *self._gate_tail), "moe_gate")
 
     def dispatch_layout(self):
-        abi._check(self._lib.moe_dispatch_layout(*self._layout_args), "moe_dispatch_layout")
+        if self.shape.reassign:
+            abi._check(self._lib.moe_dispatch_layout_reassign(*self._layout_args), "moe_dispatch_layout_reassign")
+        else:
+            abi._check(self._lib.moe_dispatch_layout(*self._layout_args), "moe_dispatch_layout")
 
     def dispatch(self, x: torch.Tensor):
         s = self.shape

@@ -21,6 +21,9 @@ Workloads (shapes taken from the workloads the source pages discuss):
   prefill_cap T=262144 (batch 128 x seq 2048), H=4096, E=64, k=8, P=8,
               logits N(0, 1.5^2) + the same Zipf-like bias, capacity
               ceil(1.25*T*k/E) per expert, bf16 transport
+  prefill_reassign
+              prefill_cap with the capacity overflow re-assigned to the
+              least-loaded expert instead of dropped
   fp8_expert, fp8_global, fp8_both
               fp8_skewed's shape and inputs with per-expert / global FP8
               groups for the dispatch, or per-token FP8 both ways (the
@@ -57,6 +60,7 @@ class Workload:
     capacity_factor: float = 0.0  # 0: no capacity limit
     identity_experts: bool = False
     fp8_combine: int = 0   # expert outputs: 0 bf16, else FP8 with this quantiser mode
+    reassign: bool = False  # capacity overflow re-assigned to the least-loaded expert
     seed: int = 1234
     note: str = field(default="", compare=False)
 
@@ -98,7 +102,11 @@ WORKLOADS = {
 for _name, _kw in (("fp8_expert", dict(fp8=2)), ("fp8_global", dict(fp8=3)),
                    ("fp8_both", dict(fp8=1, fp8_combine=1))):
     WORKLOADS[_name] = Workload(**{**WORKLOADS["fp8_skewed"].__dict__, "name": _name, **_kw})
-ORDER = ["tiny", "v2_top2", "fine_shared", "fp8_skewed", "prefill_cap", "fp8_expert", "fp8_global", "fp8_both"]
+# prefill_cap with the capacity overflow re-assigned instead of dropped
+WORKLOADS["prefill_reassign"] = Workload(**{**WORKLOADS["prefill_cap"].__dict__, "name": "prefill_reassign",
+                                            "reassign": True})
+ORDER = ["tiny", "v2_top2", "fine_shared", "fp8_skewed", "prefill_cap", "fp8_expert", "fp8_global", "fp8_both",
+         "prefill_reassign"]
 
 
 def _gen(device, seed: int) -> torch.Generator:

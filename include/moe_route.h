@@ -206,6 +206,31 @@ moe_status moe_dispatch_layout_noalloc(const int32_t *topk_idx, const int32_t *e
                                        float *gates_or_null, moe_layout *L, moe_stream_t stream);
 
 /*
+ * moe_dispatch_layout_reassign -- moe_dispatch_layout with the capacity
+ * overflow re-assigned instead of dropped ([P4] sec. 8.3.A: greedy top-k
+ * under a hard per-expert capacity, then a rolling fallback to the
+ * lowest-loaded expert of the batch).  Arguments and outputs as
+ * moe_dispatch_layout, in two passes:
+ *   1. each expert keeps its first `capacity` assignments in token order;
+ *   2. the remaining assignments, in flat order a = t*k + j, each go to the
+ *      expert with the lowest current load (ties to the lower id) that is
+ *      below capacity, raising its load by one; with none left the
+ *      assignment is dropped.
+ * counts[e] is the final load (<= capacity); an expert's rows hold its kept
+ * assignments in token order, then those it received in the order received.
+ * capacity_mask: 1 kept where routed, 2 re-assigned, 0 dropped.  Gates are
+ * zeroed for dropped slots only (a re-assigned slot keeps its weight).
+ * Partitions and part_tokens follow the final experts.  capacity <= 0: no
+ * overflow, identical to moe_dispatch_layout.  Pass 2 runs inside the same
+ * kernel: overflow assignment number m (numbered across the batch) takes
+ * place m of the water filling in (level, expert) order.
+ */
+moe_status moe_dispatch_layout_reassign(const int32_t *topk_idx, const int32_t *expert_counts,
+                                        int T, int E, int k, int P, int capacity,
+                                        float *gates_or_null, moe_layout *L,
+                                        void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
  * moe_dispatch -- permute and pack token hidden states into the
  * expert-contiguous send buffer ([P4] sec. 7 Dispatch detail), optionally
  * as affine FP8 ([P1] sec. 3.1: per-token min/max, affine map; sec. 5.2:

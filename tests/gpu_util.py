@@ -28,7 +28,8 @@ def f_of_bits(b: np.ndarray) -> np.ndarray:
 
 def shape_of(w: workloads.Workload) -> RouteShape:
     return RouteShape(T=w.T, H=w.H, E=w.E, k=w.k, P=w.P, mode=w.mode, fp8=int(w.fp8), Ks=w.Ks,
-                      capacity=w.capacity, fp8_combine=int(w.fp8_combine))
+                      capacity=w.capacity, fp8_combine=int(w.fp8_combine),
+                      reassign=bool(getattr(w, "reassign", False)))
 
 
 def gate_with_oracle(w, plan, logits: torch.Tensor):
@@ -82,7 +83,10 @@ def check_gate(w, plan, gates_pre, og, tol_gate=1e-6):
 def check_layout(w, plan, og):
     """The GPU layout (run on the oracle's gates) against the oracle's."""
     idx, g64 = og[0], og[1]
-    L = oracle.layout(idx, w.E, w.P, w.capacity, gates_f32=g64.astype(np.float32))
+    if getattr(w, "reassign", False) and w.capacity > 0:
+        L = oracle.layout_reassign(idx, w.E, w.P, w.capacity, gates_f32=g64.astype(np.float32))
+    else:
+        L = oracle.layout(idx, w.E, w.P, w.capacity, gates_f32=g64.astype(np.float32))
     lay = plan.layout
     A = w.T * w.k
     assert np.array_equal(lay.counts.cpu().numpy(), L["counts"]), "kept counts"

@@ -32,7 +32,8 @@ def test_exports_every_declared_symbol(lib):
     names = _declared()
     assert {"moe_gate", "moe_dispatch_layout", "moe_dispatch", "moe_combine", "moe_get_status",
             "moe_workspace_size", "moe_workspace_init", "moe_rows_max", "moe_status_string",
-            "moe_combine_backward", "moe_dispatch_backward", "moe_gate_backward"} <= names
+            "moe_combine_backward", "moe_dispatch_backward", "moe_gate_backward", "moe_quantize_rows",
+            "moe_combine_fp8", "moe_dispatch_layout_reassign"} <= names
     for n in names:
         assert hasattr(lib, n), f"{n} declared but not exported"
 
@@ -63,7 +64,12 @@ def test_argument_checks_return_before_any_cuda_call(lib):
     L = abi.moe_layout()
     assert lib.moe_dispatch_layout(fake, fake, 10, 8, 2, 3, 0, None, ctypes.byref(L), fake, 1 << 20, None) == abi.MOE_ERR_UNSUPPORTED
     assert lib.moe_dispatch_layout(fake, fake, 10, 8, 2, 4, 0, None, ctypes.byref(L), fake, 1 << 20, None) == abi.MOE_ERR_INVALID_ARG
+    assert lib.moe_dispatch_layout_reassign(fake, fake, 10, 8, 2, 3, 5, None, ctypes.byref(L), fake, 1 << 20,
+                                            None) == abi.MOE_ERR_UNSUPPORTED
     assert lib.moe_dispatch(fake, 10, 64, None, 0, fake, None, None) == abi.MOE_ERR_INVALID_ARG
+    assert lib.moe_dispatch(fake, 10, 64, None, 4, fake, None, None) == abi.MOE_ERR_INVALID_ARG
+    assert lib.moe_quantize_rows(fake, None, 64, 1, fake, fake, None) == abi.MOE_ERR_INVALID_ARG
+    assert lib.moe_combine_fp8(fake, fake, None, fake, None, 0, 10, 64, fake, None) == abi.MOE_ERR_INVALID_ARG
     assert lib.moe_combine(fake, None, fake, None, 0, 10, 64, fake, None) == abi.MOE_ERR_INVALID_ARG
     assert lib.moe_combine_backward(fake, fake, None, fake, 10, 64, fake, fake, None) == abi.MOE_ERR_INVALID_ARG
     assert lib.moe_dispatch_backward(fake, None, 10, 64, fake, None) == abi.MOE_ERR_INVALID_ARG
@@ -78,7 +84,8 @@ def test_binding_names_match_the_c_abi():
     from combine_moe_gate_warp_gb300 import abi
     for n in ("moe_gate", "moe_dispatch_layout", "moe_dispatch", "moe_combine", "moe_get_status",
               "moe_workspace_size", "moe_workspace_init", "moe_rows_max", "moe_combine_backward",
-              "moe_dispatch_backward", "moe_gate_backward"):
+              "moe_dispatch_backward", "moe_gate_backward", "moe_quantize_rows", "moe_combine_fp8",
+              "moe_dispatch_layout_reassign"):
         assert callable(getattr(abi, n))
     # the struct mirrors the header's field order
     hdr = open(os.path.join(ROOT, "include", "moe_route.h")).read()
