@@ -191,21 +191,32 @@ def kernel_bytes(w, R):
     return by
 
 
-KERNEL_SOURCES = {"dispatch": ("dispatch.cu",), "combine": ("combine.cu",), "gate": ("gate.cu",),
-                  "layout": ("layout.cu",), "combine_backward": ("backward.cu",),
-                  "gate_backward": ("backward.cu",), "dispatch_backward": ("combine.cu",)}
+def kernel_sources(name: str, w=None) -> tuple:
+    """Source files of the kernel behind a call (for the traffic table's
+    staleness check)."""
+    fp8 = bool(w is not None and w.fp8)
+    fp8c = bool(w is not None and w.fp8_combine)
+    table = {
+        "gate": ("gate.cu",), "layout": ("layout.cu",),
+        "dispatch": ("quant.cu", "fp8.cuh", "tma.cuh") if fp8 else ("dispatch.cu",),
+        "quantize": ("quant.cu", "fp8.cuh", "tma.cuh"),
+        "combine": ("quant.cu", "fp8.cuh") if fp8c else ("combine.cu", "tma.cuh"),
+        "combine_backward": ("backward.cu",), "gate_backward": ("backward.cu",),
+        "dispatch_backward": ("combine.cu", "tma.cuh"),
+    }
+    return table[name] + ("common.cuh",)
 
 
-def source_digest(name: str) -> str:
+def source_digest(name: str, w=None) -> str:
     csrc = os.path.join(ROOT, "combine_moe_gate_warp_gb300", "csrc")
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES[name] + ("common.cuh",):
+    for f in kernel_sources(name, w):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def measured_traffic(kernel: str, workload: str):
+def measured_traffic(kernel: str, workload: str, w=None):
     """DRAM bytes per launch from a committed ncu summary, if it was taken
     on the current kernel source; else None."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
@@ -215,7 +226,7 @@ def measured_traffic(kernel: str, workload: str):
     except (OSError, ValueError):
         return None
     ent = table.get(workload, {}).get(kernel)
-    if not ent or ent.get("source_digest") != source_digest(kernel):
+    if not ent or ent.get("source_digest") != source_digest(kernel, w):
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -471,7 +482,7 @@ def run_ours(args):
     peak, peak_kind = hbm_peak()
     dom = max(("dispatch", "combine"), key=lambda n: per[n])
     achieved = by[dom] / (per[dom] * 1e-3) / 1e9
-    traffic = measured_traffic(dom, w.name)
+    traffic = measured_traffic(dom, w.name, w)
     ms_step_serial = elapsed_ms / K
     unpipelined = {"ms_per_step": ms_step_serial,
                    "tokens_per_s": world * w.T * K / (elapsed_ms * 1e-3),
@@ -713,7 +724,7 @@ def time_backward(plan, w, inputs, eo_arg, steps, world, dev, stream, peak):
     by = workloads.nbytes_backward(w, R)
     gbs = {n: by[n] / (per[n] * 1e-3) / 1e9 for n in names}
     return {"steps": steps, "ms_per_pass": total_ms,
-            "traffic": {n: measured_traffic(n, w.name) for n in names},
+            "traffic": {n: measured_traffic(n, w.name, w) for n in names},
             "tokens_per_s": world * w.T / (total_ms * 1e-3),
             "kernels_ms": per, "kernels_gbs": gbs,
             "kernels_frac": {n: gbs[n] / peak for n in names},
