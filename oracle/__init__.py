@@ -68,6 +68,8 @@ def _lib():
         lib.oracle_combine_ref64_tokens.restype = None
         lib.oracle_layout_reassign.argtypes = [P, I64, I, I, I, I64, P, P, P, P, P, P, P, P, P, P, P]
         lib.oracle_layout_reassign.restype = I
+        lib.oracle_dedup_layout.argtypes = [P, P, P, I64, I, I, I, P, P, P, P, P]
+        lib.oracle_dedup_layout.restype = I64
         lib.oracle_fp8_group_params.argtypes = [P, I64, P, P, I64, I64, P]
         lib.oracle_fp8_group_params.restype = I
         lib.oracle_quantize_rows_with_params.argtypes = [P, I64, P, P, I64, P, P, P]
@@ -220,6 +222,29 @@ def layout_reassign(topk_idx: np.ndarray, E: int, P: int, capacity: int, gates_f
     out["R"] = R
     if g is not None:
         out["gates"] = g
+    return out
+
+
+def dedup_layout(dst_row, offsets, gates_f32, T: int, E: int, k: int, P: int):
+    """Per-partition token de-duplication of a layout (see the C function).
+    Returns dict(send_offsets [P+1], send_row [T, P], send_token [S],
+    slot_local [S, k], slot_gate [S, k], S)."""
+    dst_row = _c(dst_row, np.int32)
+    offsets = _c(offsets, np.int32)
+    gates_f32 = _c(gates_f32, np.float32)
+    s_max = max(T * min(k, P), 1)
+    out = dict(send_offsets=np.empty(P + 1, np.int32), send_row=np.empty((max(T, 1), P), np.int32),
+               send_token=np.empty(s_max, np.int32), slot_local=np.empty((s_max, k), np.int32),
+               slot_gate=np.empty((s_max, k), np.float32))
+    S = _lib().oracle_dedup_layout(_p(dst_row), _p(offsets), _p(gates_f32), T, E, k, P, _p(out["send_offsets"]),
+                                   _p(out["send_row"]), _p(out["send_token"]), _p(out["slot_local"]),
+                                   _p(out["slot_gate"]))
+    if S < 0:
+        raise ValueError("oracle_dedup_layout failed")
+    out["S"] = int(S)
+    out["send_row"] = out["send_row"][:T]
+    for key in ("send_token", "slot_local", "slot_gate"):
+        out[key] = out[key][:S]
     return out
 
 

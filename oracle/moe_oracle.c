@@ -216,14 +216,23 @@ int oracle_layout(const int32_t *topk_idx, int64_t T, int E, int k, int P, int64
     int64_t *raw_start = (int64_t *)calloc((size_t)E + 1, sizeof(int64_t));
     if (!list || !raw_start) { free(list); free(raw_start); return -2; }
 
+    /* id -1 marks an empty slot (a row with fewer than k assignments, as in
+     * the de-duplicated receive rows): no row, not counted, not an error */
+    int64_t n = 0;
     for (int64_t a = 0; a < A; ++a) {
         int32_t e = topk_idx[a];
+        if (e == -1) {
+            dst_row[a] = -1;
+            capacity_mask[a] = 0;
+            continue;
+        }
         if (e < 0 || e >= E) { free(list); free(raw_start); return -1; }
-        list[a].e = e;
-        list[a].a = a;
+        list[n].e = e;
+        list[n].a = a;
+        ++n;
         raw_start[e + 1] += 1;
     }
-    qsort(list, (size_t)A, sizeof(routed_assignment), by_expert_then_assignment);
+    qsort(list, (size_t)n, sizeof(routed_assignment), by_expert_then_assignment);
     for (int e = 0; e < E; ++e) raw_start[e + 1] += raw_start[e];
 
     /* kept counts and packed-row offsets */
@@ -237,7 +246,7 @@ int oracle_layout(const int32_t *topk_idx, int64_t T, int E, int k, int P, int64
     const int32_t R = offsets[E];
 
     /* ranks, drops, the two index maps */
-    for (int64_t s = 0; s < A; ++s) {
+    for (int64_t s = 0; s < n; ++s) {
         int32_t e = list[s].e;
         int64_t a = list[s].a;
         int64_t rank = s - raw_start[e];
@@ -269,7 +278,7 @@ int oracle_layout(const int32_t *topk_idx, int64_t T, int E, int k, int P, int64
             int hit = 0;
             for (int j = 0; j < k; ++j) {
                 int64_t a = t * k + j;
-                if (capacity_mask[a] && topk_idx[a] / per == p) hit = 1;
+                if (capacity_mask[a] && topk_idx[a] >= 0 && topk_idx[a] / per == p) hit = 1;
             }
             part_tokens[p] += hit;
         }
@@ -387,6 +396,73 @@ int oracle_layout_reassign(const int32_t *topk_idx, int64_t T, int E, int k, int
     free(load);
     free(level);
     return 0;
+}
+
+/* Per-partition token de-duplication ([P4] sec. 7 dispatch detail: the
+ * rows bound for one destination are packed together; a token that picks
+ * several experts of one partition is sent there once, with the list of
+ * its experts and gates, and the partition returns one row for it).
+ * From a layout (dst_row, offsets: the final expert of every kept slot is
+ * the expert whose rows contain dst_row) and the gates:
+ *   send_offsets[P+1]  exclusive scan of the tokens sent to each partition
+ *   send_row[t*P + p]  the send row of (t, p), or -1 if t keeps no slot in p
+ *   send_token[s]      the token of send row s (rows: partition-major,
+ *                      tokens ascending)
+ *   slot_local[s*k+q], slot_gate[s*k+q]  the q-th kept slot (slot order)
+ *                      of the token in that partition: local expert id
+ *                      (expert - p*E/P) and gate; -1 / 0 past the last.
+ * Returns the number of send rows, or -1 on bad input. */
+int64_t oracle_dedup_layout(const int32_t *dst_row, const int32_t *offsets, const float *gates, int64_t T,
+                            int E, int k, int P, int32_t *send_offsets, int32_t *send_row, int32_t *send_token,
+                            int32_t *slot_local, float *slot_gate)
+{
+    if (P <= 0 || E % P != 0) return -1;
+    const int per = E / P;
+    const int32_t R = offsets[E];
+    send_offsets[0] = 0;
+    for (int p = 0; p < P; ++p) {
+        int32_t cnt = 0;
+        for (int64_t t = 0; t < T; ++t) {
+            int hit = 0;
+            for (int j = 0; j < k; ++j) {
+                int32_t r = dst_row[t * k + j];
+                if (r < 0 || r >= R) continue;
+                int e = 0;
+                while (offsets[e + 1] <= r) ++e;
+                if (e / per == p) hit = 1;
+            }
+            cnt += hit;
+        }
+        send_offsets[p + 1] = send_offsets[p] + cnt;
+    }
+    for (int p = 0; p < P; ++p) {
+        int32_t s = send_offsets[p];
+        for (int64_t t = 0; t < T; ++t) {
+            int q = 0;
+            for (int j = 0; j < k; ++j) {
+                int32_t r = dst_row[t * k + j];
+                if (r < 0 || r >= R) continue;
+                int e = 0;
+                while (offsets[e + 1] <= r) ++e;
+                if (e / per != p) continue;
+                slot_local[(int64_t)s * k + q] = e - p * per;
+                slot_gate[(int64_t)s * k + q] = gates[t * k + j];
+                ++q;
+            }
+            if (q == 0) {
+                send_row[t * P + p] = -1;
+                continue;
+            }
+            for (int qq = q; qq < k; ++qq) {
+                slot_local[(int64_t)s * k + qq] = -1;
+                slot_gate[(int64_t)s * k + qq] = 0.0f;
+            }
+            send_row[t * P + p] = s;
+            send_token[s] = (int32_t)t;
+            ++s;
+        }
+    }
+    return send_offsets[P];
 }
 
 /* ------------------------------------------------------------------ */
