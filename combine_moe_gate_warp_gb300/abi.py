@@ -60,6 +60,16 @@ class moe_layout(ctypes.Structure):
     ]
 
 
+class moe_dedup(ctypes.Structure):
+    """Mirror of ``struct moe_dedup`` (host struct of device pointers)."""
+    _fields_ = [
+        ("T", ctypes.c_int32), ("k", ctypes.c_int32), ("P", ctypes.c_int32), ("s_max", ctypes.c_int32),
+        ("ws", ctypes.c_void_p),
+        ("send_offsets", ctypes.c_void_p), ("send_row", ctypes.c_void_p), ("send_token", ctypes.c_void_p),
+        ("slot_local", ctypes.c_void_p), ("slot_gate", ctypes.c_void_p),
+    ]
+
+
 def library_path() -> str:
     return _build.LIB_PATH
 
@@ -104,6 +114,14 @@ def lib():
     L.moe_dispatch_backward.restype = I
     L.moe_gate_backward.argtypes = [P, P, P, I, I, I, I, P, P, SZ, P]
     L.moe_gate_backward.restype = I
+    L.moe_dedup_scratch_size.argtypes = [I, I]
+    L.moe_dedup_scratch_size.restype = SZ
+    L.moe_dedup_layout.argtypes = [ctypes.POINTER(moe_layout), P, ctypes.POINTER(moe_dedup), P, SZ, P]
+    L.moe_dedup_layout.restype = I
+    L.moe_dispatch_dedup.argtypes = [P, I, I, ctypes.POINTER(moe_dedup), I, P, P, P]
+    L.moe_dispatch_dedup.restype = I
+    L.moe_combine_partials.argtypes = [P, ctypes.POINTER(moe_dedup), P, I, I, I, P, P]
+    L.moe_combine_partials.restype = I
     L.moe_get_status.argtypes = [P, P]
     L.moe_get_status.restype = I
     L.moe_status_string.argtypes = [I]
@@ -262,6 +280,28 @@ def moe_gate_backward(logits, topk_idx, d_gates, mode: int, d_logits, ws, stream
                                    _stream(stream)), "moe_gate_backward")
 
 
+def moe_dedup_scratch_size(T: int, P: int) -> int:
+    return int(lib().moe_dedup_scratch_size(T, P))
+
+
+def moe_dedup_layout(layout: "Layout", gates, dedup: "Dedup", stream=None) -> None:
+    _check(lib().moe_dedup_layout(ctypes.byref(layout.c), _ptr(gates, torch.float32, "gates"), ctypes.byref(dedup.c),
+                                  _ptr(dedup.scratch, name="scratch"), _nbytes(dedup.scratch), _stream(stream)),
+           "moe_dedup_layout")
+
+
+def moe_dispatch_dedup(x, T: int, H: int, dedup: "Dedup", fp8: int, send_buf, scales=None, stream=None) -> None:
+    _check(lib().moe_dispatch_dedup(_ptr(x, torch.bfloat16, "x"), T, H, ctypes.byref(dedup.c), int(fp8),
+                                    _ptr(send_buf, torch.uint8 if fp8 else torch.bfloat16, "send_buf"),
+                                    _ptr(scales, torch.float32, "scales"), _stream(stream)), "moe_dispatch_dedup")
+
+
+def moe_combine_partials(partials, dedup: "Dedup", shared_out, Ks: int, T: int, H: int, y, stream=None) -> None:
+    _check(lib().moe_combine_partials(_ptr(partials, torch.bfloat16, "partials"), ctypes.byref(dedup.c),
+                                      _ptr(shared_out, torch.bfloat16, "shared_out"), Ks, T, H,
+                                      _ptr(y, torch.bfloat16, "y"), _stream(stream)), "moe_combine_partials")
+
+
 def moe_get_status(ws, stream=None) -> int:
     """Synchronise, return and clear the device status recorded in ``ws``."""
     return int(lib().moe_get_status(_ptr(ws, name="ws"), _stream(stream)))
@@ -293,6 +333,29 @@ class Layout:
         c = moe_layout()
         for name in ("counts", "offsets", "part_rows", "part_offsets", "part_tokens", "src_pos",
                      "dst_row", "capacity_mask", "dropped"):
+            setattr(c, name, getattr(self, name).data_ptr())
+        self.c = c
+
+
+class Dedup:
+    """Device buffers of one ``moe_dedup`` (send rows of T tokens over P
+    partitions) plus its scratch and the ctypes struct."""
+
+    def __init__(self, T: int, k: int, P: int, device="cuda"):
+        s_max = max(T * min(k, P), 1)
+        i32 = dict(dtype=torch.int32, device=device)
+        self.send_offsets = torch.empty(P + 1, **i32)
+        self.send_row = torch.empty((max(T, 1), P), **i32)
+        self.send_token = torch.empty(s_max, **i32)
+        self.slot_local = torch.empty((s_max, k), **i32)
+        self.slot_gate = torch.empty((s_max, k), dtype=torch.float32, device=device)
+        n = moe_dedup_scratch_size(T, P)
+        if n == 0:
+            raise MoeError(MOE_ERR_UNSUPPORTED, "moe_dedup_scratch_size")
+        self.scratch = torch.empty((n + 15) // 16 * 16, dtype=torch.uint8, device=device)
+        self.s_max = s_max
+        c = moe_dedup()
+        for name in ("send_offsets", "send_row", "send_token", "slot_local", "slot_gate"):
             setattr(c, name, getattr(self, name).data_ptr())
         self.c = c
 

@@ -48,13 +48,24 @@ namespace {
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Sizes of the layout, dispatch and combine calls.  k may exceed E there: a
+// row of a de-duplicated receive buffer has up to k slots over the
+// partition's experts, the unused ones empty (-1).
 inline moe_status check_sizes(int T, int E, int k)
 {
     if (T < 0) return MOE_ERR_INVALID_ARG;
     if (E < 1 || E > MOE_MAX_EXPERTS) return MOE_ERR_UNSUPPORTED;
-    if (k < 1 || k > MOE_MAX_TOPK || k > E) return MOE_ERR_UNSUPPORTED;
+    if (k < 1 || k > MOE_MAX_TOPK) return MOE_ERR_UNSUPPORTED;
     if ((long long)T * k >= (1LL << 30)) return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
+}
+
+// The gate selects k distinct experts: k <= E as well.
+inline moe_status check_gate_sizes(int T, int E, int k)
+{
+    const moe_status st = check_sizes(T, E, k);
+    if (st != MOE_OK) return st;
+    return k > E ? MOE_ERR_UNSUPPORTED : MOE_OK;
 }
 
 inline moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
@@ -89,7 +100,7 @@ moe_status moe_gate(const float *logits, int T, int E, int k, int mode, int32_t 
                     float *gates, int32_t *expert_counts, double *aux_loss, double *entropy,
                     void *ws, size_t ws_bytes, moe_stream_t stream)
 {
-    moe_status st = check_sizes(T, E, k);
+    moe_status st = check_gate_sizes(T, E, k);
     if (st != MOE_OK) return st;
     if (mode != MOE_TOPK_SOFTMAX && mode != MOE_SOFTMAX_TOPK) return MOE_ERR_INVALID_ARG;
     if (!expert_counts || !aux_loss || !entropy || !ws) return MOE_ERR_INVALID_ARG;
@@ -230,7 +241,7 @@ moe_status moe_dispatch_backward(const void *d_packed, const moe_layout *L, int 
 moe_status moe_gate_backward(const float *logits, const int32_t *topk_idx, const float *d_gates, int T, int E,
                              int k, int mode, float *d_logits, void *ws, size_t ws_bytes, moe_stream_t stream)
 {
-    moe_status st = check_sizes(T, E, k);
+    moe_status st = check_gate_sizes(T, E, k);
     if (st != MOE_OK) return st;
     if (mode != MOE_TOPK_SOFTMAX && mode != MOE_SOFTMAX_TOPK) return MOE_ERR_INVALID_ARG;
     if (!ws) return MOE_ERR_INVALID_ARG;
@@ -239,6 +250,74 @@ moe_status moe_gate_backward(const float *logits, const int32_t *topk_idx, const
     if (ws_bytes < moe::kWsHeaderBytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
     return from_cuda(moe::launch_gate_backward(logits, topk_idx, d_gates, T, E, k, mode, d_logits, ws,
                                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_dedup_scratch_size(int T, int P)
+{
+    if (T < 0 || P < 1 || P > 16) return 0;
+    return moe::dedup_scratch_bytes(T, P);
+}
+
+// A layout view of the send rows: P slots per token, rows = send rows.
+static moe_layout dedup_view(const moe_dedup *D)
+{
+    moe_layout v = {};
+    v.T = D->T;
+    v.E = D->P;
+    v.k = D->P;
+    v.P = 1;
+    v.r_max = D->s_max;
+    v.ws = D->ws;
+    v.offsets = D->send_offsets;
+    v.dst_row = D->send_row;
+    return v;
+}
+
+moe_status moe_dedup_layout(const moe_layout *L, const float *gates, moe_dedup *D, void *scratch,
+                            size_t scratch_bytes, moe_stream_t stream)
+{
+    if (!L || !D) return MOE_ERR_INVALID_ARG;
+    moe_status st = check_layout(L, L->T);
+    if (st != MOE_OK) return st;
+    if (L->P < 1 || L->P > 16) return MOE_ERR_UNSUPPORTED;
+    if (!D->send_offsets || (L->T > 0 && (!gates || !scratch || !D->send_row || !D->send_token || !D->slot_local ||
+                                          !D->slot_gate)))
+        return MOE_ERR_INVALID_ARG;
+    if (L->T > 0 && scratch_bytes < moe::dedup_scratch_bytes(L->T, L->P)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    D->T = L->T;
+    D->k = L->k;
+    D->P = L->P;
+    D->s_max = L->T * (L->k < L->P ? L->k : L->P);
+    D->ws = L->ws;
+    return from_cuda(moe::launch_dedup_layout(L, gates, D, scratch, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_dispatch_dedup(const void *x, int T, int H, const moe_dedup *D, int fp8, void *send_buf,
+                              float *scales, moe_stream_t stream)
+{
+    if (!D || !D->send_offsets || D->T != T || D->P < 1 || D->P > 16) return MOE_ERR_INVALID_ARG;
+    if (fp8 != 0 && fp8 != MOE_FP8_PER_TOKEN) return MOE_ERR_UNSUPPORTED;
+    if (H < 8 || H % 8 != 0) return MOE_ERR_UNSUPPORTED;
+    if (fp8 && (H % 16 != 0 || H > MOE_MAX_H_FP8)) return MOE_ERR_UNSUPPORTED;
+    if (T > 0 && (!x || !send_buf || !D->send_row || (fp8 && !scales))) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(send_buf) || !aligned16(scales)) return MOE_ERR_INVALID_ARG;
+    const moe_layout v = dedup_view(D);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return from_cuda(fp8 ? moe::launch_dispatch_fp8_grouped(x, T, H, &v, MOE_FP8_PER_TOKEN, send_buf, scales, s)
+                         : moe::launch_dispatch_bf16(x, T, H, &v, send_buf, s));
+}
+
+moe_status moe_combine_partials(const void *partials, const moe_dedup *D, const void *shared_out, int Ks, int T,
+                                int H, void *y, moe_stream_t stream)
+{
+    if (!D || !D->send_offsets || D->T != T || D->P < 1 || D->P > 16) return MOE_ERR_INVALID_ARG;
+    if (H < 8 || H % 8 != 0) return MOE_ERR_UNSUPPORTED;
+    if (Ks < 0 || Ks > MOE_MAX_SHARED) return MOE_ERR_UNSUPPORTED;
+    if (T > 0 && (!partials || !y || !D->send_row || (Ks > 0 && !shared_out))) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(partials) || !aligned16(y) || !aligned16(shared_out)) return MOE_ERR_INVALID_ARG;
+    const moe_layout v = dedup_view(D);
+    return from_cuda(moe::launch_combine(partials, &v, nullptr, Ks > 0 ? shared_out : nullptr, Ks, T, H, y,
+                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_get_status(void *ws, moe_stream_t stream)

@@ -155,6 +155,9 @@ cudaError_t launch_combine_backward(const void *dy, const void *eo, const moe_la
                                    int H, void *d_eo, float *d_gates, cudaStream_t s);
 cudaError_t launch_gate_backward(const float *logits, const int32_t *topk_idx, const float *d_gates, int T, int E,
                                  int k, int mode, float *d_logits, void *ws, cudaStream_t s);
+size_t dedup_scratch_bytes(long long T, int P);
+cudaError_t launch_dedup_layout(const moe_layout *L, const float *gates, moe_dedup *D, void *scratch,
+                                cudaStream_t s);
 int device_sm_count();
 
 // Allow `fn` up to `bytes` of dynamic shared memory on the current device

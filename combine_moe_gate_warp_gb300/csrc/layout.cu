@@ -193,7 +193,8 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
             const int i = base + u * kLayoutThreads + tid;
             if (i < A) {
                 int e = w[u];
-                if (e < 0 || e >= E) { e = E; s_bad = 1; }
+                if (e == -1) e = E;  // empty slot
+                else if (e < 0 || e >= E) { e = E; s_bad = 1; }
                 s_idx[i] = e;
             }
         }

@@ -38,9 +38,10 @@
  * - bf16 tensors are raw 16-bit bfloat16 patterns; e4m3 codes are bytes in
  *   the OCP "E4M3FN" encoding.
  *
- * Supported range: 1 <= E <= 256, 1 <= k <= min(E, 16), 1 <= P <= E with
- * E % P == 0, 0 <= T and T*k < 2^30, H % 8 == 0 (H % 16 == 0 and
- * H <= 16384 for FP8), 0 <= Ks <= 8.  Anything else is
+ * Supported range: 1 <= E <= 256, 1 <= k <= 16 (k <= E for the gate; the
+ * layout, dispatch and combine also take k > E, for rows with empty slots),
+ * 1 <= P <= E with E % P == 0, 0 <= T and T*k < 2^30, H % 8 == 0 (H % 16 == 0
+ * and H <= 16384 for FP8), 0 <= Ks <= 8.  Anything else is
  * MOE_ERR_UNSUPPORTED; there is no fallback path.
  */
 #ifndef MOE_ROUTE_H
@@ -151,7 +152,10 @@ moe_status moe_gate(const float *logits, int T, int E, int k, int mode,
  * are taken in order and here dropped).
  *
  *   topk_idx       [T, k] int32 from moe_gate (ids outside [0, E) are
- *                  recorded as MOE_ERR_DEVICE_DATA and treated as dropped).
+ *                  recorded as MOE_ERR_DEVICE_DATA and treated as dropped;
+ *                  -1 marks an empty slot, e.g. of a de-duplicated receive
+ *                  row with fewer than k experts: no row, no error, and
+ *                  expert_counts must not count it).
  *   expert_counts  [E] int32 from moe_gate (must match topk_idx; a
  *                  mismatch is recorded as MOE_ERR_DEVICE_DATA).
  *   P              logical partitions; partition p = experts
@@ -302,6 +306,60 @@ moe_status moe_quantize_rows(const void *rows, const moe_layout *L, int H, int m
 moe_status moe_combine_fp8(const void *codes, const float *scales, const moe_layout *L,
                            const float *gates, const void *shared_out, int Ks, int T, int H,
                            void *y, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Per-partition token de-duplication ([P4] sec. 7 dispatch detail: the rows
+ * bound for one destination are packed into one block).  A token that keeps
+ * several slots in one partition is sent there once, with its local expert
+ * ids and gates; the partition expands it to its experts with
+ * moe_dispatch_layout (empty slots: id -1), moe_dispatch and the experts,
+ * combines them with moe_combine (one partial row per received token) and
+ * returns that row; the source adds the partial rows with
+ * moe_combine_partials.  Supported: P <= 16.
+ * ------------------------------------------------------------------------ */
+typedef struct moe_dedup {
+    int32_t T, k, P;         /* filled by moe_dedup_layout */
+    int32_t s_max;           /* send rows the buffers hold: T * min(k, P) (filled) */
+    void *ws;                /* the layout's workspace, for device status (filled) */
+    int32_t *send_offsets;   /* [P+1] first send row of partition p; [P] = S */
+    int32_t *send_row;       /* [T*P] send row of (t, p), -1 if t keeps no slot in p */
+    int32_t *send_token;     /* [s_max] token of each send row (rows >= S untouched) */
+    int32_t *slot_local;     /* [s_max*k] local expert ids of the row's slots, -1 past the last */
+    float *slot_gate;        /* [s_max*k] their gates, 0 past the last */
+} moe_dedup;
+
+/* Bytes of scratch moe_dedup_layout needs (0 if unsupported). */
+size_t moe_dedup_scratch_size(int T, int P);
+
+/*
+ * moe_dedup_layout -- the send rows of a layout (L from moe_dispatch_layout
+ * or moe_dispatch_layout_reassign; the final expert of a kept slot is the
+ * expert whose rows hold its dst_row).  Send rows are partition-major and,
+ * within a partition, in token order; a row's slots keep the token's slot
+ * order, with local ids (expert - p*E/P) and the gates from `gates` [T, k]
+ * (as left by the layout).  `scratch` is caller-owned device memory of
+ * moe_dedup_scratch_size(T, P) bytes.
+ */
+moe_status moe_dedup_layout(const moe_layout *L, const float *gates, moe_dedup *D,
+                            void *scratch, size_t scratch_bytes, moe_stream_t stream);
+
+/*
+ * moe_dispatch_dedup -- copy x[send_token[s]] to send row s of `send_buf`
+ * ([s_max, H] bf16, or uint8 e4m3 with per-row (scale, zero) in `scales` for
+ * fp8 = MOE_FP8_PER_TOKEN: the token's own pair, as moe_dispatch).
+ */
+moe_status moe_dispatch_dedup(const void *x, int T, int H, const moe_dedup *D, int fp8,
+                              void *send_buf, float *scales, moe_stream_t stream);
+
+/*
+ * moe_combine_partials -- y[t] = bf16 RNE of, in fp32 and this order,
+ *   acc = 0; acc = acc + partial[send_row[t,p]] for p ascending (p with a
+ *   send row); acc = acc + shared[s,t] for s ascending.
+ * partials [s_max, H] bf16: the row each partition returned for each send
+ * row (rows >= S are not read).
+ */
+moe_status moe_combine_partials(const void *partials, const moe_dedup *D, const void *shared_out,
+                                int Ks, int T, int H, void *y, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Backward of the path.  The gradients retrace the forward routing through

@@ -33,7 +33,8 @@ def test_exports_every_declared_symbol(lib):
     assert {"moe_gate", "moe_dispatch_layout", "moe_dispatch", "moe_combine", "moe_get_status",
             "moe_workspace_size", "moe_workspace_init", "moe_rows_max", "moe_status_string",
             "moe_combine_backward", "moe_dispatch_backward", "moe_gate_backward", "moe_quantize_rows",
-            "moe_combine_fp8", "moe_dispatch_layout_reassign"} <= names
+            "moe_combine_fp8", "moe_dispatch_layout_reassign", "moe_dedup_scratch_size", "moe_dedup_layout",
+            "moe_dispatch_dedup", "moe_combine_partials"} <= names
     for n in names:
         assert hasattr(lib, n), f"{n} declared but not exported"
 
@@ -47,7 +48,8 @@ def test_workspace_and_rows_queries(lib):
     assert abi.moe_rows_max(262144, 64, 8, 40960) == 2097152
     assert abi.moe_rows_max(100, 8, 2, 5) == 40
     assert abi.moe_rows_max(100, 8, 2, 0) == 200
-    assert abi.moe_rows_max(100, 8, 9, 0) == -1         # k > E
+    assert abi.moe_rows_max(100, 8, 17, 0) == -1        # k > 16
+    assert abi.moe_rows_max(100, 8, 9, 0) == 900        # k > E: rows with empty slots
 
 
 def test_argument_checks_return_before_any_cuda_call(lib):
@@ -76,6 +78,10 @@ def test_argument_checks_return_before_any_cuda_call(lib):
     assert lib.moe_gate_backward(fake, fake, fake, 10, 8, 2, 0, fake, fake, 100, None) == abi.MOE_ERR_WORKSPACE_TOO_SMALL
     assert lib.moe_gate_backward(fake, fake, fake, 10, 8, 2, 7, fake, fake, 1 << 20, None) == abi.MOE_ERR_INVALID_ARG
     assert lib.moe_gate_backward(fake, fake, fake, 10, 8, 9, 0, fake, fake, 1 << 20, None) == abi.MOE_ERR_UNSUPPORTED
+    assert lib.moe_dedup_scratch_size(100, 17) == 0 and lib.moe_dedup_scratch_size(100, 8) > 0
+    assert lib.moe_dedup_layout(None, fake, None, fake, 1 << 20, None) == abi.MOE_ERR_INVALID_ARG
+    assert lib.moe_dispatch_dedup(fake, 10, 64, None, 0, fake, None, None) == abi.MOE_ERR_INVALID_ARG
+    assert lib.moe_combine_partials(fake, None, None, 0, 10, 64, fake, None) == abi.MOE_ERR_INVALID_ARG
     assert lib.moe_get_status(None, None) == abi.MOE_ERR_INVALID_ARG
     assert lib.moe_status_string(5) == b"device wait timed out"
 
@@ -85,7 +91,8 @@ def test_binding_names_match_the_c_abi():
     for n in ("moe_gate", "moe_dispatch_layout", "moe_dispatch", "moe_combine", "moe_get_status",
               "moe_workspace_size", "moe_workspace_init", "moe_rows_max", "moe_combine_backward",
               "moe_dispatch_backward", "moe_gate_backward", "moe_quantize_rows", "moe_combine_fp8",
-              "moe_dispatch_layout_reassign"):
+              "moe_dispatch_layout_reassign", "moe_dedup_scratch_size", "moe_dedup_layout", "moe_dispatch_dedup",
+              "moe_combine_partials"):
         assert callable(getattr(abi, n))
     # the struct mirrors the header's field order
     hdr = open(os.path.join(ROOT, "include", "moe_route.h")).read()
