@@ -49,6 +49,8 @@ def parse_args():
                     help="time the step only as separate calls on one stream")
     ap.add_argument("--route-priority", choices=["high", "same"], default="high",
                     help="priority of the routing stream against the data stream")
+    ap.add_argument("--dedup-steps", type=int, default=200,
+                    help="passes of the per-partition de-duplicated send path timed after the forward (0: skip)")
     ap.add_argument("--backward-steps", type=int, default=500,
                     help="passes of the backward calls timed after the forward (0: skip)")
     return ap.parse_args()
@@ -497,6 +499,10 @@ def run_ours(args):
     if not args.no_e2e:
         e2e = time_e2e(w, shape, plan, inputs, eo, dev, world, args.e2e_steps, pipe is not None)
 
+    dd = None
+    if args.dedup_steps > 0 and 1 <= w.P <= 16:
+        dd = time_dedup(plan, w, inputs, args.dedup_steps, world, dev, stream, peak, R)
+
     bwd = None
     if args.backward_steps > 0:
         bwd = time_backward(plan, w, inputs, eo_arg, args.backward_steps, world, dev, stream, peak)
@@ -531,6 +537,7 @@ def run_ours(args):
             "e2e": e2e,
             "cpu_baseline": cpu,
             "backward": bwd,
+            "dedup": dd,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -680,6 +687,51 @@ def time_pipelined(w, shape, inputs, eo, dev, world, K, W, route_priority="high"
     return {"ms_per_step": ms,
             "note": "back-to-back batches (two alternating input batches and plans): gate + layout of "
                     "batch i on a high-priority stream overlap dispatch + combine of batch i-1"}
+
+
+def time_dedup(plan, w, inputs, steps, world, dev, stream, peak, R):
+    """The per-partition de-duplicated send path on the forward's layout:
+    moe_dedup_layout (send rows) and moe_dispatch_dedup (x copied once per
+    partition a token reaches).  Reports the send rows against the packed
+    rows (what an expert-parallel exchange would move) and the times."""
+    import torch
+
+    from combine_moe_gate_warp_gb300 import abi
+    D = abi.Dedup(w.T, w.k, w.P, dev)
+    fp8 = 1 if int(w.fp8) == 1 else 0
+    send = torch.empty((D.s_max, w.H), dtype=torch.uint8 if fp8 else torch.bfloat16, device=dev)
+    sc = torch.empty((D.s_max, 2), dtype=torch.float32, device=dev) if fp8 else None
+
+    def one(e=None):
+        if e:
+            e[0].record(stream)
+        abi.moe_dedup_layout(plan.layout, plan.gates, D, stream)
+        if e:
+            e[1].record(stream)
+        abi.moe_dispatch_dedup(inputs["x"], w.T, w.H, D, fp8, send, sc, stream)
+        if e:
+            e[2].record(stream)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    barrier(world)
+    for e in ev:
+        one(e)
+    torch.cuda.synchronize(dev)
+    st = plan.status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} in the de-duplicated path")
+    S = int(D.send_offsets[w.P].item())
+    t_lay = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev)
+    t_disp = statistics.fmean(e[1].elapsed_time(e[2]) for e in ev)
+    bt = 1 if fp8 else 2
+    disp_bytes = w.T * w.H * 2 + S * w.H * bt + (S * 8 if fp8 else 0)
+    return {"send_rows": S, "packed_rows": R, "send_over_packed": S / max(R, 1),
+            "layout_ms": t_lay, "dispatch_ms": t_disp,
+            "dispatch_gbs": disp_bytes / (t_disp * 1e-3) / 1e9,
+            "dispatch_frac": disp_bytes / (t_disp * 1e-3) / 1e9 / peak, "steps": steps}
 
 
 def time_backward(plan, w, inputs, eo_arg, steps, world, dev, stream, peak):

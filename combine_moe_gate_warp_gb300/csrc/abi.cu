@@ -7,7 +7,7 @@
 #include <mutex>
 #include <utility>
 
-#include "common.cuh"
+#include "launchers.h"
 
 namespace moe {
 

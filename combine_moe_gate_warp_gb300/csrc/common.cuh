@@ -131,33 +131,7 @@ __device__ __forceinline__ float bf16hi(unsigned w) { return __uint_as_float(w &
 
 }  // namespace moe
 
-// Host-side launchers (one per kernel family), called by the C ABI layer
-// after argument validation.  They enqueue on `s` and return the CUDA
-// launch status.
 namespace moe {
-cudaError_t launch_gate(const float *logits, int T, int E, int k, int mode, int32_t *topk_idx,
-                        float *gates, int32_t *expert_counts, double *aux, double *entropy,
-                        void *ws, cudaStream_t s);
-cudaError_t launch_layout(const int32_t *topk_idx, const int32_t *counts_in, int T, int E, int k,
-                          int P, int capacity, float *gates, const moe_layout *L, void *ws,
-                          cudaStream_t s, int reassign = 0);
-cudaError_t launch_dispatch_bf16(const void *x, int T, int H, const moe_layout *L, void *packed,
-                                 cudaStream_t s);
-cudaError_t launch_combine(const void *eo, const moe_layout *L, const float *gates,
-                           const void *shared, int Ks, int T, int H, void *y, cudaStream_t s);
-cudaError_t launch_dispatch_fp8_grouped(const void *x, int T, int H, const moe_layout *L, int mode, void *packed,
-                                        float *scales, cudaStream_t s);
-cudaError_t launch_quantize_rows(const void *rows, const moe_layout *L, int H, int mode, void *codes, float *scales,
-                                 cudaStream_t s);
-cudaError_t launch_combine_fp8(const void *codes, const float *scales, const moe_layout *L, const float *gates,
-                               const void *shared, int Ks, int T, int H, void *y, cudaStream_t s);
-cudaError_t launch_combine_backward(const void *dy, const void *eo, const moe_layout *L, const float *gates, int T,
-                                   int H, void *d_eo, float *d_gates, cudaStream_t s);
-cudaError_t launch_gate_backward(const float *logits, const int32_t *topk_idx, const float *d_gates, int T, int E,
-                                 int k, int mode, float *d_logits, void *ws, cudaStream_t s);
-size_t dedup_scratch_bytes(long long T, int P);
-cudaError_t launch_dedup_layout(const moe_layout *L, const float *gates, moe_dedup *D, void *scratch,
-                                cudaStream_t s);
 int device_sm_count();
 
 // Allow `fn` up to `bytes` of dynamic shared memory on the current device

@@ -7,7 +7,7 @@
 
 #include <mutex>
 
-#include "common.cuh"
+#include "launchers.h"
 
 namespace {
 
