@@ -245,9 +245,22 @@ def hbm_peak():
 # ---------------------------------------------------------------------------
 # CPU oracle baseline (bounded sample)
 # ---------------------------------------------------------------------------
-def oracle_sample_run(w, inputs_host, T_s):
+def _ranges(n, parts):
+    """Split [0, n) into `parts` contiguous ranges (as int64 index arrays)."""
+    import numpy as np
+    edges = np.linspace(0, n, parts + 1).astype(np.int64)
+    return [np.arange(edges[i], edges[i + 1], dtype=np.int64) for i in range(parts) if edges[i + 1] > edges[i]]
+
+
+def oracle_sample_run(w, inputs_host, T_s, threads=1):
     """Time the oracle on the first T_s tokens of the workload: gate, layout,
-    dispatch of every kept row, combine of every token.  Returns seconds."""
+    dispatch of every kept row, combine of every token.  Returns seconds.
+    With threads > 1 the per-token and per-row stages (gate, dispatch,
+    combine, the FP8 encodes) run over contiguous token / row ranges on a
+    thread pool (the C oracle releases the interpreter lock); the layout's
+    sort and the FP8 group extremes stay serial."""
+    import concurrent.futures as cf
+
     import numpy as np
 
     import oracle
@@ -256,33 +269,70 @@ def oracle_sample_run(w, inputs_host, T_s):
     cap = 0
     if w.capacity:
         cap = (5 * T_s * w.k + 4 * w.E - 1) // (4 * w.E)
+    pool = cf.ThreadPoolExecutor(max_workers=threads) if threads > 1 else None
+
+    def pmap(fn, parts):
+        return list(pool.map(fn, parts)) if pool else [fn(q) for q in parts]
+
+    def quantize(src, src_row, mode, offsets, rows):
+        group, ng = oracle.row_groups(mode, offsets, rows)
+        if mode == oracle.FP8_PER_TOKEN:
+            parts = pmap(lambda r: oracle.quantize_rows_grouped(src, src_row[r], np.arange(r.size, dtype=np.int32),
+                                                                r.size), _ranges(rows.size, threads))
+        else:
+            params = oracle.fp8_group_params(src, src_row, group, ng)
+            parts = pmap(lambda r: oracle.quantize_rows_with_params(src, src_row[r], group[r], params),
+                         _ranges(rows.size, threads))
+        if not parts:
+            return np.zeros((0, src.shape[1]), np.uint8), np.zeros((0, 2), np.float32)
+        return np.concatenate([p[0] for p in parts]), np.concatenate([p[1] for p in parts])
+
     t0 = time.perf_counter()
-    idx, g64, counts, aux, ent = oracle.gate(logits, w.k, w.mode)
+    gparts = pmap(lambda r: oracle.gate(logits[r[0]:r[-1] + 1], w.k, w.mode), _ranges(T_s, threads))
+    idx = np.concatenate([g[0] for g in gparts])
+    g64 = np.concatenate([g[1] for g in gparts])
     if w.reassign and cap:
         L = oracle.layout_reassign(idx, w.E, w.P, cap, gates_f32=g64.astype(np.float32))
     else:
         L = oracle.layout(idx, w.E, w.P, cap, gates_f32=g64.astype(np.float32))
     rows = np.arange(L["R"], dtype=np.int64)
     src_row = L["src_pos"].astype(np.int64) // w.k
-    if int(w.fp8) == 1:
-        packed, scales = oracle.dispatch_fp8_rows(x_bits, w.k, L["src_pos"], rows)
-    elif w.fp8:
-        group, ng = oracle.row_groups(int(w.fp8), L["offsets"], rows)
-        packed, scales = oracle.quantize_rows_grouped(x_bits, src_row, group, ng)
+    if w.fp8:
+        packed, scales = quantize(x_bits, src_row, int(w.fp8), L["offsets"], rows)
     else:
-        packed = oracle.dispatch_bf16_rows(x_bits, w.k, L["src_pos"], rows)
+        packed = np.concatenate(pmap(lambda r: oracle.dispatch_bf16_rows(x_bits, w.k, L["src_pos"], r),
+                                     _ranges(L["R"], threads)) or [np.zeros((0, w.H), np.uint16)])
     t1 = time.perf_counter()
     eo = packed if w.identity_experts else inputs_host["eo"][:max(L["R"], 1)]
     sh = None if inputs_host.get("shared") is None else np.ascontiguousarray(inputs_host["shared"][:, :T_s])
     t2 = time.perf_counter()
     if w.fp8_combine:
-        group, ng = oracle.row_groups(int(w.fp8_combine), L["offsets"], rows)
-        codes, sc = oracle.quantize_rows_grouped(eo, rows, group, ng)
-        oracle.combine_fp8_f32order(codes, sc, L["gates"], L["dst_row"], np.arange(T_s), T_s, w.k, sh)
+        codes, sc = quantize(eo, rows, int(w.fp8_combine), L["offsets"], rows)
+        pmap(lambda r: oracle.combine_fp8_f32order(codes, sc, L["gates"], L["dst_row"], r, T_s, w.k, sh),
+             _ranges(T_s, threads))
     else:
-        oracle.combine_f32order(eo, L["gates"], L["dst_row"], np.arange(T_s), T_s, w.k, sh)
+        pmap(lambda r: oracle.combine_f32order(eo, L["gates"], L["dst_row"], r, T_s, w.k, sh), _ranges(T_s, threads))
     t3 = time.perf_counter()
+    if pool:
+        pool.shutdown()
     return (t1 - t0) + (t3 - t2)
+
+
+def host_cpu():
+    """(usable cores, CPU model) of this host."""
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read().splitlines()
+        for key in ("model name", "CPU part"):
+            hit = [ln.split(":", 1)[1].strip() for ln in info if ln.startswith(key)]
+            if hit:
+                model = hit[0] if key == "model name" else f"Arm CPU part {hit[0]}"
+                break
+    except OSError:
+        pass
+    return cores, model or "unknown"
 
 
 HOST_EO_ROWS = 1 << 17  # cap on host copies of the seeded expert outputs
@@ -306,10 +356,18 @@ def cpu_baseline(w, inputs_host, target_s):
     while total < 0.5 * target_s and reps < 50:
         total += oracle_sample_run(w, inputs_host, T_s)
         reps += 1
-    return dict(value=T_s * reps / total, unit=UNIT, cores=1, kind="oracle",
-                sample=f"first {T_s} of {w.T} tokens of {w.name}, whole path (gate, layout, "
-                       f"dispatch of every kept row, combine of every token), {reps} pass(es), "
-                       f"{total:.1f} s single-threaded C oracle")
+    single = dict(value=T_s * reps / total, unit=UNIT, cores=1, kind="oracle",
+                  sample=f"first {T_s} of {w.T} tokens of {w.name}, whole path (gate, layout, "
+                         f"dispatch of every kept row, combine of every token), {reps} pass(es), "
+                         f"{total:.1f} s single-threaded C oracle")
+    cores, model = host_cpu()
+    if cores > 1:
+        tm = sum(oracle_sample_run(w, inputs_host, T_s, cores) for _ in range(reps))
+        single["threaded"] = dict(value=T_s * reps / tm, unit=UNIT, cores=cores, cpu=model,
+                                  sample=f"the same sample, {reps} pass(es), per-token and per-row stages over "
+                                         f"{cores} threads (token / row ranges), layout sort serial")
+    single["cpu"] = model
+    return single
 
 
 def host_inputs(w, inputs, eo):
