@@ -126,6 +126,7 @@ SMALL = [
     W["fine_shared"].scaled(333),
     W["fp8_skewed"].scaled(1500),
     W["prefill_cap"].scaled(700),
+    W["prefill_reassign"].scaled(700),  # re-assigned slots keep their gates and gradients
 ]
 
 
