@@ -39,7 +39,11 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--workload", "--config", default=DEFAULT_WORKLOAD,
+                    help="workload name, or C0..C4 for tiny, v2_top2, fine_shared, fp8_skewed, prefill_cap")
+    ap.add_argument("--seed", type=int, default=None, help="override the workload's seed")
+    ap.add_argument("--oracle-threads", type=int, default=0,
+                    help="threads of the second oracle baseline (0: every core this process may use)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
@@ -53,7 +57,10 @@ def parse_args():
                     help="passes of the per-partition de-duplicated send path timed after the forward (0: skip)")
     ap.add_argument("--backward-steps", type=int, default=500,
                     help="passes of the backward calls timed after the forward (0: skip)")
-    return ap.parse_args()
+    args = ap.parse_args()
+    aliases = {"C0": "tiny", "C1": "v2_top2", "C2": "fine_shared", "C3": "fp8_skewed", "C4": "prefill_cap"}
+    args.workload = aliases.get(args.workload, args.workload)
+    return args
 
 
 # ---------------------------------------------------------------------------
@@ -342,7 +349,7 @@ def max_sample_tokens(w):
     return w.T if w.identity_experts else min(w.T, HOST_EO_ROWS // w.k)
 
 
-def cpu_baseline(w, inputs_host, target_s):
+def cpu_baseline(w, inputs_host, target_s, threads=0):
     """Scale the token sample so that one oracle pass takes about target_s
     seconds (whole workload at most), then time it."""
     T_max = max_sample_tokens(w)
@@ -361,6 +368,8 @@ def cpu_baseline(w, inputs_host, target_s):
                          f"dispatch of every kept row, combine of every token), {reps} pass(es), "
                          f"{total:.1f} s single-threaded C oracle")
     cores, model = host_cpu()
+    if threads > 0:
+        cores = threads
     if cores > 1:
         tm = sum(oracle_sample_run(w, inputs_host, T_s, cores) for _ in range(reps))
         single["threaded"] = dict(value=T_s * reps / tm, unit=UNIT, cores=cores, cpu=model,
@@ -414,6 +423,8 @@ def run_reference(args):
 
     from combine_moe_gate_warp_gb300 import workloads
     w = workloads.WORKLOADS[args.workload]
+    if args.seed is not None:
+        w = workloads.Workload(**{**w.__dict__, "seed": args.seed})
     inputs = workloads.make_inputs(w, "cpu")
     hi = dict(logits=inputs["logits"].numpy(),
               x=inputs["x"].view(torch.int16).numpy().view(np.uint16))
@@ -460,6 +471,8 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     build()
     base = workloads.WORKLOADS[args.workload]
+    if args.seed is not None:
+        base = workloads.Workload(**{**base.__dict__, "seed": args.seed})
     w = rank_workload(base, rank)
 
     inputs = workloads.make_inputs(w, dev)
@@ -513,8 +526,10 @@ def run_ours(args):
             plan.step(inputs["logits"], inputs["x"], eo_arg, inputs["shared"])
             continue
         e[0].record(stream)
-        for j, (_, fn) in enumerate(calls):
+        for j, (n, fn) in enumerate(calls):
+            torch.cuda.nvtx.range_push(n)
             fn()
+            torch.cuda.nvtx.range_pop()
             e[j + 1].record(stream)
     stop.record(stream)
     torch.cuda.synchronize(dev)
@@ -587,7 +602,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, host_inputs(w, inputs, eo), args.cpu_seconds)
+        cpu = cpu_baseline(w, host_inputs(w, inputs, eo), args.cpu_seconds, args.oracle_threads)
 
     clocks = (sampler.summary(t_pw0, t_pw1) if pipe else sampler.summary(t_wall0, t_wall1)) if sampler else None
     if rank == 0:

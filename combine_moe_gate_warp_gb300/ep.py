@@ -60,9 +60,13 @@ class ExpertParallelExchange:
         FP8 scales, if given).  Returns (received rows, received scales or
         None, recv_counts [W, E/W])."""
         send_splits = self._send_splits(counts)
+        R = sum(send_splits)
+        if packed.shape[0] < R or (scales is not None and scales.shape[0] < R):
+            # refuse before any collective: the peers see this rank fail
+            # (the process group's timeout ends their pending exchange)
+            raise ValueError(f"packed buffer holds {packed.shape[0]} rows, the counts send {R}")
         recv_counts = self.exchange_counts(counts)
         recv_splits = recv_counts.sum(1).tolist()
-        R = sum(send_splits)
         recv = packed.new_empty((sum(recv_splits),) + tuple(packed.shape[1:]))
         dist.all_to_all_single(recv, packed[:R].contiguous(), recv_splits, send_splits, group=self.group)
         recv_scales = None
@@ -92,6 +96,8 @@ class ExpertParallelExchange:
         back_send = recv_counts.sum(1).tolist()
         back_recv = self._send_splits(counts)
         R = sum(back_recv)
+        if expert_out_recv.shape[0] != sum(back_send):
+            raise ValueError(f"{expert_out_recv.shape[0]} expert-output rows for {sum(back_send)} received rows")
         if out is None:
             out = expert_out_recv.new_empty((R,) + tuple(expert_out_recv.shape[1:]))
         dist.all_to_all_single(out[:R], expert_out_recv.contiguous(), back_recv, back_send, group=self.group)

@@ -44,11 +44,27 @@ def gate_with_oracle(w, plan, logits: torch.Tensor):
     return gates_pre, og
 
 
+def poison(plan):
+    """Fill every output buffer of a plan with 0xFF bytes, so that a row or
+    entry the path fails to write cannot match the oracle by accident."""
+    bufs = [plan.topk_idx, plan.gates, plan.expert_counts, plan.aux_loss, plan.entropy, plan.packed, plan.y]
+    lay = plan.layout
+    bufs += [lay.counts, lay.offsets, lay.part_rows, lay.part_offsets, lay.part_tokens, lay.src_pos, lay.dst_row,
+             lay.capacity_mask, lay.dropped]
+    for name in ("scales", "eo_codes", "eo_scales"):
+        t = getattr(plan, name, None)
+        if t is not None:
+            bufs.append(t)
+    for t in bufs:
+        t.view(torch.uint8).fill_(0xFF)
+
+
 def run_gpu(w: workloads.Workload, inputs: dict, device="cuda"):
-    """The path on the GPU.  Returns the plan, the GPU's gate weights, the
-    oracle's gate outputs, R, the expert outputs used by the combine and the
-    device status."""
+    """The path on the GPU (outputs poisoned first).  Returns the plan, the
+    GPU's gate weights, the oracle's gate outputs, R, the expert outputs used
+    by the combine and the device status."""
     plan = RoutePlan(shape_of(w), device)
+    poison(plan)
     gates_pre, og = gate_with_oracle(w, plan, inputs["logits"])
     plan.dispatch_layout()
     plan.dispatch(inputs["x"])
@@ -227,4 +243,4 @@ def route_checked(w, plan, logits):
 
 __all__ = ["bits", "f_of_bits", "shape_of", "gate_with_oracle", "run_gpu", "check_gate", "check_layout",
            "sample_rows", "oracle_fp8_rows", "check_dispatch", "oracle_expert_rows", "check_combine",
-           "route_checked", "abi"]
+           "route_checked", "abi", "poison"]

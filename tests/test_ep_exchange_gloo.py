@@ -104,3 +104,44 @@ def test_expert_parallel_exchange(tmp_path, oracle, world, cap, fp8):
         assert np.array_equal(r["y"], r["y_ref"]), "combine after the exchange differs"
     # every row a rank sent was received by someone: totals match
     assert sum(int(r["recv_counts"].sum()) for r in res) == sum(int(r["R"]) for r in res)
+
+
+def _short_worker(rank, world, port, out_dir):
+    """Rank 1 hands the exchange a packed buffer shorter than its counts: it
+    must refuse before any collective, and rank 0's exchange must end with
+    an error (the process group's short timeout), not hang."""
+    import datetime
+    import sys
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    import torch.distributed as dist
+    from combine_moe_gate_warp_gb300.ep import ExpertParallelExchange
+    dist.init_process_group("gloo", rank=rank, world_size=world, timeout=datetime.timedelta(seconds=5))
+    ex = ExpertParallelExchange(8, 2)
+    counts = torch.tensor([3, 1, 2, 2, 0, 4, 1, 1], dtype=torch.int32)
+    packed = torch.zeros((14 if rank == 0 else 9, 16), dtype=torch.bfloat16)
+    err = "none"
+    try:
+        ex.dispatch(packed, counts)
+    except ValueError as e:
+        err = "refused: " + str(e)
+    except Exception as e:  # the peer's collective ends with the group's timeout
+        err = "failed: " + type(e).__name__
+    with open(os.path.join(out_dir, f"s{rank}.txt"), "w") as f:
+        f.write(err)
+    os._exit(0)
+
+
+def test_short_send_is_refused_and_the_peer_fails(tmp_path):
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    procs = [ctx.Process(target=_short_worker, args=(r, 2, port, str(tmp_path))) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    r0 = (tmp_path / "s0.txt").read_text()
+    r1 = (tmp_path / "s1.txt").read_text()
+    assert r1.startswith("refused"), r1
+    assert r0.startswith("failed"), r0
