@@ -848,6 +848,7 @@ def time_backward(plan, w, inputs, eo_arg, steps, world, dev, stream, peak):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
     barrier(world)
     torch.cuda.synchronize(dev)
+    torch.cuda.nvtx.range_push("backward")  # a profiler can select these launches by range
     for e in ev:
         e[0].record(stream)
         plan.combine_backward(dy, eo_arg)
@@ -856,6 +857,7 @@ def time_backward(plan, w, inputs, eo_arg, steps, world, dev, stream, peak):
         e[2].record(stream)
         plan.dispatch_backward(dp)
         e[3].record(stream)
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize(dev)
     per = {n: statistics.fmean(e[j].elapsed_time(e[j + 1]) for e in ev) for j, n in enumerate(names)}
     # whole backward without events between the kernels

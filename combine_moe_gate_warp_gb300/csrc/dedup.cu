@@ -15,7 +15,8 @@
 // Design (sm_103a): three short launches over tiles of tokens (every token
 // is read by one thread: k dst_row words, a binary search of the layout
 // offsets held in shared memory):
-//   1. dedup_count_kernel: per tile, tokens per partition (shared atomics);
+//   1. dedup_count_kernel: per tile, tokens per partition (a ballot and a
+//      shared atomic per warp and partition);
 //   2. dedup_scan_kernel: one block scans the tile counts per partition and
 //      the partition totals;
 //   3. dedup_write_kernel: per tile, rounds of 256 tokens; the rank of a
@@ -90,11 +91,19 @@ __global__ void __launch_bounds__(kDedupThreads) dedup_count_kernel(DedupArgs a)
     const int rows_valid = load_offsets(a, s_off);
     const long long t0 = (long long)blockIdx.x * kDedupTile;
     const long long t1 = min(a.T, t0 + kDedupTile);
-    for (long long t = t0 + threadIdx.x; t < t1; t += kDedupThreads) {
-        unsigned long long m = token_mask(a, s_off, rows_valid, t);
-        while (m) {
-            atomicAdd(&s_cnt[__ffsll((long long)m) - 1], 1);
-            m &= m - 1ull;
+    const int lane = threadIdx.x & 31;
+    for (long long tb = t0; tb < t1; tb += kDedupThreads) {
+        const long long t = tb + threadIdx.x;
+        const unsigned long long m = t < t1 ? token_mask(a, s_off, rows_valid, t) : 0ull;
+        // one ballot and one shared atomic per partition the warp reaches
+        const unsigned lo = __reduce_or_sync(0xffffffffu, (unsigned)m);
+        const unsigned hi = __reduce_or_sync(0xffffffffu, (unsigned)(m >> 32));
+        unsigned long long wm = ((unsigned long long)hi << 32) | lo;
+        while (wm) {
+            const int p = __ffsll((long long)wm) - 1;
+            wm &= wm - 1ull;
+            const unsigned b = __ballot_sync(0xffffffffu, (unsigned)(m >> p) & 1u);
+            if (lane == 0) atomicAdd(&s_cnt[p], __popc(b));
         }
     }
     __syncthreads();

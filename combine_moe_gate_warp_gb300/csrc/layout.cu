@@ -20,16 +20,17 @@
 //      expert) carries an epoch tag, a state (aggregate / inclusive prefix)
 //      and the 30-bit value, so no flag array ever needs clearing.  The
 //      whole block looks back at once: 256/E threads per expert each read
-//      four predecessors' words per round, so a round covers 1024/E tiles
-//      for every expert with a single memory round trip.  Every wait is
+//      and reduce 16 consecutive predecessors' words per round, so a round
+//      covers 4096/E tiles for every expert with a single memory round
+//      trip.  Every wait is
 //      bounded by %globaltimer and records MOE_ERR_TIMEOUT instead of
 //      hanging.
 //   4. Rank r = prefix + warp offset + local rank; kept iff r < capacity;
 //      dst_row / src_pos / capacity_mask written, dropped gates zeroed.
 //   5. Distinct-partition tokens: a kept assignment counts when no earlier
-//      kept slot of its token falls in the same partition; warp-aggregated,
-//      then summed over tiles with integer atomics; the last block to finish
-//      publishes them.  Output stores come last, after the completion
+//      kept slot of its token falls in the same partition; aggregated per
+//      warp (ballot per partition), then summed over tiles with integer
+//      atomics; the last block to finish publishes them.  Output stores come last, after the completion
 //      ticket, so no fence waits behind them.
 #include "common.cuh"
 
@@ -37,7 +38,7 @@ namespace moe {
 namespace {
 
 constexpr int kLoadBatch = 8;  // expert-id loads in flight per thread
-constexpr int kLookPer = 4;    // look-back words read per thread per round
+constexpr int kLookPer = 16;   // look-back words read per thread per round
 constexpr int kSpecLoads = kLoadBatch;  // ids of the guessed tile fetched before the tile id is known
 
 struct LayoutArgs {
@@ -106,6 +107,23 @@ __device__ __forceinline__ void st_volatile_u64(unsigned long long *p, unsigned 
     *reinterpret_cast<volatile unsigned long long *>(p) = v;
 }
 
+// Add the warp's tokens per partition to s_ptok: one ballot and one shared
+// atomic per partition that some lane of the warp reaches (P <= 64), not
+// one atomic per (token, partition) on the same few words.  Every lane of
+// the warp calls it.
+__device__ __forceinline__ void count_partition_tokens(unsigned *s_ptok, unsigned long long pmask, int lane)
+{
+    const unsigned lo = __reduce_or_sync(0xffffffffu, (unsigned)pmask);
+    const unsigned hi = __reduce_or_sync(0xffffffffu, (unsigned)(pmask >> 32));
+    unsigned long long wm = ((unsigned long long)hi << 32) | lo;
+    while (wm) {
+        const int p = __ffsll((long long)wm) - 1;
+        wm &= wm - 1ull;
+        const unsigned b = __ballot_sync(0xffffffffu, (unsigned)(pmask >> p) & 1u);
+        if (lane == 0) atomicAdd(&s_ptok[p], (unsigned)__popc(b));
+    }
+}
+
 __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
 {
     extern __shared__ int s_dyn[];   // s_idx[tile assignments], s_rank[tile assignments]
@@ -115,7 +133,8 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
     __shared__ int s_base[MOE_MAX_EXPERTS];
     __shared__ unsigned s_ptok[MOE_MAX_EXPERTS];
     __shared__ int s_epart[MOE_MAX_EXPERTS];  // partition of each expert
-    __shared__ unsigned long long s_win[kLookPer * kLayoutThreads];
+    __shared__ unsigned s_part_add[kLayoutThreads];  // look-back segment sums
+    __shared__ int s_part_use[kLayoutThreads];       // words used | stop << 8
     __shared__ unsigned s_warp_tot[kLayoutWarps];
     __shared__ unsigned s_tile, s_epoch;
     __shared__ int s_last, s_bad, s_skip, s_abort;
@@ -340,24 +359,43 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
     }
     __syncthreads();
 
-    // 3. block-wide decoupled look-back: each round, thread (e, w) reads the
-    // flag words of kLookPer predecessors of expert e, so a round covers
-    // kLookPer * 256/E tiles per expert with one memory round trip
+    // 3. block-wide decoupled look-back.  Thread (e = tid % E, w = tid / E),
+    // w < W = 256/E, reads kLookPer consecutive predecessors of expert e
+    // (coalesced across e) and walks them itself: the sum of the aggregates
+    // up to its first inclusive prefix or its first word not yet published.
+    // One thread per expert then joins the W segments in order, so a round
+    // covers W * kLookPer tiles for every expert with one memory round trip.
     {
         const int W = kLayoutThreads / E;  // threads per expert
-        const int my_e = tid / W, my_w = tid - (tid / W) * W;
+        const int my_e = tid % E, my_w = tid / E;
         unsigned long long t_start = 0;
         while (true) {
-            if (my_e < E) {
+            if (my_w < W) {
                 const int b = s_base[my_e];
                 if (b >= 0) {
+                    unsigned long long f[kLookPer];
 #pragma unroll
                     for (int q = 0; q < kLookPer; ++q) {
-                        const int p = b - (q * W + my_w);
-                        s_win[q * kLayoutThreads + tid] =
-                            (p >= 0) ? ld_volatile_u64(flags + (size_t)p * E + my_e)
-                                     : make_flag(epoch, kFlagInclusive, 0u);
+                        const int p = b - (my_w * kLookPer + q);
+                        f[q] = (p >= 0) ? ld_volatile_u64(flags + (size_t)p * E + my_e)
+                                        : make_flag(epoch, kFlagInclusive, 0u);
                     }
+                    unsigned add = 0;
+                    int used = 0, stop = 0;  // stop: 1 = not published yet, 2 = inclusive prefix
+#pragma unroll
+                    for (int q = 0; q < kLookPer; ++q) {
+                        if (stop) continue;
+                        const unsigned state = (unsigned)(f[q] >> 30) & 3u;
+                        if ((unsigned)(f[q] >> 32) != epoch || state == 0u) {
+                            stop = 1;
+                        } else {
+                            add += (unsigned)(f[q] & 0x3FFFFFFFull);
+                            ++used;
+                            if (state == (unsigned)kFlagInclusive) stop = 2;
+                        }
+                    }
+                    s_part_add[tid] = add;
+                    s_part_use[tid] = used | (stop << 8);
                 }
             }
             __syncthreads();
@@ -366,15 +404,12 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
                 unsigned add = 0;
                 int used = 0;
                 bool done = false;
-                for (int q = 0; q < kLookPer && !done; ++q) {
-                    for (int w = 0; w < W; ++w) {
-                        const unsigned long long f = s_win[q * kLayoutThreads + tid * W + w];
-                        const unsigned state = (unsigned)(f >> 30) & 3u;
-                        if ((unsigned)(f >> 32) != epoch || state == 0u) { q = kLookPer; break; }  // not published yet
-                        add += (unsigned)(f & 0x3FFFFFFFull);
-                        ++used;
-                        if (state == (unsigned)kFlagInclusive) { done = true; break; }
-                    }
+                for (int w = 0; w < W; ++w) {
+                    const int u = s_part_use[w * E + tid];
+                    add += s_part_add[w * E + tid];
+                    used += u & 0xFF;
+                    if ((u >> 8) == 2) { done = true; break; }
+                    if ((u >> 8) == 1) break;
                 }
                 s_excl[tid] += add;
                 s_base[tid] = done ? -1 : s_base[tid] - used;
@@ -451,6 +486,7 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
                 ctot += s_cscan[w2];
             }
             long long m = base + wbase + incl - nov;
+            unsigned long long pmask = 0ull;
             if (tl < ntok) {
                 int fe[MOE_MAX_TOPK];
                 for (int j = 0; j < k; ++j) {
@@ -488,19 +524,25 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
                 for (int j = 0; j < k; ++j) {
                     if (fe[j] < 0) continue;
                     const int p = s_epart[fe[j]];
+                    if (a.P <= 64) {
+                        pmask |= 1ull << p;
+                        continue;
+                    }
                     bool first = true;
                     for (int jj = 0; jj < j; ++jj)
                         if (fe[jj] >= 0 && s_epart[fe[jj]] == p) { first = false; break; }
                     if (first) atomicAdd(&s_ptok[p], 1u);
                 }
             }
+            count_partition_tokens(s_ptok, pmask, lane);
             base += ctot;
             __syncthreads();  // s_cscan is rewritten by the next chunk
         }
     } else
-    for (int tl = tid; tl < ntok; tl += kLayoutThreads) {
+    for (int tb = 0; tb < ntok; tb += kLayoutThreads) {
+        const int tl = tb + tid;
         unsigned long long pmask = 0ull;
-        for (int j = 0; j < k; ++j) {
+        for (int j = 0; tl < ntok && j < k; ++j) {
             const int i = tl * k + j;
             const int e = s_idx[i];
             int row = -1;
@@ -528,11 +570,7 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a)
                 }
             }
         }
-        while (pmask) {
-            const int p = __ffsll((long long)pmask) - 1;
-            pmask &= pmask - 1;
-            atomicAdd(&s_ptok[p], 1u);
-        }
+        count_partition_tokens(s_ptok, pmask, lane);
     }
     __syncthreads();
     for (int p = tid; p < a.P; p += kLayoutThreads)

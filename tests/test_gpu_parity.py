@@ -127,6 +127,42 @@ def test_ties_and_signed_zeros():
     _run_with_logits(w, logits)
 
 
+# Gate shapes for every way the lanes of a token split its logits: several
+# lanes per token with power-of-two and other k (bitonic and insertion
+# merges), more than one batch of loads per lane, 16-byte loads with one
+# lane (E % 8 != 0), 4-byte loads (E % 4 != 0), and many tiles per block.
+LANE_SPLITS = [
+    _custom(3001, 16, 96, 6, 8),                # 4 lanes, 24 logits each, k = 6
+    _custom(1201, 16, 256, 5, 8, mode=1),       # 8 lanes, two batches, softmax over all E
+    _custom(999, 16, 20, 3, 4),                 # one lane, 16-byte loads, ragged batch
+    _custom(777, 16, 6, 2, 2, mode=1),          # one lane, 4-byte loads
+    _custom(200003, 16, 64, 2, 8),              # more tokens than resident lanes
+]
+
+
+@pytest.mark.parametrize("w", LANE_SPLITS, ids=[w.name for w in LANE_SPLITS])
+@pytest.mark.parametrize("ties", [False, True])
+def test_gate_lane_splits(w, ties):
+    if ties:
+        g = torch.Generator(device="cuda").manual_seed(w.E)
+        logits = torch.randint(-2, 3, (w.T, w.E), generator=g, device="cuda").float()
+        logits[torch.rand((w.T, w.E), generator=g, device="cuda") < 0.2] = -0.0
+    else:
+        logits = workloads.make_inputs(w, "cuda")["logits"]
+    _run_with_logits(w, logits)
+
+
+def test_ties_many_lanes():
+    """Integer logits with signed zeros where 4 and 8 lanes share a token:
+    equal values cross lanes in the merge."""
+    for E, k in ((64, 8), (256, 16), (128, 4)):
+        w = _custom(513, 16, E, k, 8)
+        g = torch.Generator(device="cuda").manual_seed(k)
+        logits = torch.randint(-1, 2, (w.T, w.E), generator=g, device="cuda").float()
+        logits[torch.rand((w.T, w.E), generator=g, device="cuda") < 0.3] = -0.0
+        _run_with_logits(w, logits)
+
+
 class _with_capacity:
     """A workload view with an explicit capacity (the capacity property of
     Workload is derived from its factor)."""
