@@ -60,6 +60,8 @@ EDGES = [
     _edge(64, 16384, 8, 2, 2, 3, 3),                   # longest rows
     _edge(3000, 32, 16, 4, 4, 2, 3, cap=1.25, zipf_bias=True, logit_std=3.0),  # tokens with no kept slot
     _edge(600, 48, 8, 1, 1, 3, 1),                     # k = 1, ragged 16-column groups
+    _edge(333, 80, 8, 2, 4, 1, 1, Ks=2),               # shared experts, 5 groups per row
+    _edge(200, 528, 8, 2, 4, 1, 1, Ks=1),              # 33 groups: a full span and a one-group span
 ]
 
 
