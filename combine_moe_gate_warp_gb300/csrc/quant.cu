@@ -306,13 +306,17 @@ fp8_encode_kernel(EncArgs a)
                 const float2 par = MODE == MOE_FP8_PER_TOKEN ? par_tok : s_par[g];
                 const float rcp = e4m3_rcp(par.x);
                 // the run's rows, gathered by every lane before the column loop
-                // (whose trip count differs between lanes: no warp collective in it)
+                // (whose trip count differs between lanes: no warp collective in
+                // it).  nr is warp-uniform; both loops stay unrolled so run[]
+                // lives in registers, and leave after nr rows instead of
+                // predicating all 16 (16 compares and addresses per 16 codes)
                 int run[MOE_MAX_TOPK];
                 const int nr = __popc(same);
                 unsigned m = same;
 #pragma unroll
                 for (int j = 0; j < MOE_MAX_TOPK; ++j) {
-                    run[j] = __shfl_sync(0xffffffffu, r, m ? __ffs(m) - 1 : 0);
+                    if (j >= nr) break;
+                    run[j] = __shfl_sync(0xffffffffu, r, __ffs(m) - 1);
                     m &= m - 1u;
                 }
                 for (int q = lane; q < a.npairs; q += 32) {
@@ -320,8 +324,10 @@ fp8_encode_kernel(EncArgs a)
                                         ? make_uint4(0u, 0u, 0u, 0u)
                                         : quant16(lds_v4(row + 32 * q), lds_v4(row + 32 * q + 16), par.y, par.x, rcp);
 #pragma unroll
-                    for (int j = 0; j < MOE_MAX_TOPK; ++j)
-                        if (j < nr) st_v4(a.out + (long long)run[j] * a.npairs + q, c);
+                    for (int j = 0; j < MOE_MAX_TOPK; ++j) {
+                        if (j >= nr) break;
+                        st_v4(a.out + (long long)run[j] * a.npairs + q, c);
+                    }
                 }
                 if ((same >> lane) & 1u) a.scales[r] = par;
             }
