@@ -42,6 +42,8 @@ def parse_args():
     ap.add_argument("--workload", "--config", default=DEFAULT_WORKLOAD,
                     help="workload name, or C0..C4 for tiny, v2_top2, fine_shared, fp8_skewed, prefill_cap")
     ap.add_argument("--seed", type=int, default=None, help="override the workload's seed")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override the workload's token count (a smaller case of the same shape, e.g. to profile)")
     ap.add_argument("--oracle-threads", type=int, default=0,
                     help="threads of the second oracle baseline (0: every core this process may use)")
     ap.add_argument("--e2e-steps", type=int, default=20)
@@ -61,6 +63,17 @@ def parse_args():
     aliases = {"C0": "tiny", "C1": "v2_top2", "C2": "fine_shared", "C3": "fp8_skewed", "C4": "prefill_cap"}
     args.workload = aliases.get(args.workload, args.workload)
     return args
+
+
+def resolve_workload(args):
+    """The named workload with the --seed and --tokens overrides applied."""
+    from combine_moe_gate_warp_gb300 import workloads
+    w = workloads.WORKLOADS[args.workload]
+    if args.seed is not None:
+        w = workloads.Workload(**{**w.__dict__, "seed": args.seed})
+    if args.tokens is not None:
+        w = w.scaled(args.tokens)
+    return w
 
 
 # ---------------------------------------------------------------------------
@@ -422,9 +435,7 @@ def run_reference(args):
     import torch
 
     from combine_moe_gate_warp_gb300 import workloads
-    w = workloads.WORKLOADS[args.workload]
-    if args.seed is not None:
-        w = workloads.Workload(**{**w.__dict__, "seed": args.seed})
+    w = resolve_workload(args)
     inputs = workloads.make_inputs(w, "cpu")
     hi = dict(logits=inputs["logits"].numpy(),
               x=inputs["x"].view(torch.int16).numpy().view(np.uint16))
@@ -470,10 +481,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     build()
-    base = workloads.WORKLOADS[args.workload]
-    if args.seed is not None:
-        base = workloads.Workload(**{**base.__dict__, "seed": args.seed})
-    w = rank_workload(base, rank)
+    w = rank_workload(resolve_workload(args), rank)
 
     inputs = workloads.make_inputs(w, dev)
     shape = RouteShape(T=w.T, H=w.H, E=w.E, k=w.k, P=w.P, mode=w.mode, fp8=int(w.fp8), Ks=w.Ks,
