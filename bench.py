@@ -52,7 +52,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-pipeline", action="store_true",
-                    help="time the step only as separate calls on one stream")
+                    help="do not time the back-to-back batches of RoutePipeline")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="do not time the step captured as a CUDA graph (RouteGraph)")
     ap.add_argument("--route-priority", choices=["high", "same"], default="high",
                     help="priority of the routing stream against the data stream")
     ap.add_argument("--dedup-steps", type=int, default=200,
@@ -555,6 +557,11 @@ def run_ours(args):
         t_pw0 = time.time()
         pipe = time_pipelined(w, shape, inputs, eo, dev, world, K, max(3, args.warmup), args.route_priority)
         t_pw1 = time.time()
+    graph = None
+    if not args.no_graph:
+        t_gw0 = time.time()
+        graph = time_graph(w, shape, inputs, eo, dev, world, K, max(3, args.warmup))
+        t_gw1 = time.time()
     if sampler:
         time.sleep(0.25)
         sampler.stop()
@@ -591,7 +598,15 @@ def run_ours(args):
                    "tokens_per_s": world * w.T * K / (elapsed_ms * 1e-3),
                    "hbm_frac": by["roofline_step"] / (ms_step_serial * 1e-3) / 1e9 / peak,
                    "note": "the calls of each step on one stream, one batch after another"}
-    ms_step = pipe["ms_per_step"] if pipe else ms_step_serial
+    # the headline is the fastest of the product's ways to run the same steps
+    modes = [(ms_step_serial, unpipelined["note"], (t_wall0, t_wall1))]
+    if pipe:
+        modes.append((pipe["ms_per_step"], pipe["note"], (t_pw0, t_pw1)))
+    if graph:
+        modes.append((graph["ms_per_step"], graph["note"], (t_gw0, t_gw1)))
+        graph["tokens_per_s"] = world * w.T / (graph["ms_per_step"] * 1e-3)
+        graph["hbm_frac"] = by["roofline_step"] / (graph["ms_per_step"] * 1e-3) / 1e9 / peak
+    ms_step, execution, (t_h0, t_h1) = min(modes, key=lambda m: m[0])
     tokens_per_s = world * w.T / (ms_step * 1e-3)
     step_gbs = by["roofline_step"] / (ms_step * 1e-3) / 1e9
 
@@ -612,7 +627,7 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, host_inputs(w, inputs, eo), args.cpu_seconds, args.oracle_threads)
 
-    clocks = (sampler.summary(t_pw0, t_pw1) if pipe else sampler.summary(t_wall0, t_wall1)) if sampler else None
+    clocks = sampler.summary(t_h0, t_h1) if sampler else None
     if rank == 0:
         line = {
             "metric": METRIC, "value": tokens_per_s, "unit": UNIT, "n_gpus": world, "steps": K,
@@ -634,8 +649,9 @@ def run_ours(args):
             "kernels_gbs": {n: by[n] / (per[n] * 1e-3) / 1e9 for n in names},
             "step_ms_evented": {"median": statistics.median(step_samples), "min": step_samples[0],
                                 "note": "sampled steps with events between the calls"},
-            "execution": (pipe["note"] if pipe else unpipelined["note"]),
+            "execution": execution,
             "unpipelined": unpipelined,
+            "graph": graph,
             "gpu_launches": plan.launches_per_step() * K,
             "clocks": clocks,
             "e2e": e2e,
@@ -791,6 +807,40 @@ def time_pipelined(w, shape, inputs, eo, dev, world, K, W, route_priority="high"
     return {"ms_per_step": ms,
             "note": "back-to-back batches (two alternating input batches and plans): gate + layout of "
                     "batch i on a high-priority stream overlap dispatch + combine of batch i-1"}
+
+
+def time_graph(w, shape, inputs, eo, dev, world, K, W):
+    """K replays of the one-stream step captured as a CUDA graph
+    (RouteGraph): inputs loaded into the graph's buffers once, then
+    replayed back to back between two events on the graph's stream."""
+    import torch
+
+    from combine_moe_gate_warp_gb300 import RouteGraph
+    g = RouteGraph(shape, dev)
+    g.step(inputs["logits"], inputs["x"], eo, inputs["shared"])
+    for _ in range(W):
+        g.replay()
+    torch.cuda.synchronize(dev)
+    st = g.status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the graph warm-up")
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    start.record(g.stream)
+    for _ in range(K):
+        g.replay()
+    stop.record(g.stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    ms = max_over_ranks(start.elapsed_time(stop), world, dev) / K
+    st = g.status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} during the graph replays")
+    return {"ms_per_step": ms, "launches_per_step": g.launches_per_step(),
+            "note": "the calls of each step on one stream, captured once as a CUDA graph and replayed"
+                    + (" (identity experts: the graph's expert-output buffer stands in for the packed rows)"
+                       if eo is None else "")}
 
 
 def time_dedup(plan, w, inputs, steps, world, dev, stream, peak, R):

@@ -215,6 +215,71 @@ class RoutePlan:
         return abi.moe_get_status(self.ws, self.stream)
 
 
+class RouteGraph:
+    """The one-stream step captured once as a CUDA graph and replayed.
+
+    For small batches the host cost of the step's foreign calls (one per
+    kernel) exceeds the kernels' own time; a replay submits every kernel of
+    the step in one launch.  The graph reads its inputs from fixed buffers
+    (``logits``, ``x``, ``expert_out`` [r_max, H], ``shared_out``) and leaves
+    its results in ``plan`` exactly as ``RoutePlan.step`` does; ``step``
+    copies new inputs in and replays.  The graph runs on its own stream;
+    ``step`` orders it after the caller's current stream and the caller's
+    stream after it.  Every kernel runs once before the capture, outside it:
+    per-kernel attributes and occupancy are set up on first use, which a
+    capture may not do."""
+
+    def __init__(self, shape: RouteShape, device="cuda"):
+        self.device = torch.device(device)
+        self.stream = torch.cuda.Stream(self.device)
+        self.plan = p = RoutePlan(shape, self.device, stream=self.stream)
+        s = shape
+        bf16 = dict(dtype=torch.bfloat16, device=self.device)
+        self.logits = torch.zeros((s.T, s.E), dtype=torch.float32, device=self.device)
+        self.x = torch.zeros((s.T, s.H), **bf16)
+        self.expert_out = torch.zeros((max(p.r_max, 1), s.H), **bf16)
+        self.shared_out = torch.zeros((s.Ks, s.T, s.H), **bf16) if s.Ks else None
+        self.stream.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(self.stream):
+            self._calls()
+        self.stream.synchronize()
+        st = p.status()
+        if st != abi.MOE_OK:
+            raise abi.MoeError(st, "RouteGraph warm-up")
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=self.stream):
+            self._calls()
+
+    def _calls(self):
+        self.plan.step(self.logits, self.x, self.expert_out, self.shared_out)
+
+    def replay(self):
+        """Replay on the graph's stream (inputs already in the buffers)."""
+        with torch.cuda.stream(self.stream):
+            self.graph.replay()
+
+    def step(self, logits=None, x=None, expert_out=None, shared_out=None) -> RoutePlan:
+        """Copy the given inputs into the graph's buffers and replay; returns
+        the plan holding the results."""
+        cur = torch.cuda.current_stream(self.device)
+        self.stream.wait_stream(cur)
+        with torch.cuda.stream(self.stream):
+            for src, dst in ((logits, self.logits), (x, self.x), (shared_out, self.shared_out)):
+                if src is not None:
+                    dst.copy_(src, non_blocking=True)
+            if expert_out is not None:
+                self.expert_out[:expert_out.shape[0]].copy_(expert_out, non_blocking=True)
+            self.graph.replay()
+        cur.wait_stream(self.stream)
+        return self.plan
+
+    def launches_per_step(self) -> int:
+        return self.plan.launches_per_step()
+
+    def status(self) -> int:
+        return self.plan.status()
+
+
 class RoutePipeline:
     """Back-to-back batches with the routing of one overlapping the data
     movement of the previous one ("MoE data traits ... DeepEP and MoE
