@@ -3,8 +3,10 @@
 // they are bad) and then launches the kernels of one step on `stream`.
 #include <stdint.h>
 
+#include <atomic>
 #include <map>
 #include <mutex>
+#include <tuple>
 #include <utility>
 
 #include "launchers.h"
@@ -13,16 +15,36 @@ namespace moe {
 
 int device_sm_count()
 {
-    static int cached[64] = {0};
+    static std::atomic<int> cached[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-    if (cached[dev] == 0) {
-        int n = 0;
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
             n = 148;
-        cached[dev] = n;
+        cached[dev].store(n, std::memory_order_relaxed);
     }
-    return cached[dev];
+    return n;
+}
+
+int resident_grid(const void *fn, int threads, size_t smem)
+{
+    static std::mutex mu;
+    static std::map<std::tuple<const void *, int, size_t, int>, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const auto key = std::make_tuple(fn, threads, smem, dev);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem) != cudaSuccess || n < 1) n = 1;
+    const int grid = n * device_sm_count();
+    std::lock_guard<std::mutex> lock(mu);
+    cache[key] = grid;
+    return grid;
 }
 
 cudaError_t allow_dynamic_smem(const void *fn, int bytes)

@@ -279,13 +279,6 @@ gate_bwd_kernel(const float *__restrict__ logits, const int32_t *__restrict__ to
     }
 }
 
-int resident_blocks(const void *fn, int threads)
-{
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, 0) != cudaSuccess || n < 1) n = 1;
-    return n * device_sm_count();
-}
-
 template <int K>
 cudaError_t launch_cbwd_k(const void *dy, const void *eo, const moe_layout *L, const float *gates, int T, int H,
                           void *d_eo, float *d_gates, cudaStream_t s)
@@ -294,11 +287,7 @@ cudaError_t launch_cbwd_k(const void *dy, const void *eo, const moe_layout *L, c
     // V vectors per lane and pass, chosen so the (K+1)*V vectors of a pass
     // fit in registers next to each other.
     constexpr int V = K <= 3 ? 4 : (K <= 8 ? 2 : 1);
-    static int resident[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    int &res = resident[dev & 63];
-    if (res == 0) res = resident_blocks(reinterpret_cast<const void *>(combine_bwd_kernel<K, V>), kBwdThreads);
+    const int res = resident_grid(reinterpret_cast<const void *>(combine_bwd_kernel<K, V>), kBwdThreads, 0);
     const long long need = ((long long)T + kBwdThreads / 32 - 1) / (kBwdThreads / 32);
     const unsigned grid = (unsigned)(need < res ? need : res);
     return launch_pdl(combine_bwd_kernel<K, V>, dim3(grid), dim3(kBwdThreads), 0, s, static_cast<const uint4 *>(dy),
@@ -311,12 +300,7 @@ template <int MODE, int G, int EPL, int U = (EPL <= 2 ? 4 : (EPL <= 4 ? 2 : 1))>
 cudaError_t launch_gbwd(const float *logits, const int32_t *topk_idx, const float *d_gates, int T, int E, int k,
                         float *d_logits, void *ws, cudaStream_t s)
 {
-    static int resident[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    int &res = resident[dev & 63];
-    if (res == 0)
-        res = resident_blocks(reinterpret_cast<const void *>(gate_bwd_kernel<MODE, G, EPL, U>), kGateBwdThreads);
+    const int res = resident_grid(reinterpret_cast<const void *>(gate_bwd_kernel<MODE, G, EPL, U>), kGateBwdThreads, 0);
     const long long per_block = (long long)(kGateBwdThreads / 32) * (32 / G) * U;
     const long long need = ((long long)T + per_block - 1) / per_block;
     const unsigned grid = (unsigned)(need < res ? need : res);

@@ -36,9 +36,6 @@
 // rounds exactly like the plain fp32 add).
 #include <cuda_bf16.h>
 
-#include <mutex>
-#include <unordered_map>
-
 #include "common.cuh"
 #include "tma.cuh"
 
@@ -306,23 +303,6 @@ __global__ void __launch_bounds__(kCombThreads + 32) combine_tma_kernel(CombineA
     }
 }
 
-int blocks_per_sm(const void *fn, size_t smem)
-{
-    static std::mutex mu;
-    static std::unordered_map<unsigned long long, int> cache;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    const unsigned long long key = (reinterpret_cast<unsigned long long>(fn) * 1315423911ull) ^
-                                   ((unsigned long long)smem << 8) ^ (unsigned long long)dev;
-    std::lock_guard<std::mutex> lock(mu);
-    auto it = cache.find(key);
-    if (it != cache.end()) return it->second;
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kCombThreads + 32, smem) != cudaSuccess || n < 1) n = 1;
-    cache[key] = n;
-    return n;
-}
-
 template <int K>
 cudaError_t launch_k(const CombineArgs &a, cudaStream_t s)
 {
@@ -330,7 +310,7 @@ cudaError_t launch_k(const CombineArgs &a, cudaStream_t s)
     const size_t smem = (size_t)a.ring_bytes;
     cudaError_t err = allow_dynamic_smem(fn, (int)smem);
     if (err != cudaSuccess) return err;
-    const long long resident = (long long)device_sm_count() * blocks_per_sm(fn, smem);
+    const long long resident = resident_grid(fn, kCombThreads + 32, smem);
     const unsigned grid = (unsigned)(a.units < resident ? a.units : resident);
     return launch_pdl(combine_tma_kernel<K>, dim3(grid), dim3(kCombThreads + 32), smem, s, a);
 }

@@ -134,6 +134,11 @@ __device__ __forceinline__ float bf16hi(unsigned w) { return __uint_as_float(w &
 namespace moe {
 int device_sm_count();
 
+// Blocks of `fn` that fit on the device at once (per SM, for `threads` per
+// block and `smem` bytes of dynamic shared memory, times the SM count):
+// the grid of a persistent kernel.  Cached per kernel, shape and device.
+int resident_grid(const void *fn, int threads, size_t smem);
+
 // Allow `fn` up to `bytes` of dynamic shared memory on the current device
 // (once per kernel, device and size; static + dynamic above 48 KiB needs it).
 cudaError_t allow_dynamic_smem(const void *fn, int bytes);

@@ -476,13 +476,6 @@ combine_fp8_kernel(const uint4 *__restrict__ codes, const float2 *__restrict__ s
     }
 }
 
-int resident_grid(const void *fn, int threads)
-{
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, 0) != cudaSuccess || n < 1) n = 1;
-    return n * device_sm_count();
-}
-
 template <int MODE, bool TOKENS>
 cudaError_t launch_encode(const void *src, long long n_src, int H, const moe_layout *L, void *out, float *scales,
                           cudaStream_t s)
@@ -514,9 +507,7 @@ cudaError_t launch_encode(const void *src, long long n_src, int H, const moe_lay
     const size_t smem = (size_t)a.stages * a.rowbytes;
     cudaError_t err = allow_dynamic_smem(fn, (int)smem);
     if (err != cudaSuccess) return err;
-    int bps = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, fn, threads, smem) != cudaSuccess || bps < 1) bps = 1;
-    const long long resident = (long long)bps * device_sm_count();
+    const long long resident = resident_grid(fn, threads, smem);
     const unsigned grid = (unsigned)(n_src < resident ? (n_src < 1 ? 1 : n_src) : resident);
     return launch_pdl(fp8_encode_kernel<MODE, TOKENS>, dim3(grid), dim3(threads), smem, s, a);
 }
@@ -528,12 +519,7 @@ cudaError_t launch_grouped(const void *src, long long n_src, int H, const moe_la
     const int nvec = H / 8;
     cudaError_t err = cudaSuccess;
     if (MODE != MOE_FP8_PER_TOKEN) {
-        static int res[64] = {0};
-        int dev = 0;
-        cudaGetDevice(&dev);
-        int &r = res[dev & 63];
-        if (r == 0)
-            r = resident_grid(reinterpret_cast<const void *>(fp8_group_stats_kernel<MODE, TOKENS>), kStatThreads);
+        const int r = resident_grid(reinterpret_cast<const void *>(fp8_group_stats_kernel<MODE, TOKENS>), kStatThreads, 0);
         const long long need = (n_src + kStatThreads / 32 - 1) / (kStatThreads / 32);
         const unsigned grid = (unsigned)(need < r ? (need < 1 ? 1 : need) : r);
         err = launch_pdl(fp8_group_stats_kernel<MODE, TOKENS>, dim3(grid), dim3(kStatThreads), 0, s,
@@ -549,11 +535,7 @@ cudaError_t launch_cfp8_k(const void *codes, const float *scales, const moe_layo
                           const void *shared, int Ks, int T, int H, void *y, cudaStream_t s)
 {
     constexpr int V = K <= 2 ? 2 : 1;
-    static int res[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    int &r = res[dev & 63];
-    if (r == 0) r = resident_grid(reinterpret_cast<const void *>(combine_fp8_kernel<K, V>), kCombFp8Threads);
+    const int r = resident_grid(reinterpret_cast<const void *>(combine_fp8_kernel<K, V>), kCombFp8Threads, 0);
     const long long need = ((long long)T + kCombFp8Threads / 32 - 1) / (kCombFp8Threads / 32);
     const unsigned grid = (unsigned)(need < r ? need : r);
     return launch_pdl(combine_fp8_kernel<K, V>, dim3(grid), dim3(kCombFp8Threads), 0, s,
