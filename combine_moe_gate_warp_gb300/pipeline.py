@@ -239,6 +239,9 @@ class RouteGraph:
         self.x = torch.zeros((s.T, s.H), **bf16)
         self.expert_out = torch.zeros((max(p.r_max, 1), s.H), **bf16)
         self.shared_out = torch.zeros((s.Ks, s.T, s.H), **bf16) if s.Ks else None
+        self.graph = None
+        if s.T == 0:
+            return  # nothing to launch: step() is a no-op
         self.stream.wait_stream(torch.cuda.current_stream(self.device))
         with torch.cuda.stream(self.stream):
             self._calls()
@@ -255,6 +258,8 @@ class RouteGraph:
 
     def replay(self):
         """Replay on the graph's stream (inputs already in the buffers)."""
+        if self.graph is None:
+            return
         with torch.cuda.stream(self.stream):
             self.graph.replay()
 
@@ -269,7 +274,8 @@ class RouteGraph:
                     dst.copy_(src, non_blocking=True)
             if expert_out is not None:
                 self.expert_out[:expert_out.shape[0]].copy_(expert_out, non_blocking=True)
-            self.graph.replay()
+            if self.graph is not None:
+                self.graph.replay()
         cur.wait_stream(self.stream)
         return self.plan
 

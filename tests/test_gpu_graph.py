@@ -89,3 +89,35 @@ def test_replay_matches_oracle(name, T):
         # within 1e-6 of the oracle's) times the sum of |expert outputs|
         bound = ulp + (k + w.Ks) * 2.0 ** -24 * mag + 1e-6 * mag1
         assert np.all(np.abs(y - ref) <= bound), f"{np.sum(np.abs(y - ref) > bound)} values outside the bound"
+
+
+@pytest.mark.parametrize("name,T,variant", [("fp8_skewed", 1500, {}), ("prefill_reassign", 700, {}),
+                                             ("fp8_skewed", 1200, {"fp8": 3, "fp8_combine": 2})])
+def test_replay_fp8_and_reassign(name, T, variant):
+    """FP8 dispatch (per token; global codes with FP8 expert outputs) and
+    the re-assigning layout through the graph: ids, counts, layout and
+    packed rows (codes and scales) against the oracle."""
+    w = workloads.Workload(**{**W[name].scaled(T).__dict__, **variant})
+    g = RouteGraph(shape_of(w), "cuda")
+    for seed in (w.seed, w.seed + 3):
+        wb = workloads.Workload(**{**w.__dict__, "seed": seed})
+        inp = workloads.make_inputs(wb, "cuda")
+        plan = g.step(inp["logits"], inp["x"], None, inp["shared"])
+        torch.cuda.synchronize()
+        assert g.status() == 0
+        og = oracle.gate(inp["logits"].cpu().numpy(), w.k, w.mode)
+        assert np.array_equal(plan.topk_idx[:w.T].cpu().numpy(), og[0])
+        g32 = og[1].astype(np.float32)
+        L = (oracle.layout_reassign(og[0], w.E, w.P, w.capacity, gates_f32=g32) if w.reassign
+             else oracle.layout(og[0], w.E, w.P, w.capacity, gates_f32=g32))
+        assert np.array_equal(plan.layout.offsets.cpu().numpy(), L["offsets"])
+        assert np.array_equal(plan.layout.dst_row.cpu().numpy()[:w.T * w.k], L["dst_row"])
+        check_dispatch(w, plan, L, bits(inp["x"]), np.arange(L["R"], dtype=np.int64))
+
+
+def test_empty_batch_graph():
+    w = W["v2_top2"].scaled(0)
+    g = RouteGraph(shape_of(w), "cuda")
+    g.step()
+    torch.cuda.synchronize()
+    assert g.status() == 0
