@@ -118,7 +118,14 @@ __device__ __forceinline__ bool wait_stage(uint64_t *bar, uint32_t parity)
     return true;
 }
 
-template <int K>
+// PSLEEP: the producer sleeps (suspend hint) instead of polling while it
+// waits for ring space.  Chosen per launch from the consumer mode: with all
+// four consumer warps on one large unit (many slots per token, e.g. k = 8)
+// a polling producer competes with them for issue slots (prefill_cap: 1520 ->
+// 1463 us); with one warp per small unit the producer must react at once
+// (fp8_skewed: 231 -> 243 us when it sleeps).  A runtime switch inside the
+// wait loop cost more than either, so it is a template parameter.
+template <int K, bool PSLEEP>
 __global__ void __launch_bounds__(kCombThreads + 32) combine_tma_kernel(CombineArgs a)
 {
     extern __shared__ __align__(128) unsigned char s_ring[];  // byte ring of a.ring_bytes
@@ -159,10 +166,14 @@ __global__ void __launch_bounds__(kCombThreads + 32) combine_tma_kernel(CombineA
         auto retire_oldest = [&]() -> bool {
             const int d = (int)(oldest % kDesc);
             const uint32_t par = (uint32_t)((oldest / kDesc) & 1);
-            bool ok = mbar_try_wait(&s_empty[d], par);
+            auto probe = [&]() {
+                if constexpr (PSLEEP) return mbar_try_wait_sleep(&s_empty[d], par);
+                else return mbar_try_wait(&s_empty[d], par);
+            };
+            bool ok = probe();
             if (!ok) {
                 const unsigned long long t0 = global_timer_ns();
-                while (!(ok = mbar_try_wait(&s_empty[d], par)) && global_timer_ns() - t0 < kSpinLimitNs) {
+                while (!(ok = probe()) && global_timer_ns() - t0 < kSpinLimitNs) {
                 }
             }
             ++oldest;
@@ -303,16 +314,22 @@ __global__ void __launch_bounds__(kCombThreads + 32) combine_tma_kernel(CombineA
     }
 }
 
-template <int K>
-cudaError_t launch_k(const CombineArgs &a, cudaStream_t s)
+template <int K, bool PSLEEP>
+cudaError_t launch_kp(const CombineArgs &a, cudaStream_t s)
 {
-    const void *fn = reinterpret_cast<const void *>(combine_tma_kernel<K>);
+    const void *fn = reinterpret_cast<const void *>(combine_tma_kernel<K, PSLEEP>);
     const size_t smem = (size_t)a.ring_bytes;
     cudaError_t err = allow_dynamic_smem(fn, (int)smem);
     if (err != cudaSuccess) return err;
     const long long resident = resident_grid(fn, kCombThreads + 32, smem);
     const unsigned grid = (unsigned)(a.units < resident ? a.units : resident);
-    return launch_pdl(combine_tma_kernel<K>, dim3(grid), dim3(kCombThreads + 32), smem, s, a);
+    return launch_pdl(combine_tma_kernel<K, PSLEEP>, dim3(grid), dim3(kCombThreads + 32), smem, s, a);
+}
+
+template <int K>
+cudaError_t launch_k(const CombineArgs &a, cudaStream_t s)
+{
+    return a.group == 4 ? launch_kp<K, true>(a, s) : launch_kp<K, false>(a, s);
 }
 
 }  // namespace

@@ -56,6 +56,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return done != 0;
 }
 
+// The same probe, but the thread may be suspended for up to kMbarSuspendNs
+// while it waits (it wakes when the phase completes): a waiting warp sleeps
+// instead of polling.  Callers bound their wait loops themselves.
+constexpr uint32_t kMbarSuspendNs = 1000;
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(kMbarSuspendNs)
+        : "memory");
+    return done != 0;
+}
+
 // global -> shared bulk copy, completion counted in bytes on `bar`.
 __device__ __forceinline__ void bulk_load(void *dst_smem, const void *src_gmem, uint32_t bytes, uint64_t *bar)
 {
