@@ -120,11 +120,12 @@ __device__ __forceinline__ bool wait_stage(uint64_t *bar, uint32_t parity)
 
 // PSLEEP: the producer sleeps (suspend hint) instead of polling while it
 // waits for ring space.  Chosen per launch from the consumer mode: with all
-// four consumer warps on one large unit (many slots per token, e.g. k = 8)
-// a polling producer competes with them for issue slots (prefill_cap: 1520 ->
-// 1463 us); with one warp per small unit the producer must react at once
-// (fp8_skewed: 231 -> 243 us when it sleeps).  A runtime switch inside the
-// wait loop cost more than either, so it is a template parameter.
+// four consumer warps on one large unit (many slots per token) a polling
+// producer competes with them for issue slots (262144 tokens x 4096, top-8
+// with capacity drops: 1520 -> 1463 us on GB300); with one warp per small
+// unit the producer must react at once (65536 x 4096, top-2: 231 -> 243 us
+// when it sleeps).  A runtime switch inside the wait loop cost more than
+// either, so it is a template parameter.
 template <int K, bool PSLEEP>
 __global__ void __launch_bounds__(kCombThreads + 32) combine_tma_kernel(CombineArgs a)
 {
