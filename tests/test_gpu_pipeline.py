@@ -50,3 +50,30 @@ def test_pipeline_matches_serial_calls(w):
         assert np.array_equal(y, bits(ref.y[:w.T])), f"step {i}: y differs from the serial calls"
         if w.identity_experts:
             assert np.array_equal(y, bits(inp["x"])), "identity experts: combine(dispatch(x)) == x"
+
+
+def test_pipeline_depth3_host_outputs():
+    """Three plans, y and the statistics copied into pinned host buffers
+    by the pipeline itself (the end-to-end path): y equals the serial calls
+    bit for bit, aux and entropy are the oracle's (within 1e-9 and 1e-6)."""
+    w = W["v2_top2"].scaled(1500)
+    batches = []
+    for b in range(4):
+        wb = workloads.Workload(**{**w.__dict__, "seed": w.seed + 29 * b})
+        eo = workloads.make_expert_out(wb, max(wb.r_max, 1), "cuda")
+        batches.append((wb, workloads.make_inputs(wb, "cuda"), eo))
+    pipe = RoutePipeline(shape_of(w), "cuda", depth=3)
+    ys = [torch.empty((w.T, w.H), dtype=torch.bfloat16, pin_memory=True) for _ in range(8)]
+    stats = [torch.empty(2, dtype=torch.float64, pin_memory=True) for _ in range(8)]
+    for i in range(8):
+        wb, inp, eo = batches[i % 4]
+        pipe.step(inp["logits"], inp["x"], eo, inp["shared"], out=ys[i], stats_out=stats[i])
+    assert pipe.status() == 0
+    for i in range(8):
+        wb, inp, eo = batches[i % 4]
+        ref = RoutePlan(shape_of(w), "cuda")
+        ref.step(inp["logits"], inp["x"], eo, inp["shared"])
+        assert ref.status() == 0
+        assert np.array_equal(bits(ys[i]), bits(ref.y[:w.T])), f"step {i}: y differs"
+        og = oracle.gate(inp["logits"].cpu().numpy(), w.k, w.mode)
+        assert abs(stats[i][0].item() - og[3]) <= 1e-9 and abs(stats[i][1].item() - og[4]) <= 1e-6
