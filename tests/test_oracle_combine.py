@@ -95,3 +95,63 @@ def test_dropped_slots_do_not_contribute(oracle, rng):
     dst[1] = -1
     y = oracle.combine_f32order(eo, gates, dst, np.arange(T), T, k)
     assert np.array_equal(_f(y[0]), _f(eo[0]) * np.float32(0.5))
+
+
+def _f32_to_bf16_exact(v):
+    """bf16 bits of values that are exact in bf16 (asserted)."""
+    u = np.asarray(v, np.float32).view(np.uint32)
+    assert np.all((u & 0xFFFF) == 0), "fixture value not exact in bf16"
+    return (u >> 16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("case", [0, 1])
+def test_hand_worked_shared_expert_combine(oracle, case):
+    """Shared experts (K_s = 2 and 3) added with weight 1 after the routed
+    terms, against hand-worked values: both the pinned fp32 order and the
+    fp64 reference must give the fixture's y exactly (every term and partial
+    sum is dyadic).  The shared rows differ per (s, t), so a transposed
+    [t, s] index or a dropped last shared expert fails here."""
+    g = load_golden("shared_expert_combine.json")
+    c = g["cases"][case]
+    T, Ks, k, H = c["T"], c["Ks"], g["k"], g["H"]
+    eo = _f32_to_bf16_exact(g["expert_rows"])
+    gates = np.array(c["gates"], np.float32)
+    dst = np.array(c["dst_row"], np.int32)
+    shared = _f32_to_bf16_exact(c["shared"])
+    assert shared.shape == (Ks, T, H)
+    toks = np.arange(T)
+    want = np.array(c["y"], np.float32)
+    y = oracle.combine_f32order(eo, gates, dst, toks, T, k, shared)
+    assert np.array_equal(_f(y), want)
+    ref, mag = oracle.combine_ref64(eo, gates, dst, toks, T, k, shared)
+    assert np.array_equal(ref, want.astype(np.float64))
+    # without the shared experts only the routed terms remain
+    y0 = oracle.combine_f32order(eo, gates, dst, toks, T, k, None)
+    assert np.array_equal(_f(y0), np.array(c["routed_only"], np.float32))
+    if "abs_terms_token1" in c:
+        assert np.array_equal(mag[1], np.array(c["abs_terms_token1"], np.float64))
+    # a subset of tokens reads the same shared rows (token index, not position in the list)
+    y1 = oracle.combine_f32order(eo, gates, dst, np.array([T - 1]), T, k, shared)
+    assert np.array_equal(_f(y1[0]), want[T - 1])
+
+
+@pytest.mark.parametrize("case", [0, 1])
+def test_hand_worked_shared_expert_combine_fp8(oracle, case):
+    """The FP8 combine on the same rows given as e4m3 codes with (scale,
+    zero) = (1, 0): the same hand-worked y, shared experts included."""
+    g = load_golden("shared_expert_combine.json")
+    c = g["cases"][case]
+    T, Ks, k = c["T"], c["Ks"], g["k"]
+    codes = np.array(g["expert_rows_e4m3"], np.uint8)
+    assert np.array_equal(np.array([[oracle.e4m3_decode(int(v)) for v in r] for r in codes]),
+                          np.array(g["expert_rows"], np.float64))
+    scales = np.tile(np.array([1.0, 0.0], np.float32), (codes.shape[0], 1))
+    gates = np.array(c["gates"], np.float32)
+    dst = np.array(c["dst_row"], np.int32)
+    shared = _f32_to_bf16_exact(c["shared"])
+    toks = np.arange(T)
+    want = np.array(c["y"], np.float32)
+    y = oracle.combine_fp8_f32order(codes, scales, gates, dst, toks, T, k, shared)
+    assert np.array_equal(_f(y), want)
+    ref, _ = oracle.combine_fp8_ref64(codes, scales, gates, dst, toks, T, k, shared)
+    assert np.array_equal(ref, want.astype(np.float64))
