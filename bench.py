@@ -30,17 +30,21 @@ sys.path.insert(0, ROOT)
 
 METRIC = "route+dispatch+combine tokens/s and HBM GB/s (fraction of GB300 roofline)"
 UNIT = "tokens/s"
-DEFAULT_WORKLOAD = "v2_top2"  # batch 32 x seq 512, hidden 5120, 16 experts, top-2
+# the workloads a default run times; the line's headline is the largest
+DEFAULT_WORKLOADS = ("v2_top2", "fine_shared", "fp8_skewed", "prefill_cap")
+HEADLINE_WORKLOAD = "prefill_cap"  # batch 128 x seq 2048, hidden 4096, 64 experts, top-8, capacity 1.25
 
 
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", "--config", default=DEFAULT_WORKLOAD,
-                    help="workload name, or C0..C4 for tiny, v2_top2, fine_shared, fp8_skewed, prefill_cap")
+    ap.add_argument("--workload", "--config", default="all",
+                    help="'all' (v2_top2, fine_shared, fp8_skewed and prefill_cap in one run, the headline on "
+                         "prefill_cap), a workload name, or C0..C4 for tiny, v2_top2, fine_shared, fp8_skewed, "
+                         "prefill_cap")
     ap.add_argument("--seed", type=int, default=None, help="override the workload's seed")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the workload's token count (a smaller case of the same shape, e.g. to profile)")
@@ -48,7 +52,9 @@ def parse_args():
                     help="threads of the second oracle baseline (0: every core this process may use)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
-                    help="target CPU time of the oracle baseline sample")
+                    help="target CPU time of the oracle baseline sample of the headline workload")
+    ap.add_argument("--cpu-seconds-other", type=float, default=3.0,
+                    help="target CPU time of the oracle baseline sample of each other workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-pipeline", action="store_true",
@@ -197,6 +203,8 @@ def kernel_bytes(w, R):
         "layout": w.T * w.k * (4 + 4 + 1 + 4) + R * 4,
         "dispatch": x * (2 if grouped else 1) + packed,
     }
+    # the fused routing call: logits read, ids, gates, dst_row, mask and src_pos written
+    by["route"] = w.T * w.E * 4 + w.T * w.k * (4 + 4 + 4 + 1) + R * 4
     if w.fp8_combine:
         # expert side: bf16 rows read (twice for grouped modes), codes and scales written;
         # combine: codes and scales read
@@ -211,7 +219,7 @@ def kernel_bytes(w, R):
     # expert outputs: read in bf16, codes written and read), y written
     by["roofline_step"] = x + R * w.H * bt + eo_metric + y
     # every byte the step moves
-    by["all_step"] = sum(v for k2, v in by.items() if k2 not in ("roofline_step",))
+    by["all_step"] = sum(v for k2, v in by.items() if k2 not in ("roofline_step", "gate", "layout"))
     return by
 
 
@@ -221,7 +229,7 @@ def kernel_sources(name: str, w=None) -> tuple:
     fp8 = bool(w is not None and w.fp8)
     fp8c = bool(w is not None and w.fp8_combine)
     table = {
-        "gate": ("gate.cu",), "layout": ("layout.cu",),
+        "gate": ("gate.cu",), "layout": ("layout.cu",), "route": ("route.cu",),
         "dispatch": ("quant.cu", "fp8.cuh", "tma.cuh") if fp8 else ("dispatch.cu",),
         "quantize": ("quant.cu", "fp8.cuh", "tma.cuh"),
         "combine": ("quant.cu", "fp8.cuh") if fp8c else ("combine.cu", "tma.cuh"),
@@ -437,6 +445,8 @@ def run_reference(args):
     import torch
 
     from combine_moe_gate_warp_gb300 import workloads
+    if args.workload == "all":
+        args = argparse.Namespace(**{**vars(args), "workload": HEADLINE_WORKLOAD})
     w = resolve_workload(args)
     inputs = workloads.make_inputs(w, "cpu")
     hi = dict(logits=inputs["logits"].numpy(),
@@ -475,34 +485,20 @@ def run_reference(args):
 # our arm
 # ---------------------------------------------------------------------------
 def run_ours(args):
+    import gc
+
     import torch
 
-    from combine_moe_gate_warp_gb300 import RoutePlan, RouteShape, build, workloads
+    from combine_moe_gate_warp_gb300 import build
     world, rank, local = dist_env()
     init_dist(world, "nccl")
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     build()
-    w = rank_workload(resolve_workload(args), rank)
-
-    inputs = workloads.make_inputs(w, dev)
-    shape = RouteShape(T=w.T, H=w.H, E=w.E, k=w.k, P=w.P, mode=w.mode, fp8=int(w.fp8), Ks=w.Ks,
-                       capacity=w.capacity, fp8_combine=int(w.fp8_combine), reassign=bool(w.reassign))
-    plan = RoutePlan(shape, dev)
-    eo = None if w.identity_experts else workloads.make_expert_out(w, max(plan.r_max, 1), dev)
-    stream = torch.cuda.current_stream(dev)
-
-    def step():
-        plan.step(inputs["logits"], inputs["x"], plan.packed if eo is None else eo, inputs["shared"])
-
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize(dev)
-    st = plan.status()
-    if st != 0:
-        raise RuntimeError(f"device status {st} after warm-up")
-    R = int(plan.layout.offsets[w.E].item())
-
+    if args.workload == "all":
+        names, headline = list(DEFAULT_WORKLOADS), HEADLINE_WORKLOAD
+    else:
+        names, headline = [args.workload], args.workload
     bus = None
     try:
         props = torch.cuda.get_device_properties(dev)
@@ -511,13 +507,70 @@ def run_ours(args):
         bus = None
     sampler = ClockSampler(bus) if rank == 0 else None
     time.sleep(0.3 if sampler else 0)
+    entries = {}
+    for name in names:
+        wa = argparse.Namespace(**{**vars(args), "workload": name})
+        cpu_s = args.cpu_seconds if name == headline else args.cpu_seconds_other
+        entries[name] = measure_workload(wa, world, rank, dev, sampler, cpu_s)
+        gc.collect()
+        torch.cuda.empty_cache()
+    if sampler:
+        sampler.stop()
+    if rank == 0:
+        line = dict(entries[headline])
+        if len(names) > 1:
+            line["headline_workload"] = (f"{headline}: the largest of the workloads timed here (the metric names "
+                                         "no workload); every workload's full entry is under 'workloads'")
+            line["workloads"] = {n: {k2: v for k2, v in e.items() if k2 not in LINE_ONLY_KEYS}
+                                 for n, e in entries.items()}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+# keys of the contract line that a per-workload entry does not repeat
+LINE_ONLY_KEYS = ("metric", "unit", "n_gpus", "steps", "warmup", "higher_is_better", "scaling", "vs_baseline",
+                  "data")
+
+
+def measure_workload(args, world, rank, dev, sampler, cpu_seconds):
+    """Every measurement of one workload: the timed one-stream steps (with
+    per-call events on every 8th step), the pipelined batches and the CUDA
+    graph replays (the headline takes the fastest), the data-movement calls
+    back to back for the roofline, the combine's ulp statistics, end to end
+    from host buffers, the de-duplicated send path, the backward calls and
+    the oracle's CPU baseline.  Returns the workload's JSON entry."""
+    import torch
+
+    from combine_moe_gate_warp_gb300 import RoutePipeline, RoutePlan, RouteShape, workloads
+    w = rank_workload(resolve_workload(args), rank)
+
+    inputs = workloads.make_inputs(w, dev)
+    shape = RouteShape(T=w.T, H=w.H, E=w.E, k=w.k, P=w.P, mode=w.mode, fp8=int(w.fp8), Ks=w.Ks,
+                       capacity=w.capacity, fp8_combine=int(w.fp8_combine), reassign=bool(w.reassign))
+    plan = RoutePlan(shape, dev)
+    eo = None if w.identity_experts else workloads.make_expert_out(w, max(plan.r_max, 1), dev)
+    stream = torch.cuda.current_stream(dev)
+    eo_arg = plan.packed if eo is None else eo
+
+    for _ in range(max(3, args.warmup)):
+        plan.step(inputs["logits"], inputs["x"], eo_arg, inputs["shared"])
+    torch.cuda.synchronize(dev)
+    st = plan.status()
+    if st != 0:
+        raise RuntimeError(f"{w.name}: device status {st} after warm-up")
+    R = int(plan.layout.offsets[w.E].item())
 
     K = args.steps
     EV = 8  # per-call CUDA events on every EV-th step (events between kernels cost ~10 us/step)
     sampled = list(range(0, K, EV))
-    eo_arg = plan.packed if eo is None else eo
-    calls = [("gate", lambda: plan.gate(inputs["logits"])), ("layout", plan.dispatch_layout),
-             ("dispatch", lambda: plan.dispatch(inputs["x"]))]
+    if plan.fused_route:
+        calls = [("route", lambda: plan.route(inputs["logits"]))]
+    else:
+        calls = [("gate", lambda: plan.gate(inputs["logits"])), ("layout", plan.dispatch_layout)]
+    calls += [("dispatch", lambda: plan.dispatch(inputs["x"]))]
     if w.fp8_combine:
         calls += [("quantize", lambda: plan.quantize_expert_out(eo_arg)),
                   ("combine", lambda: plan.combine_fp8(inputs["shared"]))]
@@ -549,8 +602,9 @@ def run_ours(args):
     elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     st = plan.status()
     if st != 0:
-        raise RuntimeError(f"device status {st} during the timed steps")
-    from combine_moe_gate_warp_gb300 import RoutePipeline
+        raise RuntimeError(f"{w.name}: device status {st} during the timed steps")
+    # the combine's accuracy on the last timed step's output
+    ulp = combine_ulp_stats(plan, w, eo_arg, inputs["shared"])
     pipe = None
     t_pw0 = t_pw1 = None
     if not args.no_pipeline and RoutePipeline.overlaps(shape):
@@ -562,9 +616,6 @@ def run_ours(args):
         t_gw0 = time.time()
         graph = time_graph(w, shape, inputs, eo, dev, world, K, max(3, args.warmup))
         t_gw1 = time.time()
-    if sampler:
-        time.sleep(0.25)
-        sampler.stop()
     per = {n: statistics.fmean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in sampled)
            for j, n in enumerate(names)}
     step_samples = sorted(ev[i][0].elapsed_time(ev[i][len(calls)]) for i in sampled)
@@ -589,9 +640,10 @@ def run_ours(args):
         b2b[n] = a0.elapsed_time(a1) / B2B
     st = plan.status()
     if st != 0:
-        raise RuntimeError(f"device status {st} in the back-to-back launches")
+        raise RuntimeError(f"{w.name}: device status {st} in the back-to-back launches")
     dom = max(("dispatch", "combine"), key=lambda n: b2b[n])
     achieved = by[dom] / (b2b[dom] * 1e-3) / 1e9
+    achieved_ev = by[dom] / (per[dom] * 1e-3) / 1e9
     traffic = measured_traffic(dom, w.name, w)
     ms_step_serial = elapsed_ms / K
     unpipelined = {"ms_per_step": ms_step_serial,
@@ -601,6 +653,7 @@ def run_ours(args):
     # the headline is the fastest of the product's ways to run the same steps
     modes = [(ms_step_serial, unpipelined["note"], (t_wall0, t_wall1))]
     if pipe:
+        pipe["hbm_frac"] = by["roofline_step"] / (pipe["ms_per_step"] * 1e-3) / 1e9 / peak
         modes.append((pipe["ms_per_step"], pipe["note"], (t_pw0, t_pw1)))
     if graph:
         modes.append((graph["ms_per_step"], graph["note"], (t_gw0, t_gw1)))
@@ -613,7 +666,7 @@ def run_ours(args):
     # end to end through the public API: pinned host inputs copied in, result copied out
     e2e = None
     if not args.no_e2e:
-        e2e = time_e2e(w, shape, plan, inputs, eo, dev, world, args.e2e_steps, pipe is not None)
+        e2e = time_e2e(w, shape, plan, inputs, eo, dev, world, args.e2e_steps, pipe is not None, R)
 
     dd = None
     if args.dedup_steps > 0 and 1 <= w.P <= 16:
@@ -625,59 +678,116 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, host_inputs(w, inputs, eo), args.cpu_seconds, args.oracle_threads)
+        cpu = cpu_baseline(w, host_inputs(w, inputs, eo), cpu_seconds, args.oracle_threads)
 
     clocks = sampler.summary(t_h0, t_h1) if sampler else None
-    if rank == 0:
-        line = {
-            "metric": METRIC, "value": tokens_per_s, "unit": UNIT, "n_gpus": world, "steps": K,
-            "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if w.fp8 else "bf16",
-            "data": "synthetic (seeded): x ~ N(0,1) bf16, router logits fp32, expert outputs N(0,1) bf16",
-            "config": config_of(w, world),
-            "hbm_gbs": step_gbs, "hbm_frac": step_gbs / peak, "R": R,
-            "hbm_gbs_all_bytes": by["all_step"] / (ms_step * 1e-3) / 1e9,
-            "hbm_frac_all_bytes": by["all_step"] / (ms_step * 1e-3) / 1e9 / peak,
-            "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
-                         "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                         "traffic": traffic, "algorithmic_bytes": by[dom], "launch_ms": b2b[dom],
-                         "timing": f"mean of {B2B} back-to-back launches of the call between CUDA events "
-                                   "on its stream, after the timed steps"},
-            "kernels_ms_back_to_back": b2b,
-            "kernels_ms": per,
-            "kernels_sampled_steps": len(sampled),
-            "kernels_gbs": {n: by[n] / (per[n] * 1e-3) / 1e9 for n in names},
-            "step_ms_evented": {"median": statistics.median(step_samples), "min": step_samples[0],
-                                "note": "sampled steps with events between the calls"},
-            "execution": execution,
-            "unpipelined": unpipelined,
-            "graph": graph,
-            "gpu_launches": plan.launches_per_step() * K,
-            "clocks": clocks,
-            "e2e": e2e,
-            "cpu_baseline": cpu,
-            "backward": bwd,
-            "dedup": dd,
-        }
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
-    return 0
+    return {
+        "metric": METRIC, "value": tokens_per_s, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if w.fp8 else "bf16",
+        "data": "synthetic (seeded): x ~ N(0,1) bf16, router logits fp32, expert outputs N(0,1) bf16",
+        "config": config_of(w, world),
+        "hbm_gbs": step_gbs, "hbm_frac": step_gbs / peak, "R": R,
+        "hbm_gbs_all_bytes": by["all_step"] / (ms_step * 1e-3) / 1e9,
+        "hbm_frac_all_bytes": by["all_step"] / (ms_step * 1e-3) / 1e9 / peak,
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "algorithmic_bytes": by[dom], "launch_ms": b2b[dom],
+                     "timing": f"mean of {B2B} back-to-back launches of the call between CUDA events "
+                               "on its stream, after the timed steps",
+                     "achieved_evented": achieved_ev, "frac_evented": achieved_ev / peak,
+                     "launch_ms_evented": per[dom],
+                     "timing_evented": "mean over the sampled timed steps with CUDA events around each call "
+                                       "(includes the launch gap the events add)"},
+        "kernels_ms_back_to_back": b2b,
+        "kernels_ms": per,
+        "kernels_sampled_steps": len(sampled),
+        "kernels_gbs": {n: by[n] / (per[n] * 1e-3) / 1e9 for n in names},
+        "step_ms_evented": {"median": statistics.median(step_samples), "min": step_samples[0],
+                            "note": "sampled steps with events between the calls"},
+        "execution": execution,
+        "unpipelined": unpipelined,
+        "pipelined": pipe,
+        "graph": graph,
+        "gpu_launches": plan.launches_per_step() * K,
+        "clocks": clocks,
+        "combine_ulp": ulp,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "backward": bwd,
+        "dedup": dd,
+    }
 
 
-def time_e2e(w, shape, plan, inputs, eo, dev, world, steps, pipelined):
+def combine_ulp_stats(plan, w, eo, shared):
+    """How many combine outputs of the last step lie beyond one bf16 ulp of
+    the fp64 sum of their terms (the same gates, rows and shared outputs the
+    kernel read), and the largest share of the fp32 summation allowance
+    n * 2^-24 * sum|terms| that such an output uses (above 1 would be outside
+    the bound the tests enforce).  Computed on the GPU in fp64 with torch,
+    in token chunks."""
+    import torch
+    T, k, H, Ks = w.T, w.k, w.H, w.Ks
+    if T == 0:
+        return {"outputs": 0, "beyond_1ulp": 0, "outside_bound": 0, "max_allowance_used": 0.0}
+    dst = plan.layout.dst_row[:T * k].view(T, k).long()
+    g = plan.gates[:T].double()
+    n_terms = k + Ks + (1 if w.fp8_combine else 0)
+    if w.fp8_combine:
+        vals = plan.eo_codes.view(torch.float8_e4m3fn)
+        sc = plan.eo_scales.double()
+    chunk = max(1, (1 << 24) // max(1, H))
+    beyond = outside = 0
+    used = 0.0
+    for t0 in range(0, T, chunk):
+        t1 = min(T, t0 + chunk)
+        acc = torch.zeros((t1 - t0, H), dtype=torch.float64, device=g.device)
+        mag = torch.zeros_like(acc)
+        for j in range(k):
+            r = dst[t0:t1, j]
+            keep = (r >= 0).double().unsqueeze(1)
+            rr = r.clamp(min=0)
+            if w.fp8_combine:
+                # the dequantised row is rounded to fp32 once, as the kernel does
+                rows = (vals.index_select(0, rr).double() * sc[rr, 0:1] + sc[rr, 1:2]).float().double()
+            else:
+                rows = eo.index_select(0, rr).double()
+            term = rows * g[t0:t1, j:j + 1] * keep
+            acc += term
+            mag += term.abs()
+        for s_ in range(Ks):
+            term = shared[s_, t0:t1].double()
+            acc += term
+            mag += term.abs()
+        err = (plan.y[t0:t1].double() - acc).abs()
+        _, ex = torch.frexp(acc)
+        e = torch.where(acc == 0, torch.full_like(ex, -200), ex - 1).clamp(min=-126)
+        ulp = torch.pow(2.0, (e - 7).double())
+        allow = n_terms * 2.0 ** -24 * mag
+        over = err > ulp
+        beyond += int(over.sum().item())
+        outside += int((err > ulp + allow).sum().item())
+        if bool(over.any()):
+            used = max(used, float(((err - ulp)[over] / allow[over].clamp(min=1e-300)).max().item()))
+    return {"outputs": T * H, "beyond_1ulp": beyond, "beyond_1ulp_frac": beyond / (T * H),
+            "outside_bound": outside, "max_allowance_used": used,
+            "how": "each y against the fp64 sum of its terms (the kernel's gates, rows and shared outputs), "
+                   "on the GPU; allowance n * 2^-24 * sum|terms| with n = the number of terms"}
+
+
+def time_e2e(w, shape, plan, inputs, eo, dev, world, steps, pipelined, R):
     """The same metric end to end: every step copies its inputs (router
-    logits, x, expert outputs, shared-expert outputs) from pinned host memory
-    to the device and reads y, the aux loss and the entropy back.  With the
-    pipelined executor the copies of batch i+1 overlap the work of batch i
-    (a copy stream feeds each plan's own input buffers); otherwise the
-    copies and the calls run in order on one stream."""
+    logits, x, the R expert-output rows the batch produces, shared-expert
+    outputs) from pinned host memory to the device and reads y, the aux loss
+    and the entropy back.  With the pipelined executor the copies of batch
+    i+1 overlap the work of batch i (a copy stream feeds each plan's own
+    input buffers); otherwise the copies and the calls run in order on one
+    stream.  (Every step routes the same batch, so R is the warm-up's.)"""
     import torch
 
     from combine_moe_gate_warp_gb300 import RoutePipeline
     pin = dict(logits=inputs["logits"].cpu().pin_memory(), x=inputs["x"].cpu().pin_memory())
-    eo_h = None if eo is None else eo.cpu().pin_memory()
+    eo_h = None if eo is None else eo[:max(R, 1)].cpu().pin_memory()
     sh_h = None if inputs["shared"] is None else inputs["shared"].cpu().pin_memory()
     y_h = torch.empty((w.T, w.H), dtype=torch.bfloat16, pin_memory=True)
     stats_h = torch.empty(2, dtype=torch.float64, pin_memory=True)
@@ -693,7 +803,7 @@ def time_e2e(w, shape, plan, inputs, eo, dev, world, steps, pipelined):
         d["logits"].copy_(pin["logits"], non_blocking=True)
         d["x"].copy_(pin["x"], non_blocking=True)
         if d["eo"] is not None:
-            d["eo"].copy_(eo_h, non_blocking=True)
+            d["eo"][:eo_h.shape[0]].copy_(eo_h, non_blocking=True)
         if d["shared"] is not None:
             d["shared"].copy_(sh_h, non_blocking=True)
 
@@ -882,10 +992,28 @@ def time_dedup(plan, w, inputs, steps, world, dev, stream, peak, R):
     t_disp = statistics.fmean(e[1].elapsed_time(e[2]) for e in ev)
     bt = 1 if fp8 else 2
     disp_bytes = w.T * w.H * 2 + S * w.H * bt + (S * 8 if fp8 else 0)
+    # send rows when the experts are grouped by rank of an expert-parallel
+    # exchange of W ranks (one group per rank: a token goes to a rank once)
+    by_ranks = {}
+    for g in (2, 4, 8, 16):
+        if g > w.E or w.E % g:
+            continue
+        Dg = abi.Dedup(w.T, w.k, g, dev)
+        abi.moe_dedup_layout(plan.layout, plan.gates, Dg, stream, groups=g)
+        Sg = int(Dg.send_offsets[g].item())
+        by_ranks[str(g)] = {"send_rows": Sg, "send_over_packed": Sg / max(R, 1),
+                            "bytes_saved_per_step": (R - Sg) * w.H * bt * 2}
+        del Dg
+    st = plan.status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} in the de-duplicated layouts per rank group")
     return {"send_rows": S, "packed_rows": R, "send_over_packed": S / max(R, 1),
             "layout_ms": t_lay, "dispatch_ms": t_disp,
             "dispatch_gbs": disp_bytes / (t_disp * 1e-3) / 1e9,
-            "dispatch_frac": disp_bytes / (t_disp * 1e-3) / 1e9 / peak, "steps": steps}
+            "dispatch_frac": disp_bytes / (t_disp * 1e-3) / 1e9 / peak, "steps": steps,
+            "by_ranks": by_ranks,
+            "by_ranks_note": "send rows with the experts grouped per rank of a W-rank exchange (W = key); "
+                             "bytes saved per step count both directions (rows out, partial rows back)"}
 
 
 def time_backward(plan, w, inputs, eo_arg, steps, world, dev, stream, peak):
@@ -898,7 +1026,7 @@ def time_backward(plan, w, inputs, eo_arg, steps, world, dev, stream, peak):
     from combine_moe_gate_warp_gb300 import workloads
     R = int(plan.layout.offsets[w.E].item())
     dy = workloads.make_dy(w, dev)
-    dp = workloads.make_d_packed(w, max(R, 1), dev)
+    dp = workloads.make_d_packed(w, max(plan.r_max, 1), dev)
     for _ in range(3):
         plan.backward(inputs["logits"], dy, eo_arg, dp)
     torch.cuda.synchronize(dev)

@@ -12,7 +12,7 @@ from .abi import (MOE_ERR_CUDA, MOE_ERR_DEVICE_DATA, MOE_ERR_INVALID_ARG, MOE_ER
                   MOE_FP8_PER_TOKEN, MOE_OK, MOE_SOFTMAX_TOPK, MOE_TOPK_SOFTMAX, Layout, MoeError,
                   alloc_workspace, moe_combine, moe_combine_backward, moe_combine_fp8, moe_dispatch,
                   moe_dispatch_backward, moe_dispatch_layout, moe_gate, moe_gate_backward, moe_get_status,
-                  moe_quantize_rows, moe_rows_max, moe_workspace_init, moe_workspace_size)
+                  moe_quantize_rows, moe_route, moe_rows_max, moe_workspace_init, moe_workspace_size)
 from .pipeline import RouteGraph, RoutePipeline, RoutePlan, RouteShape
 
 
@@ -23,7 +23,7 @@ def build(force: bool = False) -> str:
 
 __all__ = [
     "build", "RoutePlan", "RoutePipeline", "RouteGraph", "RouteShape", "Layout", "MoeError", "alloc_workspace",
-    "moe_gate", "moe_dispatch_layout", "moe_dispatch", "moe_combine", "moe_get_status",
+    "moe_gate", "moe_dispatch_layout", "moe_dispatch", "moe_combine", "moe_get_status", "moe_route",
     "moe_quantize_rows", "moe_combine_fp8", "moe_combine_backward", "moe_dispatch_backward",
     "moe_gate_backward", "MOE_FP8_PER_TOKEN", "MOE_FP8_PER_EXPERT", "MOE_FP8_GLOBAL",
     "moe_workspace_size", "moe_workspace_init", "moe_rows_max",

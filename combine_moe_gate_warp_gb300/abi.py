@@ -94,6 +94,8 @@ def lib():
     L.moe_rows_max.restype = ctypes.c_int64
     L.moe_gate.argtypes = [P, I, I, I, I, P, P, P, P, P, P, SZ, P]
     L.moe_gate.restype = I
+    L.moe_route.argtypes = [P, I, I, I, I, I, I, P, P, P, P, P, ctypes.POINTER(moe_layout), P, SZ, P]
+    L.moe_route.restype = I
     L.moe_dispatch_layout.argtypes = [P, P, I, I, I, I, I, P, ctypes.POINTER(moe_layout), P, SZ, P]
     L.moe_dispatch_layout.restype = I
     L.moe_dispatch_layout_reassign.argtypes = [P, P, I, I, I, I, I, P, ctypes.POINTER(moe_layout), P, SZ, P]
@@ -195,8 +197,36 @@ def moe_gate(logits, k: int, mode: int, topk_idx, gates, expert_counts, aux_loss
                           _ptr(ws, name="ws"), _nbytes(ws), _stream(stream)), "moe_gate")
 
 
+def moe_route(logits, k: int, mode: int, P: int, capacity: int, topk_idx, gates, expert_counts, aux_loss, entropy,
+              layout: "Layout", ws, stream=None) -> None:
+    """moe_gate + moe_dispatch_layout in one launch (raises MoeError with
+    MOE_ERR_UNSUPPORTED, nothing enqueued, for a batch too large for it)."""
+    T, E = logits.shape
+    _check_layout_fits(layout, T, E, k, P, capacity, "moe_route")
+    _check(lib().moe_route(_ptr(logits, torch.float32, "logits"), T, E, k, mode, P, capacity,
+                           _ptr(topk_idx, torch.int32, "topk_idx"), _ptr(gates, torch.float32, "gates"),
+                           _ptr(expert_counts, torch.int32, "expert_counts"),
+                           _ptr(aux_loss, torch.float64, "aux_loss"), _ptr(entropy, torch.float64, "entropy"),
+                           ctypes.byref(layout.c), _ptr(ws, name="ws"), _nbytes(ws), _stream(stream)), "moe_route")
+
+
+def _check_layout_fits(layout: "Layout", T: int, E: int, k: int, P: int, capacity: int, where: str):
+    """Refuse, before the foreign call, a layout call whose sizes exceed the
+    buffers `layout` was allocated for: the kernel writes T*k entries of
+    dst_row / capacity_mask and up to moe_rows_max rows of src_pos."""
+    if E > layout.E or P > layout.P:
+        raise ValueError(f"{where}: layout allocated for E={layout.E}, P={layout.P}, called with E={E}, P={P}")
+    if T < 0 or T * k > layout.A:
+        raise ValueError(f"{where}: T*k = {T * k} assignments, the layout holds {layout.A}")
+    r = moe_rows_max(T, E, k, capacity)
+    if r > layout.r_max:
+        raise ValueError(f"{where}: up to {r} packed rows for T={T}, k={k}, capacity={capacity}; "
+                         f"the layout holds {layout.r_max}")
+
+
 def moe_dispatch_layout(topk_idx, expert_counts, T: int, E: int, k: int, P: int, capacity: int,
                         gates_or_null, layout: "Layout", ws, stream=None) -> None:
+    _check_layout_fits(layout, T, E, k, P, capacity, "moe_dispatch_layout")
     _check(lib().moe_dispatch_layout(_ptr(topk_idx, torch.int32, "topk_idx"),
                                      _ptr(expert_counts, torch.int32, "expert_counts"),
                                      T, E, k, P, capacity,
@@ -207,6 +237,7 @@ def moe_dispatch_layout(topk_idx, expert_counts, T: int, E: int, k: int, P: int,
 
 def moe_dispatch_layout_reassign(topk_idx, expert_counts, T: int, E: int, k: int, P: int, capacity: int,
                                  gates_or_null, layout: "Layout", ws, stream=None) -> None:
+    _check_layout_fits(layout, T, E, k, P, capacity, "moe_dispatch_layout_reassign")
     _check(lib().moe_dispatch_layout_reassign(_ptr(topk_idx, torch.int32, "topk_idx"),
                                               _ptr(expert_counts, torch.int32, "expert_counts"),
                                               T, E, k, P, capacity,
@@ -219,6 +250,7 @@ def moe_dispatch_layout_noalloc(topk_idx, expert_counts, T: int, E: int, k: int,
                                 capacity: int, gates_or_null, layout: "Layout", stream=None) -> None:
     """moe_dispatch_layout without a workspace argument: the library's own
     fixed scratch is used (no device allocation anywhere in the call)."""
+    _check_layout_fits(layout, T, E, k, P, capacity, "moe_dispatch_layout_noalloc")
     _check(lib().moe_dispatch_layout_noalloc(_ptr(topk_idx, torch.int32, "topk_idx"),
                                              _ptr(expert_counts, torch.int32, "expert_counts"),
                                              T, E, k, P, capacity,
@@ -227,8 +259,17 @@ def moe_dispatch_layout_noalloc(topk_idx, expert_counts, T: int, E: int, k: int,
            "moe_dispatch_layout_noalloc")
 
 
+def _check_rows(t, rows: int, name: str, where: str):
+    """A row buffer read or written up to `rows` rows must hold them."""
+    if t is not None and t.shape[0] < rows:
+        raise ValueError(f"{where}: {name} has {t.shape[0]} rows, needs {rows}")
+
+
 def moe_dispatch(x, T: int, H: int, layout: "Layout", fp8: int, packed, scales=None,
                  stream=None) -> None:
+    _check_rows(x, T, "x", "moe_dispatch")
+    _check_rows(packed, layout.c.r_max, "packed", "moe_dispatch")
+    _check_rows(scales, layout.c.r_max, "scales", "moe_dispatch")
     _check(lib().moe_dispatch(_ptr(x, torch.bfloat16, "x"), T, H, ctypes.byref(layout.c), int(fp8),
                               _ptr(packed, torch.uint8 if fp8 else torch.bfloat16, "packed"),
                               _ptr(scales, torch.float32, "scales"), _stream(stream)), "moe_dispatch")
@@ -236,6 +277,8 @@ def moe_dispatch(x, T: int, H: int, layout: "Layout", fp8: int, packed, scales=N
 
 def moe_combine(expert_out, layout: "Layout", gates, shared_out, Ks: int, T: int, H: int, y,
                 stream=None) -> None:
+    _check_rows(expert_out, layout.c.r_max, "expert_out", "moe_combine")
+    _check_rows(y, T, "y", "moe_combine")
     _check(lib().moe_combine(_ptr(expert_out, torch.bfloat16, "expert_out"), ctypes.byref(layout.c),
                              _ptr(gates, torch.float32, "gates"),
                              _ptr(shared_out, torch.bfloat16, "shared_out"), Ks, T, H,
@@ -243,6 +286,8 @@ def moe_combine(expert_out, layout: "Layout", gates, shared_out, Ks: int, T: int
 
 
 def moe_quantize_rows(rows, layout: "Layout", H: int, mode: int, codes, scales, stream=None) -> None:
+    for t, name in ((rows, "rows"), (codes, "codes"), (scales, "scales")):
+        _check_rows(t, layout.c.r_max, name, "moe_quantize_rows")
     _check(lib().moe_quantize_rows(_ptr(rows, torch.bfloat16, "rows"), ctypes.byref(layout.c), H, int(mode),
                                    _ptr(codes, torch.uint8, "codes"), _ptr(scales, torch.float32, "scales"),
                                    _stream(stream)), "moe_quantize_rows")
@@ -250,6 +295,9 @@ def moe_quantize_rows(rows, layout: "Layout", H: int, mode: int, codes, scales, 
 
 def moe_combine_fp8(codes, scales, layout: "Layout", gates, shared_out, Ks: int, T: int, H: int, y,
                     stream=None) -> None:
+    _check_rows(codes, layout.c.r_max, "codes", "moe_combine_fp8")
+    _check_rows(scales, layout.c.r_max, "scales", "moe_combine_fp8")
+    _check_rows(y, T, "y", "moe_combine_fp8")
     _check(lib().moe_combine_fp8(_ptr(codes, torch.uint8, "codes"), _ptr(scales, torch.float32, "scales"),
                                  ctypes.byref(layout.c), _ptr(gates, torch.float32, "gates"),
                                  _ptr(shared_out, torch.bfloat16, "shared_out"), Ks, T, H,
@@ -258,6 +306,9 @@ def moe_combine_fp8(codes, scales, layout: "Layout", gates, shared_out, Ks: int,
 
 def moe_combine_backward(dy, expert_out, layout: "Layout", gates, T: int, H: int, d_expert_out, d_gates,
                          stream=None) -> None:
+    _check_rows(expert_out, layout.c.r_max, "expert_out", "moe_combine_backward")
+    _check_rows(d_expert_out, layout.c.r_max, "d_expert_out", "moe_combine_backward")
+    _check_rows(dy, T, "dy", "moe_combine_backward")
     _check(lib().moe_combine_backward(_ptr(dy, torch.bfloat16, "dy"),
                                       _ptr(expert_out, torch.bfloat16, "expert_out"), ctypes.byref(layout.c),
                                       _ptr(gates, torch.float32, "gates"), T, H,
@@ -267,6 +318,8 @@ def moe_combine_backward(dy, expert_out, layout: "Layout", gates, T: int, H: int
 
 
 def moe_dispatch_backward(d_packed, layout: "Layout", T: int, H: int, dx, stream=None) -> None:
+    _check_rows(d_packed, layout.c.r_max, "d_packed", "moe_dispatch_backward")
+    _check_rows(dx, T, "dx", "moe_dispatch_backward")
     _check(lib().moe_dispatch_backward(_ptr(d_packed, torch.bfloat16, "d_packed"), ctypes.byref(layout.c), T, H,
                                        _ptr(dx, torch.bfloat16, "dx"), _stream(stream)), "moe_dispatch_backward")
 
@@ -284,8 +337,21 @@ def moe_dedup_scratch_size(T: int, P: int) -> int:
     return int(lib().moe_dedup_scratch_size(T, P))
 
 
-def moe_dedup_layout(layout: "Layout", gates, dedup: "Dedup", stream=None) -> None:
-    _check(lib().moe_dedup_layout(ctypes.byref(layout.c), _ptr(gates, torch.float32, "gates"), ctypes.byref(dedup.c),
+def moe_dedup_layout(layout: "Layout", gates, dedup: "Dedup", stream=None, groups: int | None = None) -> None:
+    """Send rows of `layout` per partition, or, with `groups`, per group of
+    E/groups consecutive experts (e.g. one group per rank of an
+    expert-parallel exchange whose ranks own several partitions): the call
+    then sees a copy of the layout struct with P = groups."""
+    c = layout.c
+    if groups is not None and groups != c.P:
+        if groups < 1 or layout.E % groups != 0:
+            raise ValueError(f"groups must divide E = {layout.E}")
+        c = moe_layout.from_buffer_copy(layout.c)
+        c.P = groups
+    if dedup.P != c.P or dedup.T < c.T or dedup.k != c.k:
+        raise ValueError(f"moe_dedup_layout: the send-row buffers hold T={dedup.T}, k={dedup.k}, P={dedup.P}; "
+                         f"the call has T={c.T}, k={c.k}, P={c.P}")
+    _check(lib().moe_dedup_layout(ctypes.byref(c), _ptr(gates, torch.float32, "gates"), ctypes.byref(dedup.c),
                                   _ptr(dedup.scratch, name="scratch"), _nbytes(dedup.scratch), _stream(stream)),
            "moe_dedup_layout")
 
@@ -329,6 +395,9 @@ class Layout:
         self.dst_row = torch.empty(max(T * k, 1), **i32)
         self.capacity_mask = torch.empty(max(T * k, 1), dtype=torch.uint8, device=device)
         self.dropped = torch.empty(1, dtype=torch.int64, device=device)
+        # the sizes the buffers hold: a layout call must not exceed them
+        self.T, self.E, self.k, self.P, self.capacity = T, E, k, P, capacity
+        self.A = T * k
         self.r_max = r_max
         c = moe_layout()
         for name in ("counts", "offsets", "part_rows", "part_offsets", "part_tokens", "src_pos",
@@ -354,6 +423,7 @@ class Dedup:
             raise MoeError(MOE_ERR_UNSUPPORTED, "moe_dedup_scratch_size")
         self.scratch = torch.empty((n + 15) // 16 * 16, dtype=torch.uint8, device=device)
         self.s_max = s_max
+        self.T, self.k, self.P = T, k, P
         c = moe_dedup()
         for name in ("send_offsets", "send_row", "send_token", "slot_local", "slot_gate"):
             setattr(c, name, getattr(self, name).data_ptr())

@@ -1,6 +1,7 @@
 // abi.cu -- the extern "C" entry points declared in include/moe_route.h.
 // Each call validates its arguments on the host (nothing is enqueued when
 // they are bad) and then launches the kernels of one step on `stream`.
+#include <stddef.h>
 #include <stdint.h>
 
 #include <atomic>
@@ -100,7 +101,8 @@ size_t moe_workspace_size(int T, int E, int k, int P)
 {
     if (check_sizes(T, E, k) != MOE_OK) return 0;
     if (P < 1 || P > E || E % P != 0) return 0;
-    return moe::kWsHeaderBytes + (size_t)moe::layout_tiles(T, k) * (size_t)E * sizeof(unsigned long long);
+    const long long lt = moe::layout_tiles(T, k), rt = moe::route_tiles_bound(T);
+    return moe::kWsHeaderBytes + (size_t)(lt > rt ? lt : rt) * (size_t)E * sizeof(unsigned long long);
 }
 
 moe_status moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t stream)
@@ -173,6 +175,42 @@ moe_status moe_dispatch_layout_reassign(const int32_t *topk_idx, const int32_t *
 {
     return dispatch_layout_impl(topk_idx, expert_counts, T, E, k, P, capacity, gates_or_null, L, ws, ws_bytes,
                                 stream, 1);
+}
+
+moe_status moe_route(const float *logits, int T, int E, int k, int mode, int P, int capacity, int32_t *topk_idx,
+                     float *gates, int32_t *expert_counts, double *aux_loss, double *entropy, moe_layout *L,
+                     void *ws, size_t ws_bytes, moe_stream_t stream)
+{
+    // the argument checks of moe_gate and moe_dispatch_layout
+    moe_status st = check_gate_sizes(T, E, k);
+    if (st != MOE_OK) return st;
+    if (mode != MOE_TOPK_SOFTMAX && mode != MOE_SOFTMAX_TOPK) return MOE_ERR_INVALID_ARG;
+    if (P < 1 || P > E || E % P != 0) return MOE_ERR_UNSUPPORTED;
+    if (!expert_counts || !aux_loss || !entropy || !ws || !L) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!logits || !topk_idx || !gates)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(logits) || !aligned16(topk_idx) || !aligned16(gates) || !aligned16(ws))
+        return MOE_ERR_INVALID_ARG;
+    if (!L->counts || !L->offsets || !L->part_rows || !L->part_offsets || !L->part_tokens || !L->dropped ||
+        (T > 0 && (!L->src_pos || !L->dst_row || !L->capacity_mask)))
+        return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < moe_workspace_size(T, E, k, P)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    moe_layout prev = *L;
+    L->T = T;
+    L->E = E;
+    L->k = k;
+    L->P = P;
+    L->capacity = capacity > 0 ? capacity : 0;
+    L->r_max = (int32_t)moe_rows_max(T, E, k, capacity);
+    L->ws = ws;
+    int too_large = 0;
+    const cudaError_t err = moe::launch_route(logits, T, E, k, mode, P, capacity, topk_idx, gates, expert_counts,
+                                              aux_loss, entropy, L, ws, reinterpret_cast<cudaStream_t>(stream),
+                                              &too_large);
+    if (too_large) {
+        *L = prev;  // nothing was enqueued
+        return MOE_ERR_UNSUPPORTED;
+    }
+    return from_cuda(err);
 }
 
 static moe_status check_layout(const moe_layout *L, int T)
@@ -351,6 +389,16 @@ moe_status moe_get_status(void *ws, moe_stream_t stream)
     if (cudaMemcpy(&status, ws, sizeof(status), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
     if (status != 0) {
         if (cudaMemsetAsync(ws, 0, sizeof(status), s) != cudaSuccess) return MOE_ERR_CUDA;
+        if (status == MOE_ERR_TIMEOUT) {
+            // a wait of moe_route expired: its grid barrier may hold arrivals
+            // and totals of the unfinished call; the stream is idle, so
+            // re-arm it (arrivals and both total arrays to zero, generation kept)
+            char *base = static_cast<char *>(ws);
+            if (cudaMemsetAsync(base + offsetof(moe::WsHeader, route_bar), 0, sizeof(unsigned), s) != cudaSuccess ||
+                cudaMemsetAsync(base + offsetof(moe::WsHeader, route_counts), 0,
+                                sizeof(((moe::WsHeader *)nullptr)->route_counts), s) != cudaSuccess)
+                return MOE_ERR_CUDA;
+        }
         if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
     }
     return (moe_status)status;

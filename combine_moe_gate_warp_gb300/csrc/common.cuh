@@ -37,6 +37,12 @@ struct WsHeader {
     // max key (max_word) and min key (min_word) of its rows, zero = empty
     unsigned quant_max[MOE_MAX_EXPERTS];
     unsigned quant_min[MOE_MAX_EXPERTS];
+    // fused route kernel: grid barrier word {generation (high 32 bits),
+    // blocks arrived (low 32)}; the generation's parity selects which of the
+    // two per-expert total arrays a call accumulates into (the other one is
+    // cleared for the next call)
+    unsigned long long route_bar;
+    unsigned route_counts[2][MOE_MAX_EXPERTS];
 };
 static_assert(sizeof(WsHeader) <= 8192, "workspace header must fit 8 KiB");
 constexpr size_t kWsHeaderBytes = 8192;
@@ -72,6 +78,18 @@ __host__ __device__ inline int layout_tiles(long long T, int k)
     const long long tt = layout_tile_tokens(T, k);
     const long long n = (T + tt - 1) / tt;
     return n < 1 ? 1 : (int)n;
+}
+
+// Fused route kernel tiling (gate and layout in one launch, one bounded
+// grid-wide wait): at most kRouteMaxTiles tiles of at least
+// kRouteMinTileTokens tokens, so the workspace's flag words cover it.
+constexpr int kRouteMinTileTokens = 32;
+constexpr int kRouteMaxTiles = 1024;
+__host__ __device__ inline int route_tiles_bound(long long T)
+{
+    long long n = (T + kRouteMinTileTokens - 1) / kRouteMinTileTokens;
+    if (n < 1) n = 1;
+    return n > kRouteMaxTiles ? kRouteMaxTiles : (int)n;
 }
 
 // Flag word: [63:32] epoch, [31:30] state, [29:0] value.

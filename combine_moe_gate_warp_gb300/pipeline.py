@@ -36,6 +36,17 @@ def _check_input(t, dtype, shape, name):
         raise ValueError(f"{name}: expected leading shape {tuple(shape)}, got {tuple(t.shape)}")
 
 
+def _check_packed_rows(t, dtype, r_max, H, name):
+    """A tensor in packed-row order: the kernels read it up to the layout's
+    row count R, which only the device knows, so it must hold r_max >= R
+    rows of H values."""
+    if t.dim() != 2 or t.shape[1] != H:
+        raise ValueError(f"{name}: expected [rows, {H}], got {tuple(t.shape)}")
+    if t.shape[0] < r_max:
+        raise ValueError(f"{name}: {t.shape[0]} rows, the layout may hold up to r_max = {r_max}")
+    _check_input(t, dtype, (), name)
+
+
 class RoutePlan:
     """Buffers and bound arguments of one problem size.  The plan is bound to
     ``stream`` (default: the stream current when it is built); its methods
@@ -85,6 +96,12 @@ class RoutePlan:
         self._layout_args = (self.topk_idx.data_ptr(), self.expert_counts.data_ptr(), s.T, s.E, s.k, s.P,
                              s.capacity, self.gates.data_ptr(), self._Lref, self.ws.data_ptr(),
                              self._ws_bytes, self._sr)
+        self._route_tail = (s.T, s.E, s.k, s.mode, s.P, s.capacity, self.topk_idx.data_ptr(), self.gates.data_ptr(),
+                            self.expert_counts.data_ptr(), self.aux_loss.data_ptr(), self.entropy.data_ptr(),
+                            self._Lref, self.ws.data_ptr(), self._ws_bytes, self._sr)
+        # moe_route (gate + layout in one launch) unless the overflow is
+        # re-assigned, or the batch proves too large for one co-resident grid
+        self.fused_route = not s.reassign
         self._scales_ptr = None if self.scales is None else self.scales.data_ptr()
 
     # the four hot-path calls -------------------------------------------------
@@ -92,6 +109,22 @@ class RoutePlan:
         s = self.shape
         _check_input(logits, torch.float32, (s.T, s.E), "logits")
         abi._check(self._lib.moe_gate(logits.data_ptr(), s.T, s.E, s.k, s.mode, *self._gate_tail), "moe_gate")
+
+    def route(self, logits: torch.Tensor):
+        """The routing of one batch: moe_route (one launch), or moe_gate and
+        then the layout call when the capacity overflow is re-assigned or
+        moe_route declines the batch size (it then enqueues nothing)."""
+        s = self.shape
+        if self.fused_route:
+            _check_input(logits, torch.float32, (s.T, s.E), "logits")
+            rc = self._lib.moe_route(logits.data_ptr(), *self._route_tail)
+            if rc == abi.MOE_OK:
+                return
+            if rc != abi.MOE_ERR_UNSUPPORTED:
+                raise abi.MoeError(rc, "moe_route")
+            self.fused_route = False
+        self.gate(logits)
+        self.dispatch_layout()
 
     def dispatch_layout(self):
         if self.shape.reassign:
@@ -107,9 +140,7 @@ class RoutePlan:
 
     def combine(self, expert_out: torch.Tensor, shared_out: torch.Tensor | None = None):
         s = self.shape
-        _check_input(expert_out, torch.bfloat16, (), "expert_out")
-        if expert_out.shape[-1] != s.H:
-            raise ValueError("expert_out: last dimension must be H")
+        _check_packed_rows(expert_out, torch.bfloat16, self.r_max, s.H, "expert_out")
         sh = None
         if s.Ks:
             _check_input(shared_out, torch.bfloat16, (s.Ks, s.T, s.H), "shared_out")
@@ -121,9 +152,7 @@ class RoutePlan:
         """FP8-encode the expert-output rows (the expert side of the return
         transport) into eo_codes / eo_scales."""
         s = self.shape
-        _check_input(expert_out, torch.bfloat16, (), "expert_out")
-        if expert_out.shape[-1] != s.H:
-            raise ValueError("expert_out: last dimension must be H")
+        _check_packed_rows(expert_out, torch.bfloat16, self.r_max, s.H, "expert_out")
         abi._check(self._lib.moe_quantize_rows(expert_out.data_ptr(), self._Lref, s.H, s.fp8_combine,
                                                self.eo_codes.data_ptr(), self.eo_scales.data_ptr(), self._s),
                    "moe_quantize_rows")
@@ -140,10 +169,9 @@ class RoutePlan:
                    "moe_combine_fp8")
 
     def step(self, logits, x, expert_out, shared_out=None):
-        """gate -> layout -> dispatch -> combine; with FP8 expert outputs the
-        combine is quantise (expert side) -> FP8 combine."""
-        self.gate(logits)
-        self.dispatch_layout()
+        """route (gate + layout) -> dispatch -> combine; with FP8 expert
+        outputs the combine is quantise (expert side) -> FP8 combine."""
+        self.route(logits)
         self.dispatch(x)
         if self.shape.fp8_combine:
             self.quantize_expert_out(expert_out)
@@ -152,9 +180,10 @@ class RoutePlan:
             self.combine(expert_out, shared_out)
 
     def launches_per_step(self) -> int:
-        """Kernel launches of one step (the grouped FP8 modes take two)."""
+        """Kernel launches of one step (routing: one, or two when not fused;
+        the grouped FP8 modes take two)."""
         s = self.shape
-        n = 3 + (2 if s.fp8 in (abi.MOE_FP8_PER_EXPERT, abi.MOE_FP8_GLOBAL) else 1)
+        n = (1 if self.fused_route else 2) + 1 + (2 if s.fp8 in (abi.MOE_FP8_PER_EXPERT, abi.MOE_FP8_GLOBAL) else 1)
         if s.fp8_combine:
             n += 1 + (2 if s.fp8_combine in (abi.MOE_FP8_PER_EXPERT, abi.MOE_FP8_GLOBAL) else 1)
         return n
@@ -174,9 +203,7 @@ class RoutePlan:
         s = self.shape
         self._bwd_buffers()
         _check_input(dy, torch.bfloat16, (s.T, s.H), "dy")
-        _check_input(expert_out, torch.bfloat16, (), "expert_out")
-        if expert_out.shape[-1] != s.H:
-            raise ValueError("expert_out: last dimension must be H")
+        _check_packed_rows(expert_out, torch.bfloat16, self.r_max, s.H, "expert_out")
         abi._check(self._lib.moe_combine_backward(dy.data_ptr(), expert_out.data_ptr(), self._Lref,
                                                   self.gates.data_ptr(), s.T, s.H, self.d_expert_out.data_ptr(),
                                                   self.d_gates.data_ptr(), self._s), "moe_combine_backward")
@@ -185,9 +212,7 @@ class RoutePlan:
         """dx = sum of the gradients of each token's packed copies (fp32)."""
         s = self.shape
         self._bwd_buffers()
-        _check_input(d_packed, torch.bfloat16, (), "d_packed")
-        if d_packed.shape[-1] != s.H:
-            raise ValueError("d_packed: last dimension must be H")
+        _check_packed_rows(d_packed, torch.bfloat16, self.r_max, s.H, "d_packed")
         abi._check(self._lib.moe_dispatch_backward(d_packed.data_ptr(), self._Lref, s.T, s.H, self.dx.data_ptr(),
                                                    self._s), "moe_dispatch_backward")
 
@@ -341,8 +366,7 @@ class RoutePipeline:
         d = i % len(self.plans)
         p = self.plans[d]
         self.route_stream.wait_event(self._done[d])
-        p.gate(logits)
-        p.dispatch_layout()
+        p.route(logits)
         self._routed[d].record(self.route_stream)
         self.data_stream.wait_event(self._routed[d])
         p.dispatch(x)

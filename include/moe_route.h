@@ -109,8 +109,8 @@ typedef struct moe_layout {
     int64_t *dropped;        /* [1]   T*k - R */
 } moe_layout;
 
-/* Bytes of workspace needed by moe_gate and moe_dispatch_layout for these
- * sizes (0 if the sizes are unsupported). */
+/* Bytes of workspace needed by moe_gate, moe_dispatch_layout and
+ * moe_route for these sizes (0 if the sizes are unsupported). */
 size_t moe_workspace_size(int T, int E, int k, int P);
 
 /* Zero a workspace (cudaMemsetAsync on `stream`).  Needed once after
@@ -174,6 +174,31 @@ moe_status moe_dispatch_layout(const int32_t *topk_idx, const int32_t *expert_co
                                int T, int E, int k, int P, int capacity,
                                float *gates_or_null, moe_layout *L,
                                void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_route -- moe_gate followed by moe_dispatch_layout (dropping capacity
+ * or none), in one kernel launch, with exactly their outputs: topk_idx,
+ * gates (dropped slots set to 0), expert_counts, aux_loss, entropy and
+ * every moe_layout array.  [P2] sec. 4.3 fuses the routing kernels (gate,
+ * softmax, top-k) into one launch to cut their latency; here the layout
+ * joins them.  Definitions: those of moe_gate ([P3] ch.1, sec. 2.3; [P2]
+ * sec. 4.1) and moe_dispatch_layout ([P4] sec. 7, 7.5.4, 8.3.A).
+ *
+ *   Arguments: those of moe_gate and of moe_dispatch_layout (gates is the
+ *   layout's gates_or_null), one workspace of moe_workspace_size(T, E, k, P)
+ *   bytes.  Every block of the launch waits once for all the others (to
+ *   learn the per-expert totals before it places rows), so the grid is
+ *   sized to the blocks the GPU holds at once; a batch that would need
+ *   more returns MOE_ERR_UNSUPPORTED before anything is enqueued (use
+ *   moe_gate + moe_dispatch_layout).  That wait is bounded (1 s); if it
+ *   expires, MOE_ERR_TIMEOUT is recorded in the workspace and the outputs
+ *   are incomplete; moe_get_status then also re-arms the workspace, so the
+ *   next call is exact.  Capacity re-assignment is not offered here
+ *   (moe_dispatch_layout_reassign).
+ */
+moe_status moe_route(const float *logits, int T, int E, int k, int mode, int P, int capacity,
+                     int32_t *topk_idx, float *gates, int32_t *expert_counts, double *aux_loss,
+                     double *entropy, moe_layout *L, void *ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
  * moe_dispatch_layout_noalloc -- the same layout as moe_dispatch_layout,
@@ -338,7 +363,11 @@ size_t moe_dedup_scratch_size(int T, int P);
  * within a partition, in token order; a row's slots keep the token's slot
  * order, with local ids (expert - p*E/P) and the gates from `gates` [T, k]
  * (as left by the layout).  `scratch` is caller-owned device memory of
- * moe_dedup_scratch_size(T, P) bytes.
+ * moe_dedup_scratch_size(T, P) bytes.  Only L's T, E, k, P, r_max, ws,
+ * offsets and dst_row are read, so a caller may pass a copy of *L with P
+ * set to any divisor of E up to 16 to group the experts differently from
+ * the layout's partitions: one group per rank of an expert-parallel
+ * exchange whose ranks own several partitions sends a token to a rank once.
  */
 moe_status moe_dedup_layout(const moe_layout *L, const float *gates, moe_dedup *D,
                             void *scratch, size_t scratch_bytes, moe_stream_t stream);

@@ -22,6 +22,23 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
 
 
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """The count of combine outputs beyond one bf16 ulp of the fp64
+    reference in each full comparison (each one within the fp32 summation
+    allowance n * 2^-24 * sum|terms|, else its test failed)."""
+    gu = sys.modules.get("gpu_util")
+    recs = getattr(gu, "ULP_RECORDS", None) if gu else None
+    if not recs:
+        return
+    terminalreporter.section("combine outputs beyond 1 bf16 ulp of the fp64 reference")
+    for name, st in recs:
+        d = st.as_dict()
+        terminalreporter.write_line(
+            f"{name:>24}: {d['beyond_1ulp']} of {d['outputs']} outputs "
+            f"({d['beyond_1ulp'] / max(d['outputs'], 1):.2e}); largest share of the summation allowance "
+            f"used {d['max_allowance_used']:.3f}")
+
+
 def load_golden(name):
     with open(os.path.join(GOLDEN, name)) as f:
         return json.load(f)

@@ -41,8 +41,14 @@ def test_exports_every_declared_symbol(lib):
 
 def test_workspace_and_rows_queries(lib):
     from combine_moe_gate_warp_gb300 import abi
-    assert abi.moe_workspace_size(16384, 16, 2, 4) == 8192 + 32 * 16 * 8    # 1024-assignment tiles
-    assert abi.moe_workspace_size(262144, 64, 8, 8) == 8192 + 256 * 64 * 8   # 8192-assignment tiles
+    # 8 KiB of counters, then one 8-byte flag word per (tile, expert) for the
+    # larger of the layout's tiling (1024..8192 assignments per tile) and
+    # moe_route's bound (tiles of >= 32 tokens, at most 1024 of them)
+    assert abi.moe_workspace_size(16384, 16, 2, 4) == 8192 + 512 * 16 * 8     # route: 16384 / 32 tiles
+    assert abi.moe_workspace_size(262144, 64, 8, 8) == 8192 + 1024 * 64 * 8   # route: 1024 tiles
+    assert abi.moe_workspace_size(2048, 16, 8, 4) == 8192 + 64 * 16 * 8       # route: 2048 / 32 tiles
+    assert abi.moe_workspace_size(100, 16, 2, 4) == 8192 + 4 * 16 * 8         # route: 4 tiles
+    assert abi.moe_workspace_size(1000, 8, 16, 4) == 8192 + 32 * 8 * 8        # both 32 tiles
     assert abi.moe_workspace_size(100, 16, 2, 3) == 0   # P does not divide E
     assert abi.moe_workspace_size(100, 300, 2, 4) == 0  # E too large
     assert abi.moe_rows_max(262144, 64, 8, 40960) == 2097152
@@ -99,3 +105,59 @@ def test_binding_names_match_the_c_abi():
     body = hdr[hdr.index("typedef struct moe_layout {"):hdr.index("} moe_layout;")]
     fields = re.findall(r"\*?(\w+)(?:,|;)", re.sub(r"/\*.*?\*/", "", body, flags=re.S))
     assert [f for f, _ in abi.moe_layout._fields_] == fields
+
+
+def test_layout_wrappers_refuse_sizes_beyond_the_layout(lib):
+    """The binding refuses, before the foreign call, a layout call that would
+    write past the buffers the Layout was allocated for: more assignments
+    (T*k), more packed rows (capacity removed or raised), or another E / P."""
+    import torch
+
+    from combine_moe_gate_warp_gb300 import abi
+    lay = abi.Layout(100, 8, 2, 4, capacity=10, device="cpu")  # r_max = min(200, 8 * 10) = 80
+    assert lay.r_max == 80 and lay.A == 200
+    ids = torch.zeros((300, 2), dtype=torch.int32)
+    cnt = torch.zeros(8, dtype=torch.int32)
+    ws = torch.zeros(1 << 16, dtype=torch.uint8)
+    for fn in (abi.moe_dispatch_layout, abi.moe_dispatch_layout_reassign):
+        with pytest.raises(ValueError, match="assignments"):
+            fn(ids, cnt, 150, 8, 2, 4, 10, None, lay, ws)
+        with pytest.raises(ValueError, match="packed rows"):
+            fn(ids, cnt, 100, 8, 2, 4, 0, None, lay, ws)      # no capacity: up to 200 rows
+        with pytest.raises(ValueError, match="packed rows"):
+            fn(ids, cnt, 100, 8, 2, 4, 11, None, lay, ws)
+        with pytest.raises(ValueError, match="E=8, P=4"):
+            fn(ids, cnt, 100, 8, 2, 8, 10, None, lay, ws)     # more partitions than allocated
+        with pytest.raises(ValueError, match="E=8, P=4"):
+            fn(ids, cnt, 100, 16, 2, 4, 10, None, lay, ws)    # more experts than allocated
+    with pytest.raises(ValueError, match="packed rows"):
+        abi.moe_dispatch_layout_noalloc(ids, cnt, 100, 8, 2, 4, 0, None, lay)
+    # the sizes it was built for pass the check (and stop at the CPU tensors)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        abi.moe_dispatch_layout(ids, cnt, 100, 8, 2, 4, 10, None, lay, ws)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        abi.moe_dispatch_layout(ids, cnt, 40, 8, 2, 4, 0, None, lay, ws)  # fewer tokens, no capacity: 80 rows
+    # consumers: packed-row buffers must hold the layout's r_max rows
+    lay.c.r_max = 80
+    short = torch.zeros((79, 16), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="expert_out has 79 rows"):
+        abi.moe_combine(short, lay, None, None, 0, 100, 16, torch.zeros((100, 16), dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="packed has 79 rows"):
+        abi.moe_dispatch(torch.zeros((100, 16), dtype=torch.bfloat16), 100, 16, lay, 0, short)
+    with pytest.raises(ValueError, match="d_packed has 79 rows"):
+        abi.moe_dispatch_backward(short, lay, 100, 16, torch.zeros((100, 16), dtype=torch.bfloat16))
+
+
+def test_route_plan_requires_r_max_rows():
+    """RoutePlan's combine, quantise and backward calls read packed-row
+    tensors up to R, which only the device knows: fewer than r_max rows are
+    refused on the host."""
+    import torch
+
+    from combine_moe_gate_warp_gb300.pipeline import _check_packed_rows
+    with pytest.raises(ValueError, match="r_max = 80"):
+        _check_packed_rows(torch.zeros((79, 16), dtype=torch.bfloat16), torch.bfloat16, 80, 16, "expert_out")
+    with pytest.raises(ValueError, match=r"\[rows, 16\]"):
+        _check_packed_rows(torch.zeros((80, 8), dtype=torch.bfloat16), torch.bfloat16, 80, 16, "expert_out")
+    with pytest.raises(ValueError, match="CUDA tensor"):  # enough rows: only the device check remains
+        _check_packed_rows(torch.zeros((80, 16), dtype=torch.bfloat16), torch.bfloat16, 80, 16, "expert_out")

@@ -3,7 +3,13 @@ own batch (the oracle stands in for the kernels on CPU), sends each rank
 its partition slice, applies that rank's experts, receives its rows back,
 and combines.  The result must equal the same batch with every expert
 local (no exchange), bit for bit, for world sizes 2 and 4, with and without
-capacity drops, in bf16 and in FP8 (codes and scales travel together)."""
+capacity drops, in bf16 and in FP8 (codes and scales travel together).
+
+The de-duplicated exchange is checked the same way: each token goes to a
+rank once with that rank's expert ids and gates, the receiver expands the
+rows to its experts, combines each row's slots into one partial and sends
+the partials back, and the source's sum of the partials equals the same
+computation with every rank's experts local."""
 import os
 import socket
 
@@ -104,6 +110,121 @@ def test_expert_parallel_exchange(tmp_path, oracle, world, cap, fp8):
         assert np.array_equal(r["y"], r["y_ref"]), "combine after the exchange differs"
     # every row a rank sent was received by someone: totals match
     assert sum(int(r["recv_counts"].sum()) for r in res) == sum(int(r["R"]) for r in res)
+
+
+def _rows_of(codes_or_bits, scales, oracle):
+    """bf16 bits of the rows a receiver feeds its experts: the bf16 rows
+    themselves, or e4m3 codes dequantised (zero + scale * value, fp32, one
+    bf16 rounding) -- the expert's input transform, the same on both sides."""
+    if scales is None:
+        return codes_or_bits
+    n, H = codes_or_bits.shape
+    deq = np.array([[scales[r, 1] + scales[r, 0] * oracle.e4m3_decode(c) for c in codes_or_bits[r]]
+                    for r in range(n)], dtype=np.float32).reshape(n, H)
+    u = deq.view(np.uint32)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def _expand_and_combine(oracle, rows_bits, slot_local, slot_gate, n_experts, expert0, k, H):
+    """A receiver's work on de-duplicated rows: expand them to its experts
+    (the layout of the rows' local slots, -1 = empty), run the experts, and
+    combine each row's slots into one partial row (pinned fp32 order)."""
+    n = slot_local.shape[0]
+    if n == 0:
+        return np.zeros((0, H), np.uint16), None
+    Lr = oracle.layout(slot_local, n_experts, 1, 0, gates_f32=slot_gate)
+    R = Lr["R"]
+    packed = oracle.dispatch_bf16_rows(rows_bits, k, Lr["src_pos"], np.arange(R))
+    eo = np.zeros((max(R, 1), H), np.uint16)
+    for e in range(n_experts):
+        r0, r1 = Lr["offsets"][e], Lr["offsets"][e + 1]
+        eo[r0:r1] = _expert_fn(expert0 + e, packed[r0:r1])
+    partials = oracle.combine_f32order(eo, Lr["gates"], Lr["dst_row"], np.arange(n), n, k)
+    return partials, Lr
+
+
+def _dedup_worker(rank, world, port, out_dir, cap_factor, fp8):
+    """The de-duplicated exchange: send rows with one group per rank (a token
+    goes to a rank once, with that rank's expert ids and gates), the receiver
+    expands, runs its experts and returns one partial per row, the source adds
+    the partials.  Compared with the same computation with every group
+    local (no exchange)."""
+    import sys
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    import torch.distributed as dist
+    import oracle
+    from combine_moe_gate_warp_gb300 import workloads
+    from combine_moe_gate_warp_gb300.ep import ExpertParallelExchange
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    base = workloads.Workload("epd", T=300, H=64, E=16, k=4, P=8, seed=910, capacity_factor=cap_factor)
+    w = workloads.Workload(**{**base.__dict__, "seed": base.seed + 7919 * rank})
+    T, H, E, k = w.T, w.H, w.E, w.k
+    per = E // world
+    logits = workloads.make_logits(w, "cpu").numpy()
+    x = workloads.make_x(w, "cpu").view(torch.int16).numpy().view(np.uint16)
+    idx, g64, *_ = oracle.gate(logits, k, w.mode)
+    L = oracle.layout(idx, E, w.P, w.capacity, gates_f32=g64.astype(np.float32))
+    Do = oracle.dedup_layout(L["dst_row"], L["offsets"], L["gates"], T, E, k, world)
+    S = Do["S"]
+    if fp8:
+        send, scales = oracle.quantize_rows_grouped(x, Do["send_token"].astype(np.int64),
+                                                    np.arange(S, dtype=np.int32), S)
+        send_t, scales_t = torch.from_numpy(send), torch.from_numpy(scales)
+    else:
+        send = x[Do["send_token"]]
+        scales = None
+        send_t, scales_t = torch.from_numpy(send.view(np.int16)).view(torch.bfloat16), None
+    ex = ExpertParallelExchange(E, w.P)
+    rec = ex.dispatch_dedup(send_t, torch.from_numpy(Do["send_offsets"]), torch.from_numpy(Do["slot_local"]),
+                            torch.from_numpy(Do["slot_gate"]), torch.from_numpy(L["counts"]), scales_t)
+    # receiver: only this rank's experts arrive, each slot's count as announced
+    ids = rec.slot_local.numpy()
+    assert ids.shape == (rec.n, k) and np.all((ids >= -1) & (ids < per))
+    rows_in = rec.rows.numpy() if fp8 else rec.rows.view(torch.int16).numpy().view(np.uint16)
+    rows_bits = _rows_of(rows_in, None if rec.scales is None else rec.scales.numpy(), oracle)
+    partials, Lr = _expand_and_combine(oracle, rows_bits, ids, rec.slot_gate.numpy(), per, rank * per, k, H)
+    if Lr is not None:
+        assert np.array_equal(Lr["counts"], rec.expert_counts.numpy())
+    back = ex.combine_dedup(torch.from_numpy(partials.view(np.int16)).view(torch.bfloat16), rec, rows=S)
+    back = back.view(torch.int16).numpy().view(np.uint16)[:S]
+    y = oracle.combine_f32order(back if S else np.zeros((1, H), np.uint16), np.ones((T, world), np.float32),
+                                Do["send_row"].ravel(), np.arange(T), T, world)
+    # the same batch with every group local
+    local = np.zeros((max(S, 1), H), np.uint16)
+    src_bits = _rows_of(send, scales, oracle)
+    for g in range(world):
+        s0, s1 = int(Do["send_offsets"][g]), int(Do["send_offsets"][g + 1])
+        part, _ = _expand_and_combine(oracle, src_bits[s0:s1], Do["slot_local"][s0:s1], Do["slot_gate"][s0:s1],
+                                      per, g * per, k, H)
+        local[s0:s1] = part
+    y_ref = oracle.combine_f32order(local, np.ones((T, world), np.float32), Do["send_row"].ravel(), np.arange(T),
+                                    T, world)
+    np.savez(os.path.join(out_dir, f"d{rank}.npz"), y=y, y_ref=y_ref, back=back, local=local[:S], S=S, R=L["R"],
+             n=rec.n, dropped=L["dropped"])
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world,cap,fp8", [(2, 0.0, False), (4, 1.25, False), (4, 0.0, True), (2, 1.25, True)])
+def test_dedup_exchange(tmp_path, oracle, world, cap, fp8):
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    procs = [ctx.Process(target=_dedup_worker, args=(r, world, port, str(tmp_path), cap, fp8)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(180)
+        assert p.exitcode == 0
+    res = [np.load(tmp_path / f"d{r}.npz") for r in range(world)]
+    for r in res:
+        assert np.array_equal(r["back"], r["local"]), "partials came back to the wrong send rows"
+        assert np.array_equal(r["y"], r["y_ref"]), "combine of the exchanged partials differs"
+        assert int(r["S"]) <= int(r["R"])  # a token goes to a rank at most once
+    # every send row was received once, and fewer rows travel than packed rows
+    assert sum(int(r["n"]) for r in res) == sum(int(r["S"]) for r in res)
+    assert sum(int(r["S"]) for r in res) < sum(int(r["R"]) for r in res)
+    if cap:
+        assert any(int(r["dropped"]) > 0 for r in res)
 
 
 def _short_worker(rank, world, port, out_dir):

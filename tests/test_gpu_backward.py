@@ -14,7 +14,7 @@ import torch
 
 import oracle
 from combine_moe_gate_warp_gb300 import workloads
-from gpu_util import bits, check_gate, check_layout, f_of_bits, run_gpu, sample_rows
+from gpu_util import bits, check_gate, check_layout, chunks, f_of_bits, pmap, run_gpu, split
 
 pytestmark = pytest.mark.gpu
 
@@ -35,65 +35,92 @@ def _gather(t, rows):
     return bits(t.index_select(0, torch.from_numpy(rows.astype(np.int64)).to(t.device)))
 
 
-def _check_backward(w, token_sample=None, seed=11):
+def _check_backward(w, seed=11):
     """Forward on the GPU (gate compared, oracle gates swapped in, layout
     compared), then the backward calls on seeded gradients; the oracle gets
-    its own layout and gates and the same seeded tensors."""
-    rng = np.random.default_rng(seed)
+    its own layout and gates and the same seeded tensors.  Every token is
+    compared, in chunks of tokens over a thread pool."""
     inp = workloads.make_inputs(w, "cuda")
     plan, gates_pre, og, R, eo, status = run_gpu(w, inp)
     assert status == 0
     check_gate(w, plan, gates_pre, og)
     L = check_layout(w, plan, og)
     dy = workloads.make_dy(w, "cuda")
-    dp = workloads.make_d_packed(w, max(R, 1), "cuda")
+    dp = workloads.make_d_packed(w, max(plan.r_max, 1), "cuda")
     dg_in = workloads.make_d_gates(w, "cuda")
     plan.combine_backward(dy, eo)
     plan.gate_backward(inp["logits"], dg_in)
     plan.dispatch_backward(dp)
     assert plan.status() == 0, "device status after the backward"
-    T, k, H, E = w.T, w.k, w.H, w.E
+    T, k, H = w.T, w.k, w.H
     if T == 0:
         return plan
-    toks = np.arange(T, dtype=np.int64) if token_sample is None else sample_rows(T, rng, token_sample)
-    n = toks.size
-    dst = L["dst_row"].reshape(T, k)[toks]
-    need = np.unique(dst[dst >= 0])
-    remap = np.where(dst >= 0, np.searchsorted(need, np.maximum(dst, 0)), -1).astype(np.int32).ravel()
-    dy_c = _gather(dy, toks)
-    g_c = L["gates"][toks]
-    eo_rows = _gather(eo, need) if not w.identity_experts else \
-        (oracle.dispatch_bf16_rows(bits(inp["x"]), k, L["src_pos"], need) if need.size else _gather(eo, need))
+    x_bits = bits(inp["x"]) if w.identity_experts else None
+    logits_all = inp["logits"].cpu().numpy()
+    dg_all = plan.d_gates.cpu().numpy()[:T]
+    dgs_all = dg_in.cpu().numpy()[:T].astype(np.float64)
+    dl_all = plan.d_logits.cpu().numpy()[:T].astype(np.float64)
+    chunk = max(64, (1 << 25) // max(1, k * H))  # ~32 M expert-row values per chunk
+    for toks in chunks(T, chunk):
+        # the rows a chunk needs come off the device on this thread; the
+        # oracle and the comparisons run on the pool
+        dst = L["dst_row"].reshape(T, k)[toks]
+        need = np.unique(dst[dst >= 0])
+        eo_rows = _gather(eo, need) if not w.identity_experts else \
+            (oracle.dispatch_bf16_rows(x_bits, k, L["src_pos"], need) if need.size else _gather(eo, need))
+        got = dict(dy=_gather(dy, toks), d_eo=_gather(plan.d_expert_out, need), dp=_gather(dp, need),
+                   dx=_gather(plan.dx, toks))
+        errs = pmap(lambda sub: _check_backward_tokens(w, L, og, toks, sub, dst, need, eo_rows, got, dg_all,
+                                                       logits_all, dgs_all, dl_all),
+                    split(np.arange(toks.size, dtype=np.int64), 8))
+        errs = [e for e in errs if e]
+        assert not errs, errs[0]
+    return plan
 
+
+def _check_backward_tokens(w, L, og, toks, sub, dst, need, eo_rows, got, dg_all, logits_all, dgs_all, dl_all):
+    """The backward checks for tokens toks[sub]; returns an error message or
+    None (assertion messages do not cross the thread pool well)."""
+    T, k, H, E = w.T, w.k, w.H, w.E
+    t_ids = toks[sub]
+    n = t_ids.size
+    d = dst[sub]
+    remap = np.where(d >= 0, np.searchsorted(need, np.maximum(d, 0)), -1).astype(np.int32).ravel()
+    dy_c = got["dy"][sub]
+    g_c = np.ascontiguousarray(L["gates"][t_ids])
     # combine backward
     d_eo_ref, dg_ref = oracle.combine_backward(dy_c, eo_rows, g_c, remap, np.arange(n), k)
-    got_rows = _gather(plan.d_expert_out, need)
-    kept = dst.ravel() >= 0
-    assert np.array_equal(got_rows[remap[kept]], d_eo_ref[kept]), "d_expert_out differs from the oracle"
-    dg = plan.d_gates.cpu().numpy()[:T][toks]
-    assert np.all(dg.ravel()[~kept] == 0.0), "dropped slots must get a zero gate gradient"
-    eo_c = f_of_bits(eo_rows).astype(np.float64)
-    dyf = f_of_bits(dy_c).astype(np.float64)
+    kept = remap >= 0
+    if not np.array_equal(got["d_eo"][remap[kept]], d_eo_ref[kept]):
+        return "d_expert_out differs from the oracle"
+    dg = dg_all[t_ids]
+    if not np.all(dg.ravel()[~kept] == 0.0):
+        return "dropped slots must get a zero gate gradient"
+    dyf = np.abs(f_of_bits(dy_c).astype(np.float64))
     mag = np.zeros(n * k)
-    for i in np.flatnonzero(kept):
-        mag[i] = np.sum(np.abs(dyf[i // k] * eo_c[remap[i]]))
+    for j in range(k):
+        kj = remap[j::k] >= 0
+        if kj.any():
+            eo_abs = np.abs(f_of_bits(eo_rows[remap[j::k][kj]]).astype(np.float64))
+            mag[j::k][kj] = np.einsum("ih,ih->i", dyf[kj], eo_abs)
     bound = (H / 256 + 14) * 2.0 ** -24 * mag + 1e-30
     err = np.abs(dg.ravel().astype(np.float64) - dg_ref.ravel())
-    assert np.all(err <= bound), f"d_gates outside the fp32 bound: worst {np.max(err / bound)} x bound"
-
+    if not np.all(err <= bound):
+        return f"d_gates outside the fp32 bound: worst {np.max(err / bound)} x bound"
     # dispatch backward
-    dx_ref, dx64 = oracle.dispatch_backward(_gather(dp, need), remap, np.arange(n), k)
-    dx = _gather(plan.dx, toks)
-    assert np.array_equal(dx, dx_ref), f"dx differs from the oracle in {np.sum(dx != dx_ref)} values"
+    dx_ref, dx64 = oracle.dispatch_backward(got["dp"], remap, np.arange(n), k)
+    dx = got["dx"][sub]
+    if not np.array_equal(dx, dx_ref):
+        return f"dx differs from the oracle in {np.sum(dx != dx_ref)} values"
     none_kept = ~kept.reshape(n, k).any(1)
-    assert not np.any(dx[none_kept]), "a token with no kept slot has dx = 0"
-
+    if np.any(dx[none_kept]):
+        return "a token with no kept slot has dx = 0"
     # gate backward on the seeded gate gradients
-    logits = inp["logits"].cpu().numpy()[toks]
-    idx = og[0][toks]
-    dgs = dg_in.cpu().numpy()[toks].astype(np.float64)
+    logits = logits_all[t_ids]
+    idx = og[0][t_ids]
+    dgs = dgs_all[t_ids]
     dl_ref = oracle.gate_backward(logits, idx, dgs, w.mode)
-    dl = plan.d_logits.cpu().numpy()[:T][toks].astype(np.float64)
+    dl = dl_all[t_ids]
     l64 = logits.astype(np.float64)
     sel = np.zeros((n, E), bool)
     np.put_along_axis(sel, idx, True, 1)
@@ -114,10 +141,11 @@ def _check_backward(w, token_sample=None, seed=11):
     mag_l = p * dsel + p * S1
     c = 2.0 * (rng_l + E + k + 8) * 2.0 ** -24
     err = np.abs(dl - dl_ref)
-    assert np.all(err <= c * mag_l + 1e-37), f"d_logits outside the bound: worst {np.max(err / (c * mag_l + 1e-37))}"
-    if w.mode == workloads.TOPK_SOFTMAX:
-        assert np.all(dl[~sel] == 0.0), "unselected experts get no gradient in top-k-then-softmax"
-    return plan
+    if not np.all(err <= c * mag_l + 1e-37):
+        return f"d_logits outside the bound: worst {np.max(err / (c * mag_l + 1e-37))}"
+    if w.mode == workloads.TOPK_SOFTMAX and not np.all(dl[~sel] == 0.0):
+        return "unselected experts get no gradient in top-k-then-softmax"
+    return None
 
 
 SMALL = [
@@ -136,8 +164,8 @@ def test_backward_small_exact(w):
 
 
 @pytest.mark.parametrize("name", ["v2_top2", "fine_shared", "fp8_skewed", "prefill_cap"])
-def test_backward_full_size_sampled(name):
-    _check_backward(W[name], token_sample=400)
+def test_backward_full_size(name):
+    _check_backward(W[name])
 
 
 def _edge(T, H, E, k, P, mode=0, cap=0.0, seed=77, **kw):
@@ -166,7 +194,7 @@ def test_backward_is_deterministic():
     inp = workloads.make_inputs(w, "cuda")
     plan, _, _, R, eo, _ = run_gpu(w, inp)
     dy = workloads.make_dy(w, "cuda")
-    dp = workloads.make_d_packed(w, max(R, 1), "cuda")
+    dp = workloads.make_d_packed(w, max(plan.r_max, 1), "cuda")
     plan.backward(inp["logits"], dy, eo, dp)
     first = (plan.d_gates.clone(), plan.d_logits.clone(), plan.dx.clone(), plan.d_expert_out[:R].clone())
     plan.backward(inp["logits"], dy, eo, dp)

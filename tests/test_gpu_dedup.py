@@ -90,7 +90,7 @@ def _check(w, fp8=0):
         assert np.array_equal(rp.layout.dst_row.cpu().numpy()[:n * k], Lo["dst_row"])
         assert np.array_equal(rp.layout.offsets.cpu().numpy(), Lo["offsets"])
         Rl = Lo["R"]
-        eo = torch.empty((max(Rl, 1), H), dtype=torch.bfloat16, device="cuda")
+        eo = torch.empty((max(rp.r_max, 1), H), dtype=torch.bfloat16, device="cuda")
         local_o = oracle.dispatch_bf16_rows(x_bits[Do["send_token"][s0:s1]], k, Lo["src_pos"], np.arange(Rl))
         eo_o = np.empty_like(local_o)
         for el in range(per):

@@ -108,3 +108,34 @@ def test_lookback_wait_expires_with_timeout_status():
     assert p.status() == abi.MOE_ERR_TIMEOUT
     # the hook is cleared and the workspace usable again
     route_checked(w, p, inp["logits"])
+
+
+def test_route_non_finite_logits_reported():
+    p = _plan()
+    assert p.fused_route
+    logits = torch.randn(600, 16, device="cuda")
+    logits[17, 3] = float("nan")
+    logits[400, 0] = float("inf")
+    p.route(logits)
+    assert p.status() == abi.MOE_ERR_DEVICE_DATA
+    p.route(torch.randn(600, 16, device="cuda"))
+    assert p.status() == 0
+
+
+def test_route_wait_expires_with_timeout_status():
+    """moe_route: tile 1 is told (through the workspace hook, from the host)
+    never to arrive at the grid-wide wait; the other tiles' bounded wait
+    expires after ~1 s and the call reports MOE_ERR_TIMEOUT.  Reading the
+    status re-arms the workspace: the next calls (both parities of the
+    barrier) are exact again."""
+    w = workloads.Workload("timeout_route", T=4096, H=64, E=16, k=2, P=4, seed=13)
+    p = RoutePlan(shape_of(w), "cuda")
+    assert p.fused_route
+    inp = workloads.make_inputs(w, "cuda")
+    route_checked(w, p, inp["logits"])
+    p.ws.view(torch.int32)[3] = 2  # inject_skip_publish (byte offset 12) = tile 1 + 1
+    p.route(inp["logits"])
+    assert p.status() == abi.MOE_ERR_TIMEOUT
+    assert int(p.ws.view(torch.int32)[3].item()) == 0  # the hook was consumed
+    for _ in range(3):
+        route_checked(w, p, inp["logits"])

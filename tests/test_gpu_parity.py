@@ -13,8 +13,8 @@ import torch
 
 import oracle
 from combine_moe_gate_warp_gb300 import workloads
-from gpu_util import (bits, check_combine, check_dispatch, check_gate, check_layout, route_checked, run_gpu,
-                      sample_rows)
+from gpu_util import (bits, check_combine, check_combine_full, check_dispatch, check_dispatch_full, check_gate,
+                      check_layout, route_checked, run_gpu)
 
 pytestmark = pytest.mark.gpu
 
@@ -29,21 +29,23 @@ def _built():
     torch.cuda.init()
 
 
-def _full_check(w, rows_sample=None, token_sample=None, seed=7):
-    rng = np.random.default_rng(seed)
+def _full_check(w, seed=7, fused=None):
+    """Gate, layout, every packed row and every output token of workload w
+    against the oracle; returns the plan, the oracle layout and the
+    beyond-one-ulp statistics of the combine.  fused: routing by moe_route
+    (default where it applies) or by moe_gate + the layout call (False)."""
     inp = workloads.make_inputs(w, "cuda")
-    plan, gates_pre, og, R, eo, status = run_gpu(w, inp)
+    plan, gates_pre, og, R, eo, status = run_gpu(w, inp, fused=fused)
     assert status == 0, f"device status {status}"
     idx, counts = check_gate(w, plan, gates_pre, og)
     assert counts.sum() == w.T * w.k
     L = check_layout(w, plan, og)
     assert L["R"] == R
     x_bits = bits(inp["x"])
-    rows = np.arange(R, dtype=np.int64) if rows_sample is None else sample_rows(R, rng, rows_sample)
-    check_dispatch(w, plan, L, x_bits, rows)
-    toks = np.arange(w.T, dtype=np.int64) if token_sample is None else sample_rows(w.T, rng, token_sample)
-    frac = check_combine(w, plan, L, eo, inp["shared"], toks, x_bits)
-    return plan, L, frac
+    check_dispatch_full(w, plan, L, x_bits)
+    st = check_combine_full(w, plan, L, eo, inp["shared"], x_bits)
+    assert st.outputs == w.T * w.H
+    return plan, L, st
 
 
 # --- small cases: every output compared element by element ----------------
@@ -57,21 +59,42 @@ SMALL = [
 ]
 
 
+ROUTING = [pytest.param(True, id="moe_route"), pytest.param(False, id="gate+layout")]
+
+
+@pytest.mark.parametrize("fused", ROUTING)
 @pytest.mark.parametrize("w", SMALL, ids=[w.name for w in SMALL])
-def test_small_workloads_exact(w):
-    plan, L, frac = _full_check(w)
+def test_small_workloads_exact(w, fused):
+    plan, L, st = _full_check(w, fused=fused)
     if w.identity_experts:
         assert np.array_equal(bits(plan.y), bits(workloads.make_x(w, "cuda")))
 
 
-# --- the full-size workloads: gate and layout in full, dispatch and combine
-# on sampled rows/tokens (first, last and random) --------------------------
+# --- the full-size workloads: every output compared, in chunks ------------
 @pytest.mark.parametrize("name", ["tiny", "v2_top2", "fine_shared", "fp8_skewed", "prefill_cap"])
 def test_full_size_workloads(name):
     w = W[name]
-    plan, L, frac = _full_check(w, rows_sample=600, token_sample=600)
+    plan, L, st = _full_check(w)
     if name == "prefill_cap":
         assert L["dropped"] > 0 and np.all(L["counts"] <= w.capacity)
+
+
+@pytest.mark.parametrize("name", ["v2_top2", "fine_shared", "fp8_skewed", "prefill_cap"])
+def test_full_size_gate_and_layout_calls(name):
+    """The separate moe_gate and moe_dispatch_layout calls at full size (the
+    dispatch and combine do not depend on which routing call ran)."""
+    from combine_moe_gate_warp_gb300 import RoutePlan
+    from gpu_util import gate_with_oracle, poison, shape_of
+    w = W[name]
+    inp = workloads.make_inputs(w, "cuda")
+    plan = RoutePlan(shape_of(w), "cuda")
+    plan.fused_route = False
+    poison(plan)
+    gates_pre, og = gate_with_oracle(w, plan, inp["logits"])
+    plan.dispatch_layout()
+    assert plan.status() == 0
+    check_gate(w, plan, gates_pre, og)
+    check_layout(w, plan, og)
 
 
 # --- edge cases --------------------------------------------------------------
@@ -92,15 +115,17 @@ EDGE = [
 ]
 
 
+@pytest.mark.parametrize("fused", ROUTING)
 @pytest.mark.parametrize("w", EDGE, ids=[w.name for w in EDGE])
-def test_edge_shapes(w):
-    _full_check(w)
+def test_edge_shapes(w, fused):
+    _full_check(w, fused=fused)
 
 
-def test_empty_batch():
+@pytest.mark.parametrize("fused", ROUTING)
+def test_empty_batch(fused):
     w = _custom(0, 64, 8, 2, 4)
     inp = workloads.make_inputs(w, "cuda")
-    plan, gates_pre, og, R, eo, status = run_gpu(w, inp)
+    plan, gates_pre, og, R, eo, status = run_gpu(w, inp, fused=fused)
     assert status == 0 and R == 0
     assert plan.expert_counts.cpu().tolist() == [0] * 8
     assert plan.aux_loss.item() == 0.0 and plan.entropy.item() == 0.0
@@ -108,9 +133,9 @@ def test_empty_batch():
     assert plan.layout.part_tokens.cpu().tolist() == [0] * 4
 
 
-def _run_with_logits(w, logits):
+def _run_with_logits(w, logits, fused=None):
     inp = dict(logits=logits.contiguous(), x=workloads.make_x(w, "cuda"), shared=None)
-    plan, gates_pre, og, R, eo, status = run_gpu(w, inp)
+    plan, gates_pre, og, R, eo, status = run_gpu(w, inp, fused=fused)
     assert status == 0
     check_gate(w, plan, gates_pre, og)
     L = check_layout(w, plan, og)
@@ -119,48 +144,52 @@ def _run_with_logits(w, logits):
     return plan, L
 
 
-def test_ties_and_signed_zeros():
+@pytest.mark.parametrize("fused", ROUTING)
+def test_ties_and_signed_zeros(fused):
     w = _custom(1100, 32, 16, 4, 4)
     g = torch.Generator(device="cuda").manual_seed(5)
     logits = torch.randint(-2, 3, (w.T, w.E), generator=g, device="cuda").float()
     logits[torch.rand((w.T, w.E), generator=g, device="cuda") < 0.2] = -0.0
-    _run_with_logits(w, logits)
+    _run_with_logits(w, logits, fused)
 
 
-# Gate shapes for every way the lanes of a token split its logits: several
-# lanes per token with power-of-two and other k (bitonic and insertion
-# merges), more than one batch of loads per lane, 16-byte loads with one
-# lane (E % 8 != 0), 4-byte loads (E % 4 != 0), and many tiles per block.
-LANE_SPLITS = [
-    _custom(3001, 16, 96, 6, 8),                # 4 lanes, 24 logits each, k = 6
-    _custom(1201, 16, 256, 5, 8, mode=1),       # 8 lanes, two batches, softmax over all E
-    _custom(999, 16, 20, 3, 4),                 # one lane, 16-byte loads, ragged batch
-    _custom(777, 16, 6, 2, 2, mode=1),          # one lane, 4-byte loads
-    _custom(200003, 16, 64, 2, 8),              # more tokens than resident lanes
+# Gate shapes through the one-thread-per-token gate: k not a power of two,
+# long rows (E = 96, 256) staged with 16-byte loads, E % 4 != 0 (4-byte
+# staging loads), a ragged last tile, the SOFTMAX_TOPK mode, and more tokens
+# than the GPU holds resident threads.
+GATE_SHAPES = [
+    _custom(3001, 16, 96, 6, 8),                # k = 6 of 96
+    _custom(1201, 16, 256, 5, 8, mode=1),       # E = 256, softmax over all E
+    _custom(999, 16, 20, 3, 4),                 # E = 20, ragged last tile
+    _custom(777, 16, 6, 2, 2, mode=1),          # E = 6: 4-byte staging loads
+    _custom(200003, 16, 64, 2, 8),              # more tokens than resident threads
 ]
 
 
-@pytest.mark.parametrize("w", LANE_SPLITS, ids=[w.name for w in LANE_SPLITS])
+@pytest.mark.parametrize("fused", ROUTING)
+@pytest.mark.parametrize("w", GATE_SHAPES, ids=[w.name for w in GATE_SHAPES])
 @pytest.mark.parametrize("ties", [False, True])
-def test_gate_lane_splits(w, ties):
+def test_gate_shapes(w, ties, fused):
     if ties:
         g = torch.Generator(device="cuda").manual_seed(w.E)
         logits = torch.randint(-2, 3, (w.T, w.E), generator=g, device="cuda").float()
         logits[torch.rand((w.T, w.E), generator=g, device="cuda") < 0.2] = -0.0
     else:
         logits = workloads.make_inputs(w, "cuda")["logits"]
-    _run_with_logits(w, logits)
+    _run_with_logits(w, logits, fused)
 
 
-def test_ties_many_lanes():
-    """Integer logits with signed zeros where 4 and 8 lanes share a token:
-    equal values cross lanes in the merge."""
+@pytest.mark.parametrize("fused", ROUTING)
+def test_ties_large_k(fused):
+    """Integer logits in {-1, 0, 1} with signed zeros and k up to 16: most of
+    a token's list is made of equal values, so the insertion order decides
+    every position (ties to the lower expert id, -0 == +0)."""
     for E, k in ((64, 8), (256, 16), (128, 4)):
         w = _custom(513, 16, E, k, 8)
         g = torch.Generator(device="cuda").manual_seed(k)
         logits = torch.randint(-1, 2, (w.T, w.E), generator=g, device="cuda").float()
         logits[torch.rand((w.T, w.E), generator=g, device="cuda") < 0.3] = -0.0
-        _run_with_logits(w, logits)
+        _run_with_logits(w, logits, fused)
 
 
 class _with_capacity:

@@ -42,8 +42,8 @@ def test_reassign_small_exact(w):
     assert np.any(L["capacity_mask"] == 2), "the case must re-assign something"
 
 
-def test_reassign_full_size_sampled():
-    plan, L, _ = _full_check(W["prefill_reassign"], rows_sample=600, token_sample=600)
+def test_reassign_full_size():
+    plan, L, _ = _full_check(W["prefill_reassign"])
     assert L["dropped"] == 0 and np.all(L["counts"] <= W["prefill_reassign"].capacity)
 
 

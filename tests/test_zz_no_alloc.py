@@ -81,3 +81,59 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     fake = ctypes.c_void_p(1 << 20)
     rc = lib.moe_dispatch_layout_noalloc(fake, fake, T, E, k, P, 0, None, ctypes.byref(L), None)
     assert rc == abi.MOE_ERR_WORKSPACE_TOO_SMALL
+
+
+class _DeviceWords:
+    """A zero-copy view of device memory at a raw address (the library's
+    scratch), through the CUDA array interface, so the test can write it."""
+
+    def __init__(self, ptr, n):
+        self.__cuda_array_interface__ = {"shape": (n,), "typestr": "<i4", "data": (ptr, False), "version": 3}
+
+
+def test_noalloc_recovers_counters_left_dirty():
+    """The scratch is shared by every call and keeps the last call's
+    contents.  A call that stopped partway could leave its completion
+    counters and partition-token totals non-zero; the entry point clears
+    them before it launches.  Here the host writes such values into the
+    scratch between two calls (no GPU fault involved), and the second call
+    must still report no error and equal the workspace layout."""
+    lib = abi.lib()
+    w = workloads.WORKLOADS["prefill_cap"].scaled(4000)
+    stream = torch.cuda.current_stream()
+    inp = workloads.make_inputs(w, "cuda")
+    plan = RoutePlan(_shape(w), "cuda")
+    plan.gate(inp["logits"])
+    gates_in = plan.gates.clone()
+    plan.dispatch_layout()
+    assert plan.status() == 0
+    L2 = abi.Layout(w.T, w.E, w.k, w.P, w.capacity, "cuda")
+
+    def call():
+        g = gates_in.clone()
+        rc = lib.moe_dispatch_layout_noalloc(
+            ctypes.c_void_p(plan.topk_idx.data_ptr()), ctypes.c_void_p(plan.expert_counts.data_ptr()),
+            w.T, w.E, w.k, w.P, w.capacity, ctypes.c_void_p(g.data_ptr()), ctypes.byref(L2.c),
+            ctypes.c_void_p(stream.cuda_stream))
+        assert rc == abi.MOE_OK
+        assert lib.moe_get_status(ctypes.c_void_p(L2.c.ws), ctypes.c_void_p(stream.cuda_stream)) == 0
+        R = int(plan.layout.offsets[w.E].item())
+        for name in FIELDS:
+            a, b = getattr(plan.layout, name), getattr(L2, name)
+            if name == "src_pos":
+                a, b = a[:R], b[:R]
+            assert torch.equal(a, b), name
+        assert torch.equal(plan.gates.view(torch.int32), g.view(torch.int32))
+
+    call()
+    # scratch header, 32-bit words: [0] status, [1] completed-tile counter,
+    # [2] gate ticket, [3] test hook, [4] tile-id half and [5] epoch half of
+    # the tile/epoch word; the per-partition token totals start at byte 1152
+    words = torch.as_tensor(_DeviceWords(L2.c.ws, 1152 // 4 + w.P), device="cuda")
+    words[1] = 5
+    words[2] = 7
+    words[4] = 3
+    words[1152 // 4:] = 11
+    torch.cuda.synchronize()
+    call()
+    call()
