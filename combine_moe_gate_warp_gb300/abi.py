@@ -96,6 +96,8 @@ def lib():
     L.moe_gate.restype = I
     L.moe_route.argtypes = [P, I, I, I, I, I, I, P, P, P, P, P, ctypes.POINTER(moe_layout), P, SZ, P]
     L.moe_route.restype = I
+    L.moe_route_launches.argtypes = [I, I, I, I, I]
+    L.moe_route_launches.restype = I
     L.moe_dispatch_layout.argtypes = [P, P, I, I, I, I, I, P, ctypes.POINTER(moe_layout), P, SZ, P]
     L.moe_dispatch_layout.restype = I
     L.moe_dispatch_layout_reassign.argtypes = [P, P, I, I, I, I, I, P, ctypes.POINTER(moe_layout), P, SZ, P]
@@ -199,8 +201,8 @@ def moe_gate(logits, k: int, mode: int, topk_idx, gates, expert_counts, aux_loss
 
 def moe_route(logits, k: int, mode: int, P: int, capacity: int, topk_idx, gates, expert_counts, aux_loss, entropy,
               layout: "Layout", ws, stream=None) -> None:
-    """moe_gate + moe_dispatch_layout in one launch (raises MoeError with
-    MOE_ERR_UNSUPPORTED, nothing enqueued, for a batch too large for it)."""
+    """moe_gate + moe_dispatch_layout, in one launch where the batch allows
+    (moe_route_launches)."""
     T, E = logits.shape
     _check_layout_fits(layout, T, E, k, P, capacity, "moe_route")
     _check(lib().moe_route(_ptr(logits, torch.float32, "logits"), T, E, k, mode, P, capacity,
@@ -208,6 +210,12 @@ def moe_route(logits, k: int, mode: int, P: int, capacity: int, topk_idx, gates,
                            _ptr(expert_counts, torch.int32, "expert_counts"),
                            _ptr(aux_loss, torch.float64, "aux_loss"), _ptr(entropy, torch.float64, "entropy"),
                            ctypes.byref(layout.c), _ptr(ws, name="ws"), _nbytes(ws), _stream(stream)), "moe_route")
+
+
+def moe_route_launches(T: int, E: int, k: int, mode: int, P: int) -> int:
+    """Kernel launches moe_route takes for these sizes on the current device
+    (1 fused, 2 gate + layout, 0 unsupported)."""
+    return int(lib().moe_route_launches(T, E, k, mode, P))
 
 
 def _check_layout_fits(layout: "Layout", T: int, E: int, k: int, P: int, capacity: int, where: str):

@@ -101,8 +101,9 @@ size_t moe_workspace_size(int T, int E, int k, int P)
 {
     if (check_sizes(T, E, k) != MOE_OK) return 0;
     if (P < 1 || P > E || E % P != 0) return 0;
-    const long long lt = moe::layout_tiles(T, k), rt = moe::route_tiles_bound(T);
-    return moe::kWsHeaderBytes + (size_t)(lt > rt ? lt : rt) * (size_t)E * sizeof(unsigned long long);
+    // header, the layout's look-back flag words, moe_route's tile histograms
+    return moe::kWsHeaderBytes + (size_t)moe::layout_tiles(T, k) * (size_t)E * sizeof(unsigned long long) +
+           (size_t)moe::route_tiles_bound(T) * (size_t)E * sizeof(unsigned);
 }
 
 moe_status moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t stream)
@@ -194,7 +195,6 @@ moe_status moe_route(const float *logits, int T, int E, int k, int mode, int P, 
         (T > 0 && (!L->src_pos || !L->dst_row || !L->capacity_mask)))
         return MOE_ERR_INVALID_ARG;
     if (ws_bytes < moe_workspace_size(T, E, k, P)) return MOE_ERR_WORKSPACE_TOO_SMALL;
-    moe_layout prev = *L;
     L->T = T;
     L->E = E;
     L->k = k;
@@ -203,14 +203,29 @@ moe_status moe_route(const float *logits, int T, int E, int k, int mode, int P, 
     L->r_max = (int32_t)moe_rows_max(T, E, k, capacity);
     L->ws = ws;
     int too_large = 0;
-    const cudaError_t err = moe::launch_route(logits, T, E, k, mode, P, capacity, topk_idx, gates, expert_counts,
-                                              aux_loss, entropy, L, ws, reinterpret_cast<cudaStream_t>(stream),
-                                              &too_large);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t err = moe::launch_route(logits, T, E, k, mode, P, capacity, topk_idx, gates, expert_counts,
+                                        aux_loss, entropy, L, ws, s, &too_large);
     if (too_large) {
-        *L = prev;  // nothing was enqueued
-        return MOE_ERR_UNSUPPORTED;
+        // nothing enqueued: the batch does not fit the fused kernel's grid;
+        // the gate and layout kernels give the same outputs in two launches
+        err = moe::launch_gate(logits, T, E, k, mode, topk_idx, gates, expert_counts, aux_loss, entropy, ws, s);
+        if (err == cudaSuccess)
+            err = moe::launch_layout(topk_idx, expert_counts, T, E, k, P, capacity, gates, L, ws, s, 0);
     }
     return from_cuda(err);
+}
+
+int moe_route_launches(int T, int E, int k, int mode, int P)
+{
+    if (check_gate_sizes(T, E, k) != MOE_OK) return 0;
+    if (mode != MOE_TOPK_SOFTMAX && mode != MOE_SOFTMAX_TOPK) return 0;
+    if (P < 1 || P > E || E % P != 0) return 0;
+    int too_large = 0;
+    if (moe::launch_route(nullptr, T, E, k, mode, P, 0, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                          nullptr, nullptr, &too_large, true) != cudaSuccess)
+        return 0;
+    return too_large ? 2 : 1;
 }
 
 static moe_status check_layout(const moe_layout *L, int T)

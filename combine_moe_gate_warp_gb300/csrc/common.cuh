@@ -80,9 +80,18 @@ __host__ __device__ inline int layout_tiles(long long T, int k)
     return n < 1 ? 1 : (int)n;
 }
 
+// The route kernel's histogram region: after the layout's flag words.
+__host__ __device__ inline unsigned *ws_route_hist(void *ws, long long T, int k, int E)
+{
+    return reinterpret_cast<unsigned *>(static_cast<char *>(ws) + kWsHeaderBytes +
+                                        (size_t)layout_tiles(T, k) * (size_t)E * sizeof(unsigned long long));
+}
+
 // Fused route kernel tiling (gate and layout in one launch, one bounded
 // grid-wide wait): at most kRouteMaxTiles tiles of at least
-// kRouteMinTileTokens tokens, so the workspace's flag words cover it.
+// kRouteMinTileTokens tokens.  Its per-tile histograms (one 32-bit count per
+// (tile, expert)) live in their own region after the layout's flag words,
+// so neither kernel can mistake the other's words for its own.
 constexpr int kRouteMinTileTokens = 32;
 constexpr int kRouteMaxTiles = 1024;
 __host__ __device__ inline int route_tiles_bound(long long T)

@@ -15,6 +15,7 @@
 #include <climits>
 
 #include "common.cuh"
+#include "tma.cuh"
 
 namespace moe {
 namespace {
@@ -48,10 +49,15 @@ template <int U>
 __global__ void __launch_bounds__(kDispThreads)
 dispatch_bf16_kernel(const uint4 *__restrict__ x, long long T, int nvec, int k,
                      const int32_t *__restrict__ dst_row, int r_max, const int32_t *__restrict__ R_ptr,
-                     uint4 *__restrict__ packed, void *ws)
+                     uint4 *__restrict__ packed, void *ws, int first_wave)
 {
     __shared__ int s_rows[MOE_MAX_TOPK];
     __shared__ int s_n;
+    // the blocks of the first wave (launched while the layout kernel may
+    // still run) ask L2 for their token's row: a hint, safe before the
+    // wait; later blocks start after the layout and skip it
+    if (threadIdx.x == 0 && blockIdx.x < first_wave && blockIdx.x < T)
+        bulk_prefetch_l2(x + blockIdx.x * (long long)nvec, (uint32_t)nvec * 16u);
     pdl_wait();
     pdl_launch_dependents();
     const int rows_valid = min(r_max, __ldg(R_ptr));
@@ -96,10 +102,10 @@ cudaError_t launch_dispatch_bf16(const void *x, int T, int H, const moe_layout *
     const unsigned grid = (unsigned)grid_for(T);
     const uint4 *xp = static_cast<const uint4 *>(x);
     uint4 *pp = static_cast<uint4 *>(packed);
-#define MOE_DISPATCH_BF16(UU)                                                                     \
+#define MOE_DISPATCH_BF16(UU)                                                                                  \
     return launch_pdl(dispatch_bf16_kernel<UU>, dim3(grid), dim3(kDispThreads), 0, s, xp, (long long)T, nvec, \
                       L->k, (const int32_t *)L->dst_row, L->r_max, (const int32_t *)(L->offsets + L->E), pp,  \
-                      L->ws)
+                      L->ws, resident_grid(reinterpret_cast<const void *>(dispatch_bf16_kernel<UU>), kDispThreads, 0))
     if (per_thread <= 1) MOE_DISPATCH_BF16(1);
     else if (per_thread <= 2) MOE_DISPATCH_BF16(2);
     else if (per_thread <= 3) MOE_DISPATCH_BF16(3);

@@ -12,10 +12,11 @@ cudaError_t launch_gate(const float *logits, int T, int E, int k, int mode, int3
                         float *gates, int32_t *expert_counts, double *aux, double *entropy,
                         void *ws, cudaStream_t s);
 // gate + dropping layout in one launch; *too_large = 1 (nothing enqueued)
-// when the batch does not fit one co-resident grid
+// when the batch does not fit the fused kernel's grid; with dry_run only
+// that decision is made (nothing is read or launched)
 cudaError_t launch_route(const float *logits, int T, int E, int k, int mode, int P, int capacity,
                          int32_t *topk_idx, float *gates, int32_t *expert_counts, double *aux, double *entropy,
-                         const moe_layout *L, void *ws, cudaStream_t s, int *too_large);
+                         const moe_layout *L, void *ws, cudaStream_t s, int *too_large, bool dry_run = false);
 cudaError_t launch_layout(const int32_t *topk_idx, const int32_t *counts_in, int T, int E, int k,
                           int P, int capacity, float *gates, const moe_layout *L, void *ws,
                           cudaStream_t s, int reassign = 0);

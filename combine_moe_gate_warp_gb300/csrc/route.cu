@@ -33,19 +33,27 @@
 //
 // Workspace use: the barrier word and two arrays of per-expert totals
 // (selected by the parity of the barrier's generation: a call accumulates
-// into one and clears the other for the next call), and one flag word per
-// (tile, expert) carrying {generation, aggregate, histogram count}.
+// into one and clears the other for the next call), and one 32-bit count per
+// (tile, expert) in a region of its own (the layout kernel's look-back flag
+// words are elsewhere, so the two calls may share a workspace).
 #include <math.h>
 
 #include "common.cuh"
+#include "tma.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kRouteThreads = 256;
+// Tokens per tile: 512 / k, within [32, 256] (measured on GB300: top-2
+// over 16 experts is fastest with 256-token tiles, top-8 over 32 with 32-64:
+// the gate's per-token chain grows with k, so smaller tiles spread the
+// tokens over more SMs).  A batch that would need more tiles than the GPU
+// holds at once does not take the fused kernel (see launch_route).
 constexpr int kRouteWarps = kRouteThreads / 32;
 constexpr int kStageLoads = 8;      // logit loads in flight per thread while staging
-constexpr int kPrefixUnroll = 8;    // flag-word loads in flight per thread in the prefix sums
+constexpr int kPrefixUnroll = 32;   // histogram loads in flight per thread in the prefix sums
+constexpr int kStageBytes = 68 * 1024;  // staging buffer: one round of 256 tokens up to 64 experts
 
 struct RouteArgs {
     const float *logits;
@@ -54,7 +62,8 @@ struct RouteArgs {
     int r_max;           // rows the packed buffers hold
     int tile_tokens;     // tokens per tile (block)
     int ntiles;          // = gridDim.x
-    int round_tokens;    // tokens staged per gate round (<= kRouteThreads)
+    int round_tokens;    // tokens staged per gate round (round_tokens * lanes <= kRouteThreads)
+    int lanes;           // lanes per token in the gate: 1, 2, 4 or 8
     int32_t *topk_idx;
     float *gates;
     int32_t *expert_counts;
@@ -63,6 +72,7 @@ struct RouteArgs {
     uint8_t *cmask;
     int64_t *dropped;
     void *ws;
+    unsigned *hist;      // [ntiles, E] per-tile histograms (the workspace's route region)
 };
 
 __device__ __forceinline__ unsigned long long ld_volatile_u64(const unsigned long long *p)
@@ -75,19 +85,96 @@ __device__ __forceinline__ unsigned ld_volatile_u32(const unsigned *p)
 }
 
 // Insert (v, e) into the descending list bv/bi of length K if it beats the
-// last entry; strictly-greater comparisons keep the lower expert id first
-// on ties (-0.0 == +0.0 is a tie).
+// last entry.  v goes after every entry >= v, so an equal value keeps the
+// lower expert id first (-0.0 == +0.0 is a tie); the position is a count of
+// independent compares and the shift independent selects, a short
+// dependency chain where a compare-and-swap pass would be K - 1 steps long.
 template <int K>
 __device__ __forceinline__ void topk_insert(float (&bv)[K], int (&bi)[K], float v, int e)
 {
     if (v > bv[K - 1]) {
-        bv[K - 1] = v;
-        bi[K - 1] = e;
+        int pos = 0;
+#pragma unroll
+        for (int j = 0; j < K - 1; ++j) pos += (bv[j] >= v) ? 1 : 0;
 #pragma unroll
         for (int j = K - 1; j > 0; --j) {
-            if (bv[j] > bv[j - 1]) {
-                float tv = bv[j]; bv[j] = bv[j - 1]; bv[j - 1] = tv;
-                int ti = bi[j]; bi[j] = bi[j - 1]; bi[j - 1] = ti;
+            // old bv[j - 1] is still in place: j - 1 is updated later
+            bv[j] = j > pos ? bv[j - 1] : (j == pos ? v : bv[j]);
+            bi[j] = j > pos ? bi[j - 1] : (j == pos ? e : bi[j]);
+        }
+        if (pos == 0) {
+            bv[0] = v;
+            bi[0] = e;
+        }
+    }
+}
+
+__host__ __device__ constexpr int pow2_at_least(int k) { return k <= 1 ? 1 : (k <= 2 ? 2 : (k <= 4 ? 4 : (k <= 8 ? 8 : 16))); }
+
+// Strict total order of (logit, expert): the larger logit first, equal
+// logits (-0.0 == +0.0) by the lower expert id.
+__device__ __forceinline__ bool beats(float v1, int i1, float v2, int i2)
+{
+    return v1 > v2 || (v1 == v2 && i1 < i2);
+}
+
+// Sort a list of KP (a power of two) candidates by `beats`, best first:
+// a bitonic sorting network, every index static.
+template <int KP>
+__device__ __forceinline__ void sort_list(float (&bv)[KP], int (&bi)[KP])
+{
+#pragma unroll
+    for (int size = 2; size <= KP; size <<= 1) {
+#pragma unroll
+        for (int st = size >> 1; st > 0; st >>= 1) {
+#pragma unroll
+            for (int j = 0; j < KP; ++j) {
+                const int l = j ^ st;
+                if (l > j) {
+                    const bool best_first = (j & size) == 0;
+                    const bool sw = best_first ? beats(bv[l], bi[l], bv[j], bi[j]) : beats(bv[j], bi[j], bv[l], bi[l]);
+                    if (sw) {
+                        const float tv = bv[j]; bv[j] = bv[l]; bv[l] = tv;
+                        const int ti = bi[j]; bi[j] = bi[l]; bi[l] = ti;
+                    }
+                }
+            }
+        }
+    }
+}
+
+// The G lanes of a token (adjacent lanes, G a power of two) each hold a
+// list of KP candidates sorted by `beats`; after log2(G) butterfly rounds
+// every lane holds the top KP of the union.  A round takes the partner's
+// list, keeps the better of mine[j] and partner[KP-1-j] (the top KP of the
+// two, as a bitonic sequence) and sorts it with a bitonic merge.  The order
+// is total, so both lanes of a pair end with the same list.
+template <int KP>
+__device__ __forceinline__ void merge_lanes(float (&bv)[KP], int (&bi)[KP], int G)
+{
+    for (int m = 1; m < G; m <<= 1) {
+        float pv[KP];
+        int pi[KP];
+#pragma unroll
+        for (int j = 0; j < KP; ++j) {
+            pv[j] = __shfl_xor_sync(0xffffffffu, bv[j], m);
+            pi[j] = __shfl_xor_sync(0xffffffffu, bi[j], m);
+        }
+#pragma unroll
+        for (int j = 0; j < KP; ++j) {
+            if (!beats(bv[j], bi[j], pv[KP - 1 - j], pi[KP - 1 - j])) {
+                bv[j] = pv[KP - 1 - j];
+                bi[j] = pi[KP - 1 - j];
+            }
+        }
+#pragma unroll
+        for (int st = KP / 2; st > 0; st >>= 1) {
+#pragma unroll
+            for (int j = 0; j < KP; ++j) {
+                if ((j & st) == 0 && beats(bv[j + st], bi[j + st], bv[j], bi[j])) {
+                    const float tv = bv[j]; bv[j] = bv[j + st]; bv[j + st] = tv;
+                    const int ti = bi[j]; bi[j] = bi[j + st]; bi[j + st] = ti;
+                }
             }
         }
     }
@@ -146,7 +233,6 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a)
     __shared__ int s_bad, s_abort, s_skip;
 
     WsHeader *ws = static_cast<WsHeader *>(a.ws);
-    unsigned long long *flags = ws_flags(a.ws);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int E = a.E;
     const int tile = blockIdx.x;
@@ -163,6 +249,14 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a)
     for (int p = tid; p < MOE_MAX_EXPERTS; p += kRouteThreads) s_ptok[p] = 0u;
     const int per = E / a.P;
     for (int e = tid; e < E; e += kRouteThreads) s_epart[e] = e / per;
+    if (tid == 0) {
+        // the tile's logits are contiguous: ask L2 for them while the
+        // previous kernel in the stream finishes (a hint, safe before the wait)
+        const char *src = reinterpret_cast<const char *>(a.logits + tok0 * (long long)E);
+        const long long bytes = ((long long)ntok * E * (long long)sizeof(float)) & ~15LL;
+        for (long long o = 0; o < bytes; o += 32768)
+            bulk_prefetch_l2(src + o, (uint32_t)min(32768LL, bytes - o));
+    }
     pdl_wait();
     pdl_launch_dependents();
     if (tid == 0) {
@@ -220,7 +314,74 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a)
             }
         }
         __syncthreads();
-        if (tid < rows) {
+        if (a.lanes > 1) {
+            // G lanes per token: lane `sub` takes a contiguous chunk of the row
+            constexpr int KP = pow2_at_least(K);
+            const int G = a.lanes;
+            const int tk = tid / G, sub = tid - tk * G;
+            const bool active = tk < rows;
+            const float *row = s_stage + (active ? tk : 0) * stride;
+            const int chunk = (E + G - 1) / G;
+            const int e0 = sub * chunk, e1 = min(E, e0 + chunk);
+            float bv[KP];
+            int bi[KP];
+#pragma unroll
+            for (int j = 0; j < KP; ++j) {
+                bv[j] = -INFINITY;
+                bi[j] = 0x40000000 + sub * KP + j;  // empty places: lose to every expert
+            }
+            bool finite = true;
+            if (e1 - e0 <= KP) {
+                // the chunk fits the list: take it whole and sort it
+#pragma unroll
+                for (int j = 0; j < KP; ++j) {
+                    if (e0 + j < e1) {
+                        bv[j] = row[e0 + j];
+                        bi[j] = e0 + j;
+                        finite &= isfinite(bv[j]);
+                    }
+                }
+                sort_list<KP>(bv, bi);
+            } else {
+                for (int e = e0; e < e1; ++e) {
+                    const float v = row[e];
+                    finite &= isfinite(v);
+                    topk_insert<KP>(bv, bi, v, e);
+                }
+            }
+            merge_lanes<KP>(bv, bi, G);
+            const float m = bv[0];
+            // the softmax denominator: SOFTMAX_TOPK over every logit (each lane
+            // its chunk), TOPK_SOFTMAX over the selected ones (each lane the
+            // slots j = sub, sub + G, ...); then a butterfly over the G lanes
+            // (every lane adds the same pairs, so every lane has the same total)
+            float part = 0.0f;
+            if constexpr (MODE != MOE_TOPK_SOFTMAX) {
+                for (int e = e0; e < e1; ++e) part = __fadd_rn(part, expf(__fsub_rn(row[e], m)));
+            } else {
+#pragma unroll
+                for (int j = 0; j < K; ++j)
+                    if (j % G == sub) part = __fadd_rn(part, expf(__fsub_rn(bv[j], m)));
+            }
+            for (int mm = 1; mm < G; mm <<= 1) part = __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, mm));
+            if (active) {
+                if (!finite) s_bad = 1;
+                const long long t = tok0 + r0 + tk;
+                int *si = s_idx + (r0 + tk) * K;
+#pragma unroll
+                for (int j = 0; j < K; ++j) {
+                    if (j % G != sub) continue;  // lane `sub` writes slots sub, sub + G, ...
+                    int id = bi[j];
+                    if (id < 0 || id >= E) {  // only with non-finite logits (already reported)
+                        id = 0;
+                        s_bad = 1;
+                    }
+                    a.topk_idx[t * K + j] = id;
+                    a.gates[t * K + j] = __fdiv_rn(expf(__fsub_rn(bv[j], m)), part);
+                    si[j] = id;
+                }
+            }
+        } else if (tid < rows) {
             const float *row = s_stage + tid * stride;
             float bv[K];
             int bi[K];
@@ -311,8 +472,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a)
             s_whist[w][tid] = agg;
             agg += v;
         }
-        *reinterpret_cast<volatile unsigned long long *>(flags + (size_t)tile * E + tid) =
-            make_flag(gen, kFlagAggregate, agg);
+        *reinterpret_cast<volatile unsigned *>(a.hist + (size_t)tile * E + tid) = agg;
         if (agg) atomicAdd(&ws->route_counts[parity][tid], agg);
     }
     if (tile == 0) {
@@ -362,21 +522,17 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a)
         const int W = kRouteThreads / E;  // threads per expert
         const int my_e = tid % E, my_w = tid / E;
         if (my_w < W) {
+            // every tile wrote its histogram before arriving: all are this call's
             unsigned add = 0;
             for (int b0 = my_w; b0 < tile; b0 += W * kPrefixUnroll) {
-                unsigned long long f[kPrefixUnroll];
+                unsigned h[kPrefixUnroll];
 #pragma unroll
                 for (int u = 0; u < kPrefixUnroll; ++u) {
                     const int b = b0 + u * W;
-                    f[u] = b < tile ? ld_volatile_u64(flags + (size_t)b * E + my_e)
-                                    : make_flag(gen, kFlagAggregate, 0u);
+                    h[u] = b < tile ? ld_volatile_u32(a.hist + (size_t)b * E + my_e) : 0u;
                 }
 #pragma unroll
-                for (int u = 0; u < kPrefixUnroll; ++u) {
-                    if ((unsigned)(f[u] >> 32) != gen || ((unsigned)(f[u] >> 30) & 3u) != (unsigned)kFlagAggregate)
-                        s_bad = 1;  // a histogram of another call: cannot happen after the wait
-                    add += (unsigned)(f[u] & 0x3FFFFFFFull);
-                }
+                for (int u = 0; u < kPrefixUnroll; ++u) add += h[u];
             }
             s_part_add[tid] = add;
         }
@@ -407,36 +563,45 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a)
     }
     __syncthreads();
 
-    // ---- rows: one thread per token; a token counts once for every
-    // partition that holds one of its kept slots --------------------------
+    // ---- rows: one thread per assignment (rank -> row, kept or dropped),
+    // written out at once; s_rank[i] becomes the row or -1 --------------
+    for (int i = tid; i < A; i += kRouteThreads) {
+        const int e = s_idx[i];
+        const unsigned pr = (unsigned)s_rank[i];
+        const unsigned r = s_excl[e] + s_whist[pr >> 24][e] + (pr & 0xFFFFFFu);
+        int row = -1;
+        if (r < a.cap) {
+            const int cand = s_off[e] + (int)r;
+            if (cand < s_off[e + 1] && cand < a.r_max) row = cand;
+            else s_bad = 1;  // keep writes in bounds
+        }
+        s_rank[i] = row;
+        const long long as = tok0 * K + i;
+        a.dst_row[as] = row;
+        a.cmask[as] = (uint8_t)(row >= 0 ? 1 : 0);
+        if (row >= 0) a.src_pos[row] = (int32_t)as;
+        else a.gates[as] = 0.0f;
+    }
+    __syncthreads();
+    // a token counts once for every partition that holds one of its kept slots
     for (int tb = 0; tb < ntok; tb += kRouteThreads) {
         const int tl = tb + tid;
         unsigned long long pmask = 0ull;
         if (tl < ntok) {
+#pragma unroll
             for (int j = 0; j < K; ++j) {
                 const int i = tl * K + j;
-                const int e = s_idx[i];
-                const unsigned pr = (unsigned)s_rank[i];
-                const unsigned r = s_excl[e] + s_whist[pr >> 24][e] + (pr & 0xFFFFFFu);
-                int row = -1;
-                if (r < a.cap) {
-                    const int cand = s_off[e] + (int)r;
-                    if (cand < s_off[e + 1] && cand < a.r_max) row = cand;
-                    else s_bad = 1;  // keep writes in bounds
-                }
-                s_rank[i] = row;
-                if (row >= 0) {
-                    const int p = s_epart[e];
-                    if (a.P <= 64) {
-                        pmask |= 1ull << p;
-                    } else {
-                        bool first = true;
-                        for (int jj = 0; jj < j; ++jj) {
-                            const int ii = tl * K + jj;
-                            if (s_rank[ii] >= 0 && s_epart[s_idx[ii]] == p) { first = false; break; }
-                        }
-                        if (first) atomicAdd(&s_ptok[p], 1u);
+                if (s_rank[i] < 0) continue;
+                const int p = s_epart[s_idx[i]];
+                if (a.P <= 64) {
+                    pmask |= 1ull << p;
+                } else {
+                    bool first = true;
+                    for (int jj = 0; jj < j; ++jj) {
+                        const int ii = tl * K + jj;
+                        if (s_rank[ii] >= 0 && s_epart[s_idx[ii]] == p) { first = false; break; }
                     }
+                    if (first) atomicAdd(&s_ptok[p], 1u);
                 }
             }
         }
@@ -445,16 +610,6 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a)
     __syncthreads();
     for (int p = tid; p < a.P; p += kRouteThreads)
         if (s_ptok[p]) atomicAdd(reinterpret_cast<unsigned *>(a.part_tokens + p), s_ptok[p]);
-
-    // outputs of this tile
-    for (int i = tid; i < A; i += kRouteThreads) {
-        const long long as = tok0 * K + i;
-        const int row = s_rank[i];
-        a.dst_row[as] = row;
-        a.cmask[as] = (uint8_t)(row >= 0 ? 1 : 0);
-        if (row >= 0) a.src_pos[row] = (int32_t)as;
-        else a.gates[as] = 0.0f;
-    }
 
     if (tile == 0) {
         // the per-expert / per-partition summary and the statistics:
@@ -525,46 +680,60 @@ size_t route_smem(int tile_tokens, int K, int round_tokens, int E)
 }
 
 template <int K, int MODE>
-cudaError_t launch_k(RouteArgs a, cudaStream_t s, int *too_large)
+cudaError_t launch_k(RouteArgs a, cudaStream_t s, int *too_large, bool dry_run)
 {
     const void *fn = reinterpret_cast<const void *>(route_kernel<K, MODE>);
     const int stride = a.E | 1;
-    // gate rounds: a staging buffer of at most 64 KiB
+    // gate rounds: a staging buffer of at most kStageBytes
     int rt = kRouteThreads;
-    while (rt > 32 && (size_t)rt * stride * sizeof(float) > 64 * 1024) rt >>= 1;
-    // tiles: about two per SM, at least kRouteMinTileTokens tokens each, and
-    // never more than the blocks the GPU holds at once (the wait needs them all)
-    const int sms = device_sm_count();
-    long long tt = ((long long)a.T + 2LL * sms - 1) / (2LL * sms);
+    while (rt > 32 && (size_t)rt * stride * sizeof(float) > kStageBytes) rt >>= 1;
+    // tiles of 512 / K tokens (at most one gate round per thread) while the
+    // grid fits the GPU at once (the wait needs every block), else larger
+    long long tt = 512 / K;
+    if (tt > kRouteThreads) tt = kRouteThreads;
+    if (tt > a.T) tt = a.T;
     tt = (tt + kRouteMinTileTokens - 1) / kRouteMinTileTokens * kRouteMinTileTokens;
     if (tt < kRouteMinTileTokens) tt = kRouteMinTileTokens;
     while (true) {
         long long ntiles = ((long long)a.T + tt - 1) / tt;
         if (ntiles < 1) ntiles = 1;
         const size_t smem = route_smem((int)tt, K, (int)min((long long)rt, tt), a.E);
-        if (smem > 200 * 1024 || tt > (1LL << 24)) {  // the batch does not fit one launch
-            *too_large = 1;
-            return cudaSuccess;
-        }
         cudaError_t err = allow_dynamic_smem(fn, (int)smem);
         if (err != cudaSuccess) return err;
         const int resident = resident_grid(fn, kRouteThreads, smem);
         if (ntiles <= resident && ntiles <= kRouteMaxTiles) {
+            if (dry_run) return cudaSuccess;
             a.tile_tokens = (int)tt;
             a.ntiles = (int)ntiles;
-            a.round_tokens = (int)min((long long)rt, tt);
+            // a small tile spreads each token over up to 8 lanes, so that
+            // every thread of the block works on the gate
+            int lanes = 1;
+            while (lanes < 8 && (long long)lanes * 2 * tt <= kRouteThreads && lanes * 2 <= a.E) lanes *= 2;
+            a.lanes = lanes;
+            a.round_tokens = (int)min((long long)rt, min(tt, (long long)(kRouteThreads / lanes)));
             return launch_pdl(route_kernel<K, MODE>, dim3((unsigned)ntiles), dim3(kRouteThreads), smem, s, a);
         }
-        tt += tt;  // fewer, larger tiles
+        if (smem > 160 * 1024) {
+            // the tile's ids and ranks no longer fit beside the staging
+            // buffer: the separate gate and layout kernels take the batch
+            *too_large = 1;
+            return cudaSuccess;
+        }
+        // fewer, larger tiles (several gate rounds per block).  On its own
+        // such a batch is routed faster by the separate kernels (262144
+        // tokens, 64 experts, top-8: 102 vs 85 us on GB300), but beside the
+        // previous batch's copies the fused kernel disturbs them less (per
+        // pipelined batch 2836-2845 vs 2898 us), so it keeps the batch.
+        tt += tt;
     }
 }
 
 template <int MODE>
-cudaError_t launch_mode(const RouteArgs &a, int k, cudaStream_t s, int *too_large)
+cudaError_t launch_mode(const RouteArgs &a, int k, cudaStream_t s, int *too_large, bool dry_run)
 {
     switch (k) {
 #define MOE_ROUTE_CASE(KK) \
-    case KK: return launch_k<KK, MODE>(a, s, too_large);
+    case KK: return launch_k<KK, MODE>(a, s, too_large, dry_run);
         MOE_ROUTE_CASE(1) MOE_ROUTE_CASE(2) MOE_ROUTE_CASE(3) MOE_ROUTE_CASE(4)
         MOE_ROUTE_CASE(5) MOE_ROUTE_CASE(6) MOE_ROUTE_CASE(7) MOE_ROUTE_CASE(8)
         MOE_ROUTE_CASE(9) MOE_ROUTE_CASE(10) MOE_ROUTE_CASE(11) MOE_ROUTE_CASE(12)
@@ -578,10 +747,17 @@ cudaError_t launch_mode(const RouteArgs &a, int k, cudaStream_t s, int *too_larg
 
 cudaError_t launch_route(const float *logits, int T, int E, int k, int mode, int P, int capacity,
                          int32_t *topk_idx, float *gates, int32_t *expert_counts, double *aux, double *entropy,
-                         const moe_layout *L, void *ws, cudaStream_t s, int *too_large)
+                         const moe_layout *L, void *ws, cudaStream_t s, int *too_large, bool dry_run)
 {
     *too_large = 0;
-    RouteArgs a;
+    RouteArgs a = {};
+    if (dry_run) {  // only the tiling decision (no pointers are read)
+        a.T = T;
+        a.E = E;
+        a.P = P;
+        if (mode == MOE_TOPK_SOFTMAX) return launch_mode<MOE_TOPK_SOFTMAX>(a, k, s, too_large, true);
+        return launch_mode<MOE_SOFTMAX_TOPK>(a, k, s, too_large, true);
+    }
     a.logits = logits;
     a.T = T;
     a.E = E;
@@ -604,8 +780,9 @@ cudaError_t launch_route(const float *logits, int T, int E, int k, int mode, int
     a.cmask = L->capacity_mask;
     a.dropped = L->dropped;
     a.ws = ws;
-    if (mode == MOE_TOPK_SOFTMAX) return launch_mode<MOE_TOPK_SOFTMAX>(a, k, s, too_large);
-    return launch_mode<MOE_SOFTMAX_TOPK>(a, k, s, too_large);
+    a.hist = ws_route_hist(ws, T, k, E);
+    if (mode == MOE_TOPK_SOFTMAX) return launch_mode<MOE_TOPK_SOFTMAX>(a, k, s, too_large, false);
+    return launch_mode<MOE_SOFTMAX_TOPK>(a, k, s, too_large, false);
 }
 
 }  // namespace moe

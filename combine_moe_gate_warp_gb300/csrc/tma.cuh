@@ -83,6 +83,16 @@ __device__ __forceinline__ void bulk_load(void *dst_smem, const void *src_gmem, 
         : "memory");
 }
 
+// Hint: start bringing `bytes` (a multiple of 16, 16-byte aligned, all
+// inside one allocation) of global memory into L2.  L2 is where every SM's
+// writes land, so a line prefetched before its producer has finished
+// writing it is updated there, and a later load still sees the final data:
+// a kernel may issue this for its inputs before griddepcontrol.wait.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src_gmem, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src_gmem), "r"(bytes) : "memory");
+}
+
 // shared -> global bulk copy in the issuing thread's current bulk group.
 __device__ __forceinline__ void bulk_store(void *dst_gmem, const void *src_smem, uint32_t bytes)
 {

@@ -99,8 +99,8 @@ class RoutePlan:
         self._route_tail = (s.T, s.E, s.k, s.mode, s.P, s.capacity, self.topk_idx.data_ptr(), self.gates.data_ptr(),
                             self.expert_counts.data_ptr(), self.aux_loss.data_ptr(), self.entropy.data_ptr(),
                             self._Lref, self.ws.data_ptr(), self._ws_bytes, self._sr)
-        # moe_route (gate + layout in one launch) unless the overflow is
-        # re-assigned, or the batch proves too large for one co-resident grid
+        # moe_route (gate + layout, one launch where the batch allows) unless
+        # the overflow is re-assigned
         self.fused_route = not s.reassign
         self._scales_ptr = None if self.scales is None else self.scales.data_ptr()
 
@@ -111,18 +111,13 @@ class RoutePlan:
         abi._check(self._lib.moe_gate(logits.data_ptr(), s.T, s.E, s.k, s.mode, *self._gate_tail), "moe_gate")
 
     def route(self, logits: torch.Tensor):
-        """The routing of one batch: moe_route (one launch), or moe_gate and
-        then the layout call when the capacity overflow is re-assigned or
-        moe_route declines the batch size (it then enqueues nothing)."""
+        """The routing of one batch: moe_route, or moe_gate and then the
+        layout call when the capacity overflow is re-assigned."""
         s = self.shape
         if self.fused_route:
             _check_input(logits, torch.float32, (s.T, s.E), "logits")
-            rc = self._lib.moe_route(logits.data_ptr(), *self._route_tail)
-            if rc == abi.MOE_OK:
-                return
-            if rc != abi.MOE_ERR_UNSUPPORTED:
-                raise abi.MoeError(rc, "moe_route")
-            self.fused_route = False
+            abi._check(self._lib.moe_route(logits.data_ptr(), *self._route_tail), "moe_route")
+            return
         self.gate(logits)
         self.dispatch_layout()
 
@@ -183,7 +178,8 @@ class RoutePlan:
         """Kernel launches of one step (routing: one, or two when not fused;
         the grouped FP8 modes take two)."""
         s = self.shape
-        n = (1 if self.fused_route else 2) + 1 + (2 if s.fp8 in (abi.MOE_FP8_PER_EXPERT, abi.MOE_FP8_GLOBAL) else 1)
+        route = abi.moe_route_launches(s.T, s.E, s.k, s.mode, s.P) if self.fused_route else 2
+        n = route + 1 + (2 if s.fp8 in (abi.MOE_FP8_PER_EXPERT, abi.MOE_FP8_GLOBAL) else 1)
         if s.fp8_combine:
             n += 1 + (2 if s.fp8_combine in (abi.MOE_FP8_PER_EXPERT, abi.MOE_FP8_GLOBAL) else 1)
         return n

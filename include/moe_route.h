@@ -177,20 +177,22 @@ moe_status moe_dispatch_layout(const int32_t *topk_idx, const int32_t *expert_co
 
 /*
  * moe_route -- moe_gate followed by moe_dispatch_layout (dropping capacity
- * or none), in one kernel launch, with exactly their outputs: topk_idx,
- * gates (dropped slots set to 0), expert_counts, aux_loss, entropy and
- * every moe_layout array.  [P2] sec. 4.3 fuses the routing kernels (gate,
- * softmax, top-k) into one launch to cut their latency; here the layout
- * joins them.  Definitions: those of moe_gate ([P3] ch.1, sec. 2.3; [P2]
- * sec. 4.1) and moe_dispatch_layout ([P4] sec. 7, 7.5.4, 8.3.A).
+ * or none), with exactly their outputs: topk_idx, gates (dropped slots set
+ * to 0), expert_counts, aux_loss, entropy and every moe_layout array, in
+ * one kernel launch where the batch allows.  [P2] sec. 4.3 fuses the
+ * routing kernels (gate, softmax, top-k) into one launch to cut their
+ * latency; here the layout joins them.  Definitions: those of moe_gate
+ * ([P3] ch.1, sec. 2.3; [P2] sec. 4.1) and moe_dispatch_layout ([P4] sec.
+ * 7, 7.5.4, 8.3.A).
  *
  *   Arguments: those of moe_gate and of moe_dispatch_layout (gates is the
  *   layout's gates_or_null), one workspace of moe_workspace_size(T, E, k, P)
- *   bytes.  Every block of the launch waits once for all the others (to
- *   learn the per-expert totals before it places rows), so the grid is
- *   sized to the blocks the GPU holds at once; a batch that would need
- *   more returns MOE_ERR_UNSUPPORTED before anything is enqueued (use
- *   moe_gate + moe_dispatch_layout).  That wait is bounded (1 s); if it
+ *   bytes.  In the fused kernel every block waits once for all the others
+ *   (to learn the per-expert totals before it places rows), so its grid is
+ *   sized to the blocks the GPU holds at once (larger tiles for larger
+ *   batches); a batch whose tiles would not fit in shared memory runs the
+ *   kernels of moe_gate and moe_dispatch_layout instead (two launches, the
+ *   same outputs; moe_route_launches tells which).  The wait is bounded (1 s); if it
  *   expires, MOE_ERR_TIMEOUT is recorded in the workspace and the outputs
  *   are incomplete; moe_get_status then also re-arms the workspace, so the
  *   next call is exact.  Capacity re-assignment is not offered here
@@ -199,6 +201,11 @@ moe_status moe_dispatch_layout(const int32_t *topk_idx, const int32_t *expert_co
 moe_status moe_route(const float *logits, int T, int E, int k, int mode, int P, int capacity,
                      int32_t *topk_idx, float *gates, int32_t *expert_counts, double *aux_loss,
                      double *entropy, moe_layout *L, void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Kernel launches moe_route takes for these sizes on the current device: 1
+ * (the fused kernel) or 2 (gate and layout kernels); 0 if unsupported.
+ * Queries the device's occupancy; enqueues nothing. */
+int moe_route_launches(int T, int E, int k, int mode, int P);
 
 /*
  * moe_dispatch_layout_noalloc -- the same layout as moe_dispatch_layout,

@@ -41,14 +41,14 @@ def test_exports_every_declared_symbol(lib):
 
 def test_workspace_and_rows_queries(lib):
     from combine_moe_gate_warp_gb300 import abi
-    # 8 KiB of counters, then one 8-byte flag word per (tile, expert) for the
-    # larger of the layout's tiling (1024..8192 assignments per tile) and
-    # moe_route's bound (tiles of >= 32 tokens, at most 1024 of them)
-    assert abi.moe_workspace_size(16384, 16, 2, 4) == 8192 + 512 * 16 * 8     # route: 16384 / 32 tiles
-    assert abi.moe_workspace_size(262144, 64, 8, 8) == 8192 + 1024 * 64 * 8   # route: 1024 tiles
-    assert abi.moe_workspace_size(2048, 16, 8, 4) == 8192 + 64 * 16 * 8       # route: 2048 / 32 tiles
-    assert abi.moe_workspace_size(100, 16, 2, 4) == 8192 + 4 * 16 * 8         # route: 4 tiles
-    assert abi.moe_workspace_size(1000, 8, 16, 4) == 8192 + 32 * 8 * 8        # both 32 tiles
+    # 8 KiB of counters, one 8-byte look-back flag word per (layout tile,
+    # expert) (tiles of 1024..8192 assignments), then one 4-byte histogram
+    # word per (moe_route tile, expert) (tiles of >= 32 tokens, at most 1024)
+    assert abi.moe_workspace_size(16384, 16, 2, 4) == 8192 + 32 * 16 * 8 + 512 * 16 * 4
+    assert abi.moe_workspace_size(262144, 64, 8, 8) == 8192 + 256 * 64 * 8 + 1024 * 64 * 4
+    assert abi.moe_workspace_size(2048, 16, 8, 4) == 8192 + 16 * 16 * 8 + 64 * 16 * 4
+    assert abi.moe_workspace_size(100, 16, 2, 4) == 8192 + 1 * 16 * 8 + 4 * 16 * 4
+    assert abi.moe_workspace_size(1000, 8, 16, 4) == 8192 + 16 * 8 * 8 + 32 * 8 * 4
     assert abi.moe_workspace_size(100, 16, 2, 3) == 0   # P does not divide E
     assert abi.moe_workspace_size(100, 300, 2, 4) == 0  # E too large
     assert abi.moe_rows_max(262144, 64, 8, 40960) == 2097152

@@ -333,3 +333,20 @@ def test_repeated_calls_reuse_workspace():
         route_checked(wr, plan, inp["logits"])
         plan.dispatch(inp["x"])
         assert plan.status() == 0
+
+
+def test_mixed_routing_calls_share_a_workspace():
+    """moe_route and moe_gate + moe_dispatch_layout alternate on one plan's
+    workspace (their cross-block words live in separate regions): every
+    call matches the oracle."""
+    from combine_moe_gate_warp_gb300 import RoutePlan
+    from gpu_util import gate_with_oracle, shape_of
+    w = W["prefill_cap"].scaled(6000)
+    plan = RoutePlan(shape_of(w), "cuda")
+    for rep in range(6):
+        wr = workloads.Workload(**{**w.__dict__, "seed": 700 + rep})
+        inp = workloads.make_inputs(wr, "cuda")
+        plan.fused_route = rep % 2 == 0
+        route_checked(wr, plan, inp["logits"])
+        plan.dispatch(inp["x"])
+        assert plan.status() == 0
