@@ -229,8 +229,8 @@ def kernel_sources(name: str, w=None) -> tuple:
     fp8 = bool(w is not None and w.fp8)
     fp8c = bool(w is not None and w.fp8_combine)
     table = {
-        "gate": ("gate.cu",), "layout": ("layout.cu",), "route": ("route.cu",),
-        "dispatch": ("quant.cu", "fp8.cuh", "tma.cuh") if fp8 else ("dispatch.cu",),
+        "gate": ("gate.cu",), "layout": ("layout.cu",), "route": ("route.cu", "tma.cuh"),
+        "dispatch": ("quant.cu", "fp8.cuh", "tma.cuh") if fp8 else ("dispatch.cu", "tma.cuh"),
         "quantize": ("quant.cu", "fp8.cuh", "tma.cuh"),
         "combine": ("quant.cu", "fp8.cuh") if fp8c else ("combine.cu", "tma.cuh"),
         "combine_backward": ("backward.cu",), "gate_backward": ("backward.cu",),
