@@ -54,6 +54,13 @@ constexpr int kRouteWarps = kRouteThreads / 32;
 constexpr int kStageLoads = 8;      // logit loads in flight per thread while staging
 constexpr int kPrefixUnroll = 32;   // histogram loads in flight per thread in the prefix sums
 constexpr int kStageBytes = 68 * 1024;  // staging buffer: one round of 256 tokens up to 64 experts
+#ifndef MOE_ROUTE_MAX_LANES
+#define MOE_ROUTE_MAX_LANES 8   // lanes per token in the gate of a small tile
+#endif
+#ifndef MOE_ROUTE_INSERT_UNROLL
+#define MOE_ROUTE_INSERT_UNROLL 8  // unroll of the one-lane gate's insertion loop
+#endif
+constexpr int kInsertUnroll = MOE_ROUTE_INSERT_UNROLL;
 
 struct RouteArgs {
     const float *logits;
@@ -402,7 +409,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a)
                     }
                 }
             }
-#pragma unroll 8
+#pragma unroll (kInsertUnroll)
             for (int e = K; e < E; ++e) {
                 const float v = row[e];
                 finite &= isfinite(v);
@@ -698,6 +705,13 @@ cudaError_t launch_k(RouteArgs a, cudaStream_t s, int *too_large, bool dry_run)
         long long ntiles = ((long long)a.T + tt - 1) / tt;
         if (ntiles < 1) ntiles = 1;
         const size_t smem = route_smem((int)tt, K, (int)min((long long)rt, tt), a.E);
+        if (smem > 160 * 1024) {
+            // the tile's ids and ranks no longer fit beside the staging
+            // buffer: the separate gate and layout kernels take the batch
+            // (checked before any runtime call, so none fails)
+            *too_large = 1;
+            return cudaSuccess;
+        }
         cudaError_t err = allow_dynamic_smem(fn, (int)smem);
         if (err != cudaSuccess) return err;
         const int resident = resident_grid(fn, kRouteThreads, smem);
@@ -708,16 +722,11 @@ cudaError_t launch_k(RouteArgs a, cudaStream_t s, int *too_large, bool dry_run)
             // a small tile spreads each token over up to 8 lanes, so that
             // every thread of the block works on the gate
             int lanes = 1;
-            while (lanes < 8 && (long long)lanes * 2 * tt <= kRouteThreads && lanes * 2 <= a.E) lanes *= 2;
+            while (lanes < MOE_ROUTE_MAX_LANES && (long long)lanes * 2 * tt <= kRouteThreads && lanes * 2 <= a.E)
+                lanes *= 2;
             a.lanes = lanes;
             a.round_tokens = (int)min((long long)rt, min(tt, (long long)(kRouteThreads / lanes)));
             return launch_pdl(route_kernel<K, MODE>, dim3((unsigned)ntiles), dim3(kRouteThreads), smem, s, a);
-        }
-        if (smem > 160 * 1024) {
-            // the tile's ids and ranks no longer fit beside the staging
-            // buffer: the separate gate and layout kernels take the batch
-            *too_large = 1;
-            return cudaSuccess;
         }
         // fewer, larger tiles (several gate rounds per block).  On its own
         // such a batch is routed faster by the separate kernels (262144

@@ -139,3 +139,18 @@ def test_route_wait_expires_with_timeout_status():
     assert int(p.ws.view(torch.int32)[3].item()) == 0  # the hook was consumed
     for _ in range(3):
         route_checked(w, p, inp["logits"])
+
+
+def test_route_launches_query():
+    """moe_route_launches: 1 (the fused kernel) for the batches used here, 2
+    (gate and layout kernels) for a batch whose tiles cannot fit in shared
+    memory, 0 for unsupported sizes; the plan counts its launches with it.
+    Only the occupancy of the kernel is queried: nothing is launched."""
+    for name in ("tiny", "v2_top2", "fine_shared", "fp8_skewed", "prefill_cap"):
+        w = workloads.WORKLOADS[name]
+        assert abi.moe_route_launches(w.T, w.E, w.k, w.mode, w.P) == 1, name
+    assert abi.moe_route_launches(1 << 25, 256, 16, 0, 8) == 2
+    assert abi.moe_route_launches(100, 8, 9, 0, 4) == 0   # k > E for the gate
+    assert abi.moe_route_launches(100, 8, 2, 5, 4) == 0   # bad mode
+    p = _plan()
+    assert p.launches_per_step() == 3
