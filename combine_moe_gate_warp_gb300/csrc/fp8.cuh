@@ -8,6 +8,7 @@
 #include <cuda_fp8.h>
 
 #include "common.cuh"
+#include "tma.cuh"
 
 namespace moe {
 
@@ -49,7 +50,12 @@ __device__ __forceinline__ unsigned short e4m3x2(float lo, float hi)
 // fallback when the rounding is in doubt.  The arithmetic runs on packed
 // fp32 pairs (__fadd2_rn / __fmul2_rn), the test over 8 values at once,
 // and the fallback recomputes all 8 (a branch too long to be if-converted:
-// free when no lane needs it).  rcp = 0 forces the fallback.
+// free when no lane needs it).  rcp = 0 forces the fallback.  The inputs
+// are read from shared memory, and the fallback reads them again instead of
+// keeping them: held across the conversions for a branch that is rarely
+// taken (~1.5 % of 8-value groups of N(0,1) rows, where a quotient lands
+// exactly on an e4m3 rounding midpoint), they cost the encode kernel 15
+// registers and ~2.7 instructions per element.
 
 // 1 / scale for the fast quotient, or 0 (always fall back) where the
 // reciprocal would leave the normal range.
@@ -58,10 +64,11 @@ __device__ __forceinline__ float e4m3_rcp(float scale)
     return scale >= 1e-30f ? __frcp_rn(scale) : 0.0f;
 }
 
-// 8 bf16 (one 16-byte vector) -> 8 codes (two words), code i from element
-// i (low bytes first).
-__device__ __forceinline__ uint2 quant8(const uint4 &a, float zero, float scale, float rcp)
+// 8 bf16 (one 16-byte vector in shared memory, unchanged during the call)
+// -> 8 codes (two words), code i from element i (low bytes first).
+__device__ __forceinline__ uint2 quant8(const unsigned char *src, float zero, float scale, float rcp)
 {
+    const uint4 a = lds_v4(src);
     const unsigned w[4] = {a.x, a.y, a.z, a.w};
     const float2 nz = make_float2(-zero, -zero), r2 = make_float2(rcp, rcp);
     const float2 dn = make_float2(1.0f - 0x1p-20f, 1.0f - 0x1p-20f), up = make_float2(1.0f + 0x1p-20f, 1.0f + 0x1p-20f);
@@ -76,11 +83,13 @@ __device__ __forceinline__ uint2 quant8(const uint4 &a, float zero, float scale,
         hi[i] = (unsigned)e4m3x2(h0.x, h0.y) | ((unsigned)e4m3x2(h1.x, h1.y) << 16);
     }
     if (__builtin_expect((lo[0] != hi[0]) | (lo[1] != hi[1]) | (rcp == 0.0f), 0)) {
+        const uint4 b = lds_v4(src);  // read again (a volatile load: not forwarded from `a`)
+        const unsigned v[4] = {b.x, b.y, b.z, b.w};
         float q[8];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            q[2 * i] = __fdiv_rn(__fsub_rn(bf16lo(w[i]), zero), scale);
-            q[2 * i + 1] = __fdiv_rn(__fsub_rn(bf16hi(w[i]), zero), scale);
+            q[2 * i] = __fdiv_rn(__fsub_rn(bf16lo(v[i]), zero), scale);
+            q[2 * i + 1] = __fdiv_rn(__fsub_rn(bf16hi(v[i]), zero), scale);
         }
         lo[0] = (unsigned)e4m3x2(q[0], q[1]) | ((unsigned)e4m3x2(q[2], q[3]) << 16);
         lo[1] = (unsigned)e4m3x2(q[4], q[5]) | ((unsigned)e4m3x2(q[6], q[7]) << 16);
@@ -88,10 +97,10 @@ __device__ __forceinline__ uint2 quant8(const uint4 &a, float zero, float scale,
     return make_uint2(lo[0], lo[1]);
 }
 
-// 16 bf16 (two 16-byte vectors) -> 16 codes (one 16-byte vector).
-__device__ __forceinline__ uint4 quant16(const uint4 &a, const uint4 &b, float zero, float scale, float rcp)
+// 16 bf16 (32 bytes in shared memory) -> 16 codes (one 16-byte vector).
+__device__ __forceinline__ uint4 quant16(const unsigned char *src, float zero, float scale, float rcp)
 {
-    const uint2 l = quant8(a, zero, scale, rcp), h = quant8(b, zero, scale, rcp);
+    const uint2 l = quant8(src, zero, scale, rcp), h = quant8(src + 16, zero, scale, rcp);
     return make_uint4(l.x, l.y, h.x, h.y);
 }
 

@@ -322,7 +322,7 @@ fp8_encode_kernel(EncArgs a)
                 for (int q = lane; q < a.npairs; q += 32) {
                     const uint4 c = par.x == 0.0f
                                         ? make_uint4(0u, 0u, 0u, 0u)
-                                        : quant16(lds_v4(row + 32 * q), lds_v4(row + 32 * q + 16), par.y, par.x, rcp);
+                                        : quant16(row + 32 * q, par.y, par.x, rcp);
 #pragma unroll
                     for (int j = 0; j < MOE_MAX_TOPK; ++j) {
                         if (j >= nr) break;
