@@ -80,6 +80,7 @@ combine_bwd_kernel(const uint4 *__restrict__ dy, const uint4 *__restrict__ eo, c
 {
     pdl_wait();
     pdl_launch_dependents();
+    const uint64_t pol = l2_stream_policy(false);
     const int lane = threadIdx.x & 31;
     const long long nwarps = (long long)gridDim.x * (kBwdThreads / 32);
     const int rows_valid = min(r_max, __ldg(R_ptr));
@@ -112,7 +113,7 @@ combine_bwd_kernel(const uint4 *__restrict__ dy, const uint4 *__restrict__ eo, c
 #pragma unroll
             for (int u = 0; u < V; ++u) {
                 const int c = c0 + 32 * u;
-                d[u] = c < nvec ? ld_stream_v4(dyrow + c) : make_uint4(0, 0, 0, 0);
+                d[u] = c < nvec ? ld_stream_v4(dyrow + c, pol) : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
             for (int j = 0; j < K; ++j) {
@@ -120,7 +121,7 @@ combine_bwd_kernel(const uint4 *__restrict__ dy, const uint4 *__restrict__ eo, c
 #pragma unroll
                 for (int u = 0; u < V; ++u) {
                     const int c = c0 + 32 * u;
-                    e[j][u] = c < nvec ? ld_stream_v4(src + c) : make_uint4(0, 0, 0, 0);
+                    e[j][u] = c < nvec ? ld_stream_v4(src + c, pol) : make_uint4(0, 0, 0, 0);
                 }
             }
 #pragma unroll
@@ -130,7 +131,7 @@ combine_bwd_kernel(const uint4 *__restrict__ dy, const uint4 *__restrict__ eo, c
 #pragma unroll
                 for (int u = 0; u < V; ++u) {
                     const int c = c0 + 32 * u;
-                    if (c < nvec) st_v4(dst + c, scale_row_vec(g[j], d[u]));
+                    if (c < nvec) st_stream_v4(dst + c, scale_row_vec(g[j], d[u]), pol);
                 }
             }
             // per vector: its 8 products summed from 0, then added to the slot's sum

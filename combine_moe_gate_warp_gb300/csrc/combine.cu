@@ -118,15 +118,21 @@ __device__ __forceinline__ bool wait_stage(uint64_t *bar, uint32_t parity)
     return true;
 }
 
-// PSLEEP: the producer sleeps (suspend hint) instead of polling while it
-// waits for ring space.  Chosen per launch from the consumer mode: with all
-// four consumer warps on one large unit (many slots per token) a polling
-// producer competes with them for issue slots (262144 tokens x 4096, top-8
-// with capacity drops: 1520 -> 1463 us on GB300); with one warp per small
-// unit the producer must react at once (65536 x 4096, top-2: 231 -> 243 us
-// when it sleeps).  A runtime switch inside the wait loop cost more than
-// either, so it is a template parameter.
-template <int K, bool PSLEEP>
+// WIDE: all four consumer warps share each (large) unit, chosen per launch
+// from the unit size.  Two choices follow it, both measured on GB300:
+//  * the producer sleeps (suspend hint) instead of polling while it waits
+//    for ring space.  With four warps on one large unit (many slots per
+//    token) a polling producer competes with them for issue slots (262144
+//    tokens x 4096, top-8 with capacity drops: 1520 -> 1463 us); with one
+//    warp per small unit the producer must react at once (65536 x 4096,
+//    top-2: 231 -> 243 us when it sleeps).  A runtime switch inside the
+//    wait loop cost more than either, so it is a template parameter;
+//  * the rows are read and y is written with the evict-first L2 policy
+//    (8192 x 2048, top-8 + 2 shared experts: the batch 118 -> 111 us;
+//    the top-8 prefill batch 2886 -> 2861 us), which slows the one-warp
+//    mode (65536 x 4096, top-2: 230 -> 238 us), so that mode keeps the
+//    normal policy.
+template <int K, bool WIDE>
 __global__ void __launch_bounds__(kCombThreads + 32) combine_tma_kernel(CombineArgs a)
 {
     extern __shared__ __align__(128) unsigned char s_ring[];  // byte ring of a.ring_bytes
@@ -152,6 +158,7 @@ __global__ void __launch_bounds__(kCombThreads + 32) combine_tma_kernel(CombineA
     __syncthreads();
     pdl_wait();
     pdl_launch_dependents();
+    const uint64_t pol = l2_stream_policy(WIDE);
 
     if (warp == 0) {
         // ---- producer warp ----------------------------------------------
@@ -168,7 +175,7 @@ __global__ void __launch_bounds__(kCombThreads + 32) combine_tma_kernel(CombineA
             const int d = (int)(oldest % kDesc);
             const uint32_t par = (uint32_t)((oldest / kDesc) & 1);
             auto probe = [&]() {
-                if constexpr (PSLEEP) return mbar_try_wait_sleep(&s_empty[d], par);
+                if constexpr (WIDE) return mbar_try_wait_sleep(&s_empty[d], par);
                 else return mbar_try_wait(&s_empty[d], par);
             };
             bool ok = probe();
@@ -245,12 +252,12 @@ __global__ void __launch_bounds__(kCombThreads + 32) combine_tma_kernel(CombineA
 #pragma unroll
                         for (int j = 0; j < K; ++j) {
                             if (rb[j] >= 0) {
-                                bulk_load(dst, a.eo + (long long)rb[j] * a.rowbytes + col0, bytes, &s_full[d]);
+                                bulk_load(dst, a.eo + (long long)rb[j] * a.rowbytes + col0, bytes, &s_full[d], pol);
                                 dst += bytes;
                             }
                         }
                         for (int q = 0; q < a.Ks; ++q) {
-                            bulk_load(dst, a.shared + ((long long)q * a.T + t) * a.rowbytes + col0, bytes, &s_full[d]);
+                            bulk_load(dst, a.shared + ((long long)q * a.T + t) * a.rowbytes + col0, bytes, &s_full[d], pol);
                             dst += bytes;
                         }
                     } else {
@@ -309,22 +316,22 @@ __global__ void __launch_bounds__(kCombThreads + 32) combine_tma_kernel(CombineA
             o.y = pack_bf16x2(acc[2], acc[3]);
             o.z = pack_bf16x2(acc[4], acc[5]);
             o.w = pack_bf16x2(acc[6], acc[7]);
-            st_v4(yrow + v, o);
+            st_stream_v4(yrow + v, o, pol);
         }
         mbar_arrive(&s_empty[d]);
     }
 }
 
-template <int K, bool PSLEEP>
+template <int K, bool WIDE>
 cudaError_t launch_kp(const CombineArgs &a, cudaStream_t s)
 {
-    const void *fn = reinterpret_cast<const void *>(combine_tma_kernel<K, PSLEEP>);
+    const void *fn = reinterpret_cast<const void *>(combine_tma_kernel<K, WIDE>);
     const size_t smem = (size_t)a.ring_bytes;
     cudaError_t err = allow_dynamic_smem(fn, (int)smem);
     if (err != cudaSuccess) return err;
     const long long resident = resident_grid(fn, kCombThreads + 32, smem);
     const unsigned grid = (unsigned)(a.units < resident ? a.units : resident);
-    return launch_pdl(combine_tma_kernel<K, PSLEEP>, dim3(grid), dim3(kCombThreads + 32), smem, s, a);
+    return launch_pdl(combine_tma_kernel<K, WIDE>, dim3(grid), dim3(kCombThreads + 32), smem, s, a);
 }
 
 template <int K>

@@ -124,21 +124,96 @@ __device__ __forceinline__ void record_status(void *ws, unsigned code)
     if (ws) atomicCAS(&static_cast<WsHeader *>(ws)->status, 0u, code);
 }
 
-// Streaming 16-byte load (read once: do not keep in L1).
-__device__ __forceinline__ uint4 ld_stream_v4(const uint4 *p)
+// Rows that a call reads or writes once (token rows, packed rows, expert
+// outputs, y, FP8 codes) may go through L2 with an evict-first policy, so
+// that what the next calls reuse -- their code, the router logits, the
+// routing metadata and the workspace, a few MB -- stays in L2 while hundreds
+// of MB of rows stream through it.  Each kernel picks evict-first or the
+// normal policy by what was measured for it, and creates the policy once
+// per thread.
+#ifndef MOE_L2_STREAM_HINT
+#define MOE_L2_STREAM_HINT 1
+#endif
+__device__ __forceinline__ uint64_t l2_stream_policy(bool evict_first)
+{
+    uint64_t pol = 0;
+#if MOE_L2_STREAM_HINT
+    if (evict_first) asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    else asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+#endif
+    return pol;
+}
+
+// Streaming 16-byte load (read once: not kept in L1, evicted first from L2).
+__device__ __forceinline__ uint4 ld_stream_v4(const uint4 *p, uint64_t pol)
 {
     uint4 v;
+#if MOE_L2_STREAM_HINT
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+#else
+    (void)pol;
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
+#endif
     return v;
 }
 
-__device__ __forceinline__ void st_v4(uint4 *p, const uint4 &v)
+// Streaming 16-byte store (written once: evicted first from L2).
+__device__ __forceinline__ void st_stream_v4(uint4 *p, const uint4 &v, uint64_t pol)
 {
+#if MOE_L2_STREAM_HINT == 1
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p), "r"(v.x),
+                 "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+                 : "memory");
+#else
+    (void)pol;
     asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                  "r"(v.w)
                  : "memory");
+#endif
+}
+
+// 32-byte vectors (sm_100 and later move 256 bits per load or store
+// instruction: half the load/store instructions of 16-byte vectors).  The
+// address must be 32-byte aligned.
+struct __align__(32) u32x8 {
+    uint4 lo, hi;
+};
+
+__device__ __forceinline__ u32x8 ld_stream_v8(const u32x8 *p, uint64_t pol)
+{
+    u32x8 v;
+#if MOE_L2_STREAM_HINT
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
+                 : "=r"(v.lo.x), "=r"(v.lo.y), "=r"(v.lo.z), "=r"(v.lo.w), "=r"(v.hi.x), "=r"(v.hi.y), "=r"(v.hi.z),
+                   "=r"(v.hi.w)
+                 : "l"(p), "l"(pol));
+#else
+    (void)pol;
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v.lo.x), "=r"(v.lo.y), "=r"(v.lo.z), "=r"(v.lo.w), "=r"(v.hi.x), "=r"(v.hi.y), "=r"(v.hi.z),
+                   "=r"(v.hi.w)
+                 : "l"(p));
+#endif
+    return v;
+}
+
+__device__ __forceinline__ void st_stream_v8(u32x8 *p, const u32x8 &v, uint64_t pol)
+{
+#if MOE_L2_STREAM_HINT == 1
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8}, %9;" ::"l"(p),
+                 "r"(v.lo.x), "r"(v.lo.y), "r"(v.lo.z), "r"(v.lo.w), "r"(v.hi.x), "r"(v.hi.y), "r"(v.hi.z),
+                 "r"(v.hi.w), "l"(pol)
+                 : "memory");
+#else
+    (void)pol;
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v.lo.x), "r"(v.lo.y),
+                 "r"(v.lo.z), "r"(v.lo.w), "r"(v.hi.x), "r"(v.hi.y), "r"(v.hi.z), "r"(v.hi.w)
+                 : "memory");
+#endif
 }
 
 // Programmatic dependent launch.  Every kernel of the path is launched so

@@ -80,6 +80,7 @@ fp8_group_stats_kernel(const uint4 *__restrict__ src, long long n_src, int nvec,
     const int ngroups = MODE == MOE_FP8_GLOBAL ? 1 : E;
     pdl_wait();
     pdl_launch_dependents();
+    const uint64_t pol = l2_stream_policy(false);  // measured: evict-first slows the FP8 paths
     for (int i = threadIdx.x; i <= E; i += kStatThreads) s_off[i] = __ldg(offsets + i);
     for (int i = threadIdx.x; i < ngroups; i += kStatThreads) s_max[i] = s_min[i] = 0u;
     __syncthreads();
@@ -106,7 +107,7 @@ fp8_group_stats_kernel(const uint4 *__restrict__ src, long long n_src, int nvec,
             uint4 v[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u)
-                if (c + 32 * u < nvec) v[u] = ld_stream_v4(row + c + 32 * u);
+                if (c + 32 * u < nvec) v[u] = ld_stream_v4(row + c + 32 * u, pol);
 #pragma unroll
             for (int u = 0; u < 4; ++u)
                 if (c + 32 * u < nvec) minmax8(v[u], kmax, kmin);
@@ -200,6 +201,7 @@ fp8_encode_kernel(EncArgs a)
     }
     pdl_wait();
     pdl_launch_dependents();
+    const uint64_t pol = l2_stream_policy(false);  // measured: evict-first slows the FP8 paths
     for (int i = tid; i <= a.E; i += blockDim.x) s_off[i] = __ldg(a.offsets + i);
     for (int g = tid; g < ngroups; g += blockDim.x) {
         const unsigned wmx = *((volatile unsigned *)&h->quant_max[g]);
@@ -226,7 +228,7 @@ fp8_encode_kernel(EncArgs a)
                 const long long r = blockIdx.x + i * stride;
                 mbar_arrive_expect_tx(&s_full[st], (uint32_t)a.rowbytes);
                 bulk_load(s_ring + (size_t)st * a.rowbytes, a.src + r * a.rowbytes, (uint32_t)a.rowbytes,
-                          &s_full[st]);
+                          &s_full[st], pol);
             }
             // never leave with copies still landing in shared memory: wait for
             // the last copy issued into each stage
@@ -326,7 +328,7 @@ fp8_encode_kernel(EncArgs a)
 #pragma unroll
                     for (int j = 0; j < MOE_MAX_TOPK; ++j) {
                         if (j >= nr) break;
-                        st_v4(a.out + (long long)run[j] * a.npairs + q, c);
+                        st_stream_v4(a.out + (long long)run[j] * a.npairs + q, c, pol);
                     }
                 }
                 if ((same >> lane) & 1u) a.scales[r] = par;
@@ -400,6 +402,7 @@ combine_fp8_kernel(const uint4 *__restrict__ codes, const float2 *__restrict__ s
 {
     pdl_wait();
     pdl_launch_dependents();
+    const uint64_t pol = l2_stream_policy(false);
     const int lane = threadIdx.x & 31;
     const long long nwarps = (long long)gridDim.x * (kCombFp8Threads / 32);
     const int rows_valid = min(r_max, __ldg(R_ptr));
@@ -440,7 +443,7 @@ combine_fp8_kernel(const uint4 *__restrict__ codes, const float2 *__restrict__ s
                     const uint4 *src = codes + (long long)row[j] * n16;
 #pragma unroll
                     for (int u = 0; u < V; ++u)
-                        if (c0 + 32 * u < n16) cv[j][u] = ld_stream_v4(src + c0 + 32 * u);
+                        if (c0 + 32 * u < n16) cv[j][u] = ld_stream_v4(src + c0 + 32 * u, pol);
                 }
             }
 #pragma unroll
@@ -455,7 +458,7 @@ combine_fp8_kernel(const uint4 *__restrict__ codes, const float2 *__restrict__ s
                     if (j < n) fma16_fp8(acc, g[j], sc[j], zr[j], cv[j][u]);
                 for (int s = 0; s < Ks; ++s) {
                     const uint4 *sh = shared + ((long long)s * T + t) * (2LL * n16) + 2 * c;
-                    const uint4 a = ld_stream_v4(sh), b = ld_stream_v4(sh + 1);
+                    const uint4 a = ld_stream_v4(sh, pol), b = ld_stream_v4(sh + 1, pol);
                     add8_bf16(acc, a);
                     add8_bf16(acc + 8, b);
                 }
@@ -469,8 +472,8 @@ combine_fp8_kernel(const uint4 *__restrict__ codes, const float2 *__restrict__ s
                 o1.z = pack2_bf16(acc[12], acc[13]);
                 o1.w = pack2_bf16(acc[14], acc[15]);
                 uint4 *yr = y + t * (2LL * n16) + 2 * c;
-                st_v4(yr, o0);
-                st_v4(yr + 1, o1);
+                st_stream_v4(yr, o0, pol);
+                st_stream_v4(yr + 1, o1, pol);
             }
         }
     }

@@ -73,14 +73,25 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
     return done != 0;
 }
 
-// global -> shared bulk copy, completion counted in bytes on `bar`.
-__device__ __forceinline__ void bulk_load(void *dst_smem, const void *src_gmem, uint32_t bytes, uint64_t *bar)
+// global -> shared bulk copy, completion counted in bytes on `bar`; `pol`
+// is the L2 policy of the source lines (l2_stream_policy for rows read once).
+__device__ __forceinline__ void bulk_load(void *dst_smem, const void *src_gmem, uint32_t bytes, uint64_t *bar,
+                                          uint64_t pol)
 {
+#if MOE_L2_STREAM_HINT
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(smem_addr(dst_smem)),
+        "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+        : "memory");
+#else
+    (void)pol;
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
             smem_addr(dst_smem)),
         "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar))
         : "memory");
+#endif
 }
 
 // Hint: start bringing `bytes` (a multiple of 16, 16-byte aligned, all

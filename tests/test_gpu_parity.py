@@ -350,3 +350,30 @@ def test_mixed_routing_calls_share_a_workspace():
         route_checked(wr, plan, inp["logits"])
         plan.dispatch(inp["x"])
         assert plan.status() == 0
+
+
+@pytest.mark.parametrize("H", [1024, 1032])
+@pytest.mark.parametrize("x_off,p_off", [(0, 0), (16, 0), (0, 16), (16, 16)])
+def test_dispatch_vector_widths(H, x_off, p_off):
+    """The bf16 dispatch moves 32-byte vectors where x, packed and the row
+    length (2H bytes) are 32-byte aligned, and 16-byte vectors otherwise:
+    both against the oracle, with base pointers 16 bytes past a 32-byte
+    boundary and a row of 2064 bytes."""
+    from combine_moe_gate_warp_gb300 import RoutePlan, abi
+    from gpu_util import shape_of
+    w = workloads.Workload("vec", T=777, H=H, E=8, k=3, P=4, seed=11)
+    plan = RoutePlan(shape_of(w), "cuda")
+    L = route_checked(w, plan, workloads.make_logits(w, "cuda"))
+    x0 = workloads.make_x(w, "cuda")
+    xb = torch.empty(w.T * H + 16, dtype=torch.bfloat16, device="cuda")
+    x = xb[x_off // 2: x_off // 2 + w.T * H].view(w.T, H)
+    x.copy_(x0)
+    pb = torch.full((plan.r_max * H + 16,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    packed = pb[p_off // 2: p_off // 2 + plan.r_max * H].view(plan.r_max, H)
+    assert x.data_ptr() % 32 == x_off and packed.data_ptr() % 32 == p_off
+    abi.moe_dispatch(x, w.T, H, plan.layout, 0, packed)
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    R = int(L["R"])
+    src_tok = L["src_pos"].astype(np.int64) // w.k
+    assert np.array_equal(bits(packed[:R]), bits(x0)[src_tok])
