@@ -164,7 +164,7 @@ __device__ __forceinline__ uint4 ld_stream_v4(const uint4 *p, uint64_t pol)
 // Streaming 16-byte store (written once: evicted first from L2).
 __device__ __forceinline__ void st_stream_v4(uint4 *p, const uint4 &v, uint64_t pol)
 {
-#if MOE_L2_STREAM_HINT == 1
+#if MOE_L2_STREAM_HINT
     asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p), "r"(v.x),
                  "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
                  : "memory");
@@ -203,7 +203,7 @@ __device__ __forceinline__ u32x8 ld_stream_v8(const u32x8 *p, uint64_t pol)
 
 __device__ __forceinline__ void st_stream_v8(u32x8 *p, const u32x8 &v, uint64_t pol)
 {
-#if MOE_L2_STREAM_HINT == 1
+#if MOE_L2_STREAM_HINT
     asm volatile("st.global.L1::no_allocate.L2::cache_hint.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8}, %9;" ::"l"(p),
                  "r"(v.lo.x), "r"(v.lo.y), "r"(v.lo.z), "r"(v.lo.w), "r"(v.hi.x), "r"(v.hi.y), "r"(v.hi.z),
                  "r"(v.hi.w), "l"(pol)

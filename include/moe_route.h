@@ -287,6 +287,9 @@ moe_status moe_dispatch_layout_reassign(const int32_t *topk_idx, const int32_t *
  *            Two kernels (extremes, then codes), which use the workspace L->ws
  *            and leave it clean.
  *   Rows >= R are not written.
+ *   x and packed must be 16-byte aligned; for fp8 = 0 with both 32-byte
+ *   aligned and H a multiple of 16, the copy moves 32-byte vectors (fewer
+ *   load/store instructions: faster for large k).
  */
 moe_status moe_dispatch(const void *x, int T, int H, const moe_layout *L, int fp8,
                         void *packed, float *scales, moe_stream_t stream);
