@@ -54,6 +54,9 @@ constexpr int kRouteWarps = kRouteThreads / 32;
 constexpr int kStageLoads = 8;      // logit loads in flight per thread while staging
 constexpr int kPrefixUnroll = 32;   // histogram loads in flight per thread in the prefix sums
 constexpr int kStageBytes = 68 * 1024;  // staging buffer: one round of 256 tokens up to 64 experts
+#ifndef MOE_ROUTE_BALANCE
+#define MOE_ROUTE_BALANCE 1  // large batches: tiles sized to the resident slots
+#endif
 #ifndef MOE_ROUTE_MAX_LANES
 #define MOE_ROUTE_MAX_LANES 8   // lanes per token in the gate of a small tile
 #endif
@@ -701,10 +704,11 @@ cudaError_t launch_k(RouteArgs a, cudaStream_t s, int *too_large, bool dry_run)
     if (tt > a.T) tt = a.T;
     tt = (tt + kRouteMinTileTokens - 1) / kRouteMinTileTokens * kRouteMinTileTokens;
     if (tt < kRouteMinTileTokens) tt = kRouteMinTileTokens;
+    bool grown = false;
     while (true) {
         long long ntiles = ((long long)a.T + tt - 1) / tt;
         if (ntiles < 1) ntiles = 1;
-        const size_t smem = route_smem((int)tt, K, (int)min((long long)rt, tt), a.E);
+        size_t smem = route_smem((int)tt, K, (int)min((long long)rt, tt), a.E);
         if (smem > 160 * 1024) {
             // the tile's ids and ranks no longer fit beside the staging
             // buffer: the separate gate and layout kernels take the batch
@@ -714,8 +718,28 @@ cudaError_t launch_k(RouteArgs a, cudaStream_t s, int *too_large, bool dry_run)
         }
         cudaError_t err = allow_dynamic_smem(fn, (int)smem);
         if (err != cudaSuccess) return err;
-        const int resident = resident_grid(fn, kRouteThreads, smem);
+        int resident = resident_grid(fn, kRouteThreads, smem);
         if (ntiles <= resident && ntiles <= kRouteMaxTiles) {
+            if (MOE_ROUTE_BALANCE && grown && resident <= kRouteMaxTiles) {
+                // the doubling overshoots (262144 tokens, top-8: 256 tiles
+                // of 1024 on 304 slots, so some SMs hold two tiles and
+                // others one, and the wait takes the slowest); tiles of
+                // ceil(T / resident) tokens fill every slot evenly.  They
+                // are no larger, so they fit as well.
+                const long long tb = ((a.T + resident - 1) / resident + kRouteMinTileTokens - 1) /
+                                     kRouteMinTileTokens * kRouteMinTileTokens;
+                if (tb < tt) {
+                    const size_t sb = route_smem((int)tb, K, (int)min((long long)rt, tb), a.E);
+                    const int rb = resident_grid(fn, kRouteThreads, sb);
+                    const long long nb = ((long long)a.T + tb - 1) / tb;
+                    if (nb <= rb) {
+                        tt = tb;
+                        ntiles = nb;
+                        smem = sb;
+                        resident = rb;
+                    }
+                }
+            }
             if (dry_run) return cudaSuccess;
             a.tile_tokens = (int)tt;
             a.ntiles = (int)ntiles;
@@ -734,6 +758,7 @@ cudaError_t launch_k(RouteArgs a, cudaStream_t s, int *too_large, bool dry_run)
         // previous batch's copies the fused kernel disturbs them less (per
         // pipelined batch 2836-2845 vs 2898 us), so it keeps the batch.
         tt += tt;
+        grown = true;
     }
 }
 
