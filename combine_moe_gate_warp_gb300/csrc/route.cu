@@ -54,6 +54,9 @@ constexpr int kRouteWarps = kRouteThreads / 32;
 constexpr int kStageLoads = 8;      // logit loads in flight per thread while staging
 constexpr int kPrefixUnroll = 32;   // histogram loads in flight per thread in the prefix sums
 constexpr int kStageBytes = 68 * 1024;  // staging buffer: one round of 256 tokens up to 64 experts
+#ifndef MOE_ROUTE_BUBBLE
+#define MOE_ROUTE_BUBBLE 1
+#endif
 #ifndef MOE_ROUTE_BALANCE
 #define MOE_ROUTE_BALANCE 1  // large batches: tiles sized to the resident slots
 #endif
@@ -102,6 +105,26 @@ __device__ __forceinline__ unsigned ld_volatile_u32(const unsigned *p)
 template <int K>
 __device__ __forceinline__ void topk_insert(float (&bv)[K], int (&bi)[K], float v, int e)
 {
+#if MOE_ROUTE_BUBBLE
+    // v enters at the bottom and rises while it beats its predecessor
+    // strictly (an equal logit stays below the earlier, lower id): one
+    // compare and four selects per place
+    if (v > bv[K - 1]) {
+        bv[K - 1] = v;
+        bi[K - 1] = e;
+#pragma unroll
+        for (int j = K - 1; j > 0; --j) {
+            const bool up = bv[j] > bv[j - 1];
+            const float hv = up ? bv[j] : bv[j - 1], lv = up ? bv[j - 1] : bv[j];
+            const int hx = up ? bi[j] : bi[j - 1], lx = up ? bi[j - 1] : bi[j];
+            bv[j - 1] = hv;
+            bv[j] = lv;
+            bi[j - 1] = hx;
+            bi[j] = lx;
+        }
+    }
+    return;
+#endif
     if (v > bv[K - 1]) {
         int pos = 0;
 #pragma unroll
