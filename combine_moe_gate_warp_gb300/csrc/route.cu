@@ -54,9 +54,6 @@ constexpr int kRouteWarps = kRouteThreads / 32;
 constexpr int kStageLoads = 8;      // logit loads in flight per thread while staging
 constexpr int kPrefixUnroll = 32;   // histogram loads in flight per thread in the prefix sums
 constexpr int kStageBytes = 68 * 1024;  // staging buffer: one round of 256 tokens up to 64 experts
-#ifndef MOE_ROUTE_BUBBLE
-#define MOE_ROUTE_BUBBLE 1
-#endif
 #ifndef MOE_ROUTE_BALANCE
 #define MOE_ROUTE_BALANCE 1  // large batches: tiles sized to the resident slots
 #endif
@@ -99,16 +96,16 @@ __device__ __forceinline__ unsigned ld_volatile_u32(const unsigned *p)
 
 // Insert (v, e) into the descending list bv/bi of length K if it beats the
 // last entry.  v goes after every entry >= v, so an equal value keeps the
-// lower expert id first (-0.0 == +0.0 is a tie); the position is a count of
-// independent compares and the shift independent selects, a short
-// dependency chain where a compare-and-swap pass would be K - 1 steps long.
+// lower expert id first (-0.0 == +0.0 is a tie): it enters at the bottom and
+// rises while it beats its predecessor strictly, one compare and four
+// selects per place.  This chain is K - 1 steps long; the alternative, a
+// position counted by independent compares and a shift by independent
+// selects, is shorter but takes ~60 % more instructions, and the gate of a
+// large batch (256 tokens per round, 8 warps a block) is bound by issue:
+// 262144 tokens, 64 experts, top-8: 110 -> 100 us on GB300.
 template <int K>
 __device__ __forceinline__ void topk_insert(float (&bv)[K], int (&bi)[K], float v, int e)
 {
-#if MOE_ROUTE_BUBBLE
-    // v enters at the bottom and rises while it beats its predecessor
-    // strictly (an equal logit stays below the earlier, lower id): one
-    // compare and four selects per place
     if (v > bv[K - 1]) {
         bv[K - 1] = v;
         bi[K - 1] = e;
@@ -121,23 +118,6 @@ __device__ __forceinline__ void topk_insert(float (&bv)[K], int (&bi)[K], float 
             bv[j] = lv;
             bi[j - 1] = hx;
             bi[j] = lx;
-        }
-    }
-    return;
-#endif
-    if (v > bv[K - 1]) {
-        int pos = 0;
-#pragma unroll
-        for (int j = 0; j < K - 1; ++j) pos += (bv[j] >= v) ? 1 : 0;
-#pragma unroll
-        for (int j = K - 1; j > 0; --j) {
-            // old bv[j - 1] is still in place: j - 1 is updated later
-            bv[j] = j > pos ? bv[j - 1] : (j == pos ? v : bv[j]);
-            bi[j] = j > pos ? bi[j - 1] : (j == pos ? e : bi[j]);
-        }
-        if (pos == 0) {
-            bv[0] = v;
-            bi[0] = e;
         }
     }
 }
