@@ -124,6 +124,23 @@ __device__ __forceinline__ long long unit_order(long long i, long long n, int in
     return !interleave ? i : ((i & 1) ? n - 1 - (i >> 1) : (i >> 1));
 }
 
+// Token of unit u.  The producer pays this per unit on its serial path,
+// where a 64-bit division costs more than the rest of the unit's
+// bookkeeping: in the four-warp mode rows of up to ~8 KiB are one unit each
+// (nch == 1: no division) and otherwise a 32-bit division serves where u
+// allows it (262144 x 4096, top-8 with capacity: 1387 -> 1363 us on GB300).
+// The one-warp mode keeps the plain division: there the faster producer
+// measured slower (65536 x 4096, top-2: 230 -> 242 us).
+template <bool FAST>
+__device__ __forceinline__ long long unit_token(long long u, int nch)
+{
+    if constexpr (FAST) {
+        if (nch == 1) return u;
+        if (u < (1LL << 32)) return (long long)((unsigned)u / (unsigned)nch);
+    }
+    return u / nch;
+}
+
 // Bounded wait on a stage barrier.  Returns false if the bound expired.
 __device__ __forceinline__ bool wait_stage(uint64_t *bar, uint32_t parity)
 {
@@ -207,7 +224,7 @@ __global__ void __launch_bounds__(kCombThreads + 32) combine_tma_kernel(CombineA
             int rows[K];
             float g[K];
             if (batch + lane < n_units) {
-                const long long t = (blockIdx.x + unit_order(batch + lane, n_units, a.interleave) * stride) / a.nch;
+                const long long t = unit_token<WIDE>(blockIdx.x + unit_order(batch + lane, n_units, a.interleave) * stride, a.nch);
 #pragma unroll
                 for (int j = 0; j < K; ++j) {
                     rows[j] = __ldg(a.dst_row + t * K + j);
@@ -225,7 +242,7 @@ __global__ void __launch_bounds__(kCombThreads + 32) combine_tma_kernel(CombineA
                 int ok = 1;
                 if (lane == 0) {
                     const long long u = blockIdx.x + unit_order(i, n_units, a.interleave) * stride;
-                    const long long t = u / a.nch;
+                    const long long t = unit_token<WIDE>(u, a.nch);
                     const int col0 = (int)(u - t * a.nch) * a.cb;
                     const int bytes = min(a.cb, a.rowbytes - col0);
                     int n = 0;
@@ -313,7 +330,7 @@ __global__ void __launch_bounds__(kCombThreads + 32) combine_tma_kernel(CombineA
             return;
         }
         const long long u = blockIdx.x + unit_order(i, n_units, a.interleave) * stride;
-        const long long t = u / a.nch;
+        const long long t = unit_token<WIDE>(u, a.nch);
         const int col0 = (int)(u - t * a.nch) * a.cb;
         const int bytes = min(a.cb, a.rowbytes - col0);
         const int nv = bytes >> 4;
