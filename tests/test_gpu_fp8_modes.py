@@ -96,3 +96,39 @@ def test_constant_groups_and_clean_workspace():
             assert not plan.packed[:R].any() and not plan.eo_codes[:R].any()
             assert torch.all(plan.scales[:R, 0] == 0) and torch.all(plan.scales[:R, 1] == 1.25)
             assert torch.all(plan.y[:w.T].float() == -0.5)
+
+
+@pytest.mark.parametrize("H,fp8c", [(1024, 1), (2048, 1), (1024, 2)])
+def test_expert_rows_split_between_two_warps(H, fp8c):
+    """Rows of expert outputs of 1024 columns or more are encoded by two
+    warps, each half of the columns, their extremes meeting in shared
+    memory.  Rows whose extremes sit in one half only, in the other, and
+    signed zeros as extremes (whose sign the ordered keys decide) must give
+    the oracle's codes and scales exactly."""
+    w = _edge(300, H, 8, 2, 4, 1, fp8c, seed=47)
+    plan = RoutePlan(shape_of(w), "cuda")
+    inp = workloads.make_inputs(w, "cuda")
+    L = route_checked(w, plan, inp["logits"])
+    plan.dispatch(inp["x"])
+    R = L["R"]
+    eo = workloads.make_expert_out(w, max(plan.r_max, 1), "cuda")
+    h = H // 2
+    eo[0] = 0.0
+    eo[0, ::3] = -0.0                      # max +0, min -0: both extremes zero
+    eo[1] = -0.0                           # constant -0
+    eo[2] = -eo[2].abs()
+    eo[2, h:] = -0.0                       # max -0, in the second half only
+    eo[3] = eo[3].abs()
+    eo[3, 5] = -0.0                        # min -0, in the first half only
+    eo[4] = eo[4] * 0.01
+    eo[4, H - 1] = 7.0                     # max in the second half,
+    eo[4, 0] = -3.0                        # min in the first
+    eo[5] = eo[5] * 0.01
+    eo[5, h + 1] = 5.0                     # both extremes in the second half
+    eo[5, H - 2] = -5.0
+    eo[6, :h] = 0.0                        # first half flat zero, second half random
+    plan.quantize_expert_out(eo)
+    plan.combine_fp8(None)
+    assert plan.status() == 0
+    check_combine(w, plan, L, eo, None, np.arange(w.T, dtype=np.int64))
+    assert R >= 7

@@ -377,3 +377,14 @@ def test_dispatch_vector_widths(H, x_off, p_off):
     R = int(L["R"])
     src_tok = L["src_pos"].astype(np.int64) // w.k
     assert np.array_equal(bits(packed[:R]), bits(x0)[src_tok])
+
+
+def test_route_large_batch_resized_tiles():
+    """A batch whose 64-token tiles outnumber the blocks the GPU holds at
+    once: moe_route doubles the tile until the grid fits, then resizes it to
+    ceil(T / resident slots) tokens so every SM holds as many tiles (here
+    several gate rounds per tile, the last one partial, and a ragged last
+    tile); top-8 of 64 with capacity drops, against the oracle in full."""
+    w = workloads.Workload("route_resized", T=120001, H=64, E=64, k=8, P=8, logit_std=1.5, zipf_bias=True,
+                           capacity_factor=1.25, seed=52)
+    _full_check(w, fused=True)
