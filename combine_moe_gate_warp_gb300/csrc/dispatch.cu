@@ -9,9 +9,11 @@
 // Design (sm_103a): scatter form -- each token's row is read from HBM
 // exactly once and written to each of its (<= k) kept packed rows, so the
 // traffic is the algorithmic minimum (x read once, packed written once).
-// One block per token; every thread moves a fixed set of 16-byte chunks
-// with all loads issued before the stores, giving ~U*16 bytes in flight
-// per thread.
+// One block per token; every thread moves a fixed set of 32-byte vectors
+// (16-byte where x, packed or the row length is not 32-byte aligned) with
+// all loads issued before the stores, giving ~U vectors in flight per
+// thread.  Rows are read and written with the evict-first L2 policy: they
+// are touched once, and what the next calls reuse stays in L2.
 #include <climits>
 
 #include "common.cuh"
