@@ -61,6 +61,9 @@ def parse_args():
                     help="do not time the back-to-back batches of RoutePipeline")
     ap.add_argument("--no-graph", action="store_true",
                     help="do not time the step captured as a CUDA graph (RouteGraph)")
+    ap.add_argument("--data-streams", type=int, choices=[0, 1, 2], default=0,
+                    help="streams the pipelined batches' dispatch and combine alternate over "
+                         "(0: time both and keep the faster)")
     ap.add_argument("--route-priority", choices=["high", "same"], default="high",
                     help="priority of the routing stream against the data stream")
     ap.add_argument("--dedup-steps", type=int, default=200,
@@ -608,9 +611,15 @@ def measure_workload(args, world, rank, dev, sampler, cpu_seconds):
     pipe = None
     t_pw0 = t_pw1 = None
     if not args.no_pipeline and RoutePipeline.overlaps(shape):
-        t_pw0 = time.time()
-        pipe = time_pipelined(w, shape, inputs, eo, dev, world, K, max(3, args.warmup), args.route_priority)
-        t_pw1 = time.time()
+        runs = []
+        for ds in ((1, 2) if args.data_streams == 0 else (args.data_streams,)):
+            t0 = time.time()
+            r = time_pipelined(w, shape, inputs, eo, dev, world, K, max(3, args.warmup), args.route_priority, ds)
+            r["data_streams"] = ds
+            runs.append((r, t0, time.time()))
+        pipe, t_pw0, t_pw1 = min(runs, key=lambda x: x[0]["ms_per_step"])
+        if len(runs) > 1:
+            pipe["data_streams_ms"] = {str(r["data_streams"]): r["ms_per_step"] for r, _, _ in runs}
     graph = None
     if not args.no_graph:
         t_gw0 = time.time()
@@ -666,7 +675,8 @@ def measure_workload(args, world, rank, dev, sampler, cpu_seconds):
     # end to end through the public API: pinned host inputs copied in, result copied out
     e2e = None
     if not args.no_e2e:
-        e2e = time_e2e(w, shape, plan, inputs, eo, dev, world, args.e2e_steps, pipe is not None, R)
+        e2e = time_e2e(w, shape, plan, inputs, eo, dev, world, args.e2e_steps, pipe is not None, R,
+                       pipe["data_streams"] if pipe else 1)
 
     dd = None
     if args.dedup_steps > 0 and 1 <= w.P <= 16:
@@ -775,7 +785,7 @@ def combine_ulp_stats(plan, w, eo, shared):
                    "on the GPU; allowance n * 2^-24 * sum|terms| with n = the number of terms"}
 
 
-def time_e2e(w, shape, plan, inputs, eo, dev, world, steps, pipelined, R):
+def time_e2e(w, shape, plan, inputs, eo, dev, world, steps, pipelined, R, data_streams=2):
     """The same metric end to end: every step copies its inputs (router
     logits, x, the R expert-output rows the batch produces, shared-expert
     outputs) from pinned host memory to the device and reads y, the aux loss
@@ -810,7 +820,7 @@ def time_e2e(w, shape, plan, inputs, eo, dev, world, steps, pipelined, R):
     K2 = max(1, steps)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if pipelined:
-        pipe = RoutePipeline(shape, dev)
+        pipe = RoutePipeline(shape, dev, data_streams=data_streams)
         bufs = [dev_buffers() for _ in pipe.plans]
         copy_stream = torch.cuda.Stream(dev)
         copied = [torch.cuda.Event() for _ in pipe.plans]
@@ -823,7 +833,7 @@ def time_e2e(w, shape, plan, inputs, eo, dev, world, steps, pipelined, R):
                 copy_in(bufs[d])
             copied[d].record(copy_stream)
             pipe.route_stream.wait_event(copied[d])
-            pipe.data_stream.wait_event(copied[d])
+            pipe.stream_for(i).wait_event(copied[d])
             p = pipe.plan_for(i)
             bd = bufs[d]
             pipe.step(bd["logits"], bd["x"], p.packed if bd["eo"] is None else bd["eo"], bd["shared"],
@@ -835,11 +845,10 @@ def time_e2e(w, shape, plan, inputs, eo, dev, world, steps, pipelined, R):
         barrier(world)
         torch.cuda.synchronize(dev)
         a.record(copy_stream)
-        pipe.route_stream.wait_event(a)
-        pipe.data_stream.wait_event(a)
+        pipe.wait_event(a)
         for _ in range(K2):
             one()
-        b.record(pipe.data_stream)
+        pipe.record(b)
         torch.cuda.synchronize(dev)
         st = pipe.status()
         path = ("pinned host -> device copies on a copy stream into each plan's input buffers, the C-ABI "
@@ -875,7 +884,11 @@ def time_e2e(w, shape, plan, inputs, eo, dev, world, steps, pipelined, R):
             "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / K2, "steps": K2, "path": path}
 
 
-def time_pipelined(w, shape, inputs, eo, dev, world, K, W, route_priority="high"):
+def pipe_streams(pipe) -> int:
+    return len(getattr(pipe, "data_streams", [pipe.data_stream]))
+
+
+def time_pipelined(w, shape, inputs, eo, dev, world, K, W, route_priority="high", data_streams=2):
     """K back-to-back batches through RoutePipeline: two plans and two input
     batches (the workload's seed and the next one) alternate, so every step
     routes a batch while the previous batch's dispatch and combine run."""
@@ -884,7 +897,7 @@ def time_pipelined(w, shape, inputs, eo, dev, world, K, W, route_priority="high"
     from combine_moe_gate_warp_gb300 import RoutePipeline, workloads
     w2 = workloads.Workload(**{**w.__dict__, "seed": w.seed + 1})
     inputs2 = workloads.make_inputs(w2, dev)
-    pipe = RoutePipeline(shape, dev, route_priority=route_priority)
+    pipe = RoutePipeline(shape, dev, route_priority=route_priority, data_streams=data_streams)
     eo2 = None if eo is None else workloads.make_expert_out(w2, max(pipe.plans[0].r_max, 1), dev)
     batches = [(inputs, eo), (inputs2, eo2)]
 
@@ -904,10 +917,10 @@ def time_pipelined(w, shape, inputs, eo, dev, world, K, W, route_priority="high"
     barrier(world)
     torch.cuda.synchronize(dev)
     start.record(pipe.data_stream)
-    pipe.route_stream.wait_event(start)
+    pipe.wait_event(start)
     for i in range(K):
         one(W + i)
-    stop.record(pipe.data_stream)
+    pipe.record(stop)
     torch.cuda.synchronize(dev)
     barrier(world)
     ms = max_over_ranks(start.elapsed_time(stop), world, dev) / K
@@ -916,7 +929,8 @@ def time_pipelined(w, shape, inputs, eo, dev, world, K, W, route_priority="high"
         raise RuntimeError(f"device status {st} during the pipelined steps")
     return {"ms_per_step": ms,
             "note": "back-to-back batches (two alternating input batches and plans): gate + layout of "
-                    "batch i on a high-priority stream overlap dispatch + combine of batch i-1"}
+                    "batch i on a high-priority stream overlap dispatch + combine of batch i-1; the data "
+                    "calls of consecutive batches on %d alternating streams" % pipe_streams(pipe)}
 
 
 def time_graph(w, shape, inputs, eo, dev, world, K, W):

@@ -314,26 +314,32 @@ class RoutePipeline:
 
     Two plans alternate between batches.  The gate and the layout of batch i
     run on a high-priority routing stream while dispatch and combine of
-    batch i-1 run on the data stream: the first two are short chains of
+    batch i-1 run on a data stream: the first two are short chains of
     dependent round trips that leave HBM idle, the last two stream HBM.
     Batch i's dispatch waits for its layout (an event); batch i's gate waits
     until batch i-2, the last user of the same plan, has finished its
-    combine.  Each call is still one C-ABI call; nothing is skipped or
-    reordered within a batch.
+    combine.  With two data streams (the default) consecutive batches' data
+    calls go to alternate streams, so batch i's dispatch, which needs only
+    its own layout, may start while batch i-1's combine still runs instead of
+    after it (the two are independent).  Each call is still one C-ABI call;
+    nothing is skipped or reordered within a batch.
     """
 
-    def __init__(self, shape: RouteShape, device="cuda", depth: int = 2, route_priority: str = "high"):
+    def __init__(self, shape: RouteShape, device="cuda", depth: int = 2, route_priority: str = "high",
+                 data_streams: int = 2):
         self.device = torch.device(device)
         lo, hi = torch.cuda.Stream.priority_range()
-        self.data_stream = torch.cuda.Stream(self.device, priority=lo)
+        n = max(1, min(int(data_streams), depth))
+        self.data_streams = [torch.cuda.Stream(self.device, priority=lo) for _ in range(n)]
+        self.data_stream = self.data_streams[0]
         self.route_stream = torch.cuda.Stream(self.device, priority=hi if route_priority == "high" else lo)
-        self.plans = [RoutePlan(shape, self.device, stream=self.data_stream, route_stream=self.route_stream)
-                      for _ in range(depth)]
+        self.plans = [RoutePlan(shape, self.device, stream=self.data_streams[d % n], route_stream=self.route_stream)
+                      for d in range(depth)]
         self._routed = [torch.cuda.Event() for _ in range(depth)]
         self._done = [torch.cuda.Event() for _ in range(depth)]
         self.step_index = 0
-        for ev in self._done:
-            ev.record(self.data_stream)
+        for d, ev in enumerate(self._done):
+            ev.record(self.plans[d].stream)
 
     @staticmethod
     def overlaps(shape: RouteShape) -> bool:
@@ -348,6 +354,23 @@ class RoutePipeline:
 
     def plan_for(self, i: int) -> RoutePlan:
         return self.plans[i % len(self.plans)]
+
+    def stream_for(self, i: int) -> torch.cuda.Stream:
+        """The data stream of step i's dispatch and combine."""
+        return self.plan_for(i).stream
+
+    def wait_event(self, ev: torch.cuda.Event):
+        """Make every stream of the pipeline wait for `ev`."""
+        self.route_stream.wait_event(ev)
+        for st in self.data_streams:
+            st.wait_event(ev)
+
+    def record(self, ev: torch.cuda.Event):
+        """Record `ev` once the work enqueued so far on every data stream is
+        done (the first data stream waits for the others)."""
+        for st in self.data_streams[1:]:
+            self.data_stream.wait_stream(st)
+        ev.record(self.data_stream)
 
     def step(self, logits, x, expert_out, shared_out=None, out=None, stats_out=None) -> RoutePlan:
         """Enqueue one batch; returns the plan whose buffers (y, layout,
@@ -364,7 +387,7 @@ class RoutePipeline:
         self.route_stream.wait_event(self._done[d])
         p.route(logits)
         self._routed[d].record(self.route_stream)
-        self.data_stream.wait_event(self._routed[d])
+        p.stream.wait_event(self._routed[d])
         p.dispatch(x)
         if p.shape.fp8_combine:
             p.quantize_expert_out(expert_out)
@@ -372,13 +395,13 @@ class RoutePipeline:
         else:
             p.combine(expert_out, shared_out)
         if out is not None or stats_out is not None:
-            with torch.cuda.stream(self.data_stream):
+            with torch.cuda.stream(p.stream):
                 if out is not None:
                     out.copy_(p.y[:p.shape.T], non_blocking=True)
                 if stats_out is not None:
                     stats_out[0:1].copy_(p.aux_loss, non_blocking=True)
                     stats_out[1:2].copy_(p.entropy, non_blocking=True)
-        self._done[d].record(self.data_stream)
+        self._done[d].record(p.stream)
         return p
 
     def release_event(self, i: int) -> torch.cuda.Event:
@@ -389,7 +412,8 @@ class RoutePipeline:
 
     def synchronize(self):
         self.route_stream.synchronize()
-        self.data_stream.synchronize()
+        for st in self.data_streams:
+            st.synchronize()
 
     def status(self) -> int:
         """Synchronise and return the first non-zero device status of the plans."""
