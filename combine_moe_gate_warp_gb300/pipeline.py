@@ -343,14 +343,15 @@ class RoutePipeline:
 
     @staticmethod
     def overlaps(shape: RouteShape) -> bool:
-        """Whether back-to-back batches gain from the overlap.  The bf16 copy
-        kernels leave SM room for the short routing kernels; the FP8 encode
-        kernels are persistent and fill every SM (shared-memory rings), so
-        there the routing of the next batch only delays the next data kernel
-        (measured on GB300: bf16 workloads 10-17 % faster per batch, FP8
-        workloads equal or slower) and the calls are best issued in order
-        on one stream (RoutePlan.step)."""
-        return not (shape.fp8 or shape.fp8_combine)
+        """Whether back-to-back batches gain from the overlap: every shape the
+        path takes.  Measured on GB300: the bf16 workloads run 5-17 % faster
+        per batch than on one stream; the FP8 ones, whose encode kernels are
+        persistent and fill every SM, gained nothing while the data calls of
+        all batches shared one stream, and gain with two alternating data
+        streams, where one batch's encode overlaps the previous batch's
+        combine (65536 x 4096, top-2, e4m3 dispatch: 422 -> 403 us; FP8 both
+        ways: 660 -> 633 us)."""
+        return True
 
     def plan_for(self, i: int) -> RoutePlan:
         return self.plans[i % len(self.plans)]
