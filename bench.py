@@ -62,8 +62,8 @@ def parse_args():
     ap.add_argument("--no-graph", action="store_true",
                     help="do not time the step captured as a CUDA graph (RouteGraph)")
     ap.add_argument("--data-streams", type=int, choices=[0, 1, 2], default=0,
-                    help="streams the pipelined batches' dispatch and combine alternate over "
-                         "(0: time both and keep the faster)")
+                    help="streams the pipelined batches' dispatch and combine alternate over, with two "
+                         "plans (0: time the configurations of PIPE_CONFIGS and keep the fastest)")
     ap.add_argument("--route-priority", choices=["high", "same"], default="high",
                     help="priority of the routing stream against the data stream")
     ap.add_argument("--dedup-steps", type=int, default=200,
@@ -612,14 +612,18 @@ def measure_workload(args, world, rank, dev, sampler, cpu_seconds):
     t_pw0 = t_pw1 = None
     if not args.no_pipeline and RoutePipeline.overlaps(shape):
         runs = []
-        for ds in ((1, 2) if args.data_streams == 0 else (args.data_streams,)):
+        configs = PIPE_CONFIGS if args.data_streams == 0 else ((2, args.data_streams),)
+        for depth, ds in configs:
             t0 = time.time()
-            r = time_pipelined(w, shape, inputs, eo, dev, world, K, max(3, args.warmup), args.route_priority, ds)
-            r["data_streams"] = ds
+            r = time_pipelined(w, shape, inputs, eo, dev, world, K, max(3, args.warmup), args.route_priority, ds,
+                               depth)
+            r["depth"], r["data_streams"] = depth, ds
             runs.append((r, t0, time.time()))
+            torch.cuda.empty_cache()
         pipe, t_pw0, t_pw1 = min(runs, key=lambda x: x[0]["ms_per_step"])
         if len(runs) > 1:
-            pipe["data_streams_ms"] = {str(r["data_streams"]): r["ms_per_step"] for r, _, _ in runs}
+            pipe["configs_ms"] = {f"plans {r['depth']}, data streams {r['data_streams']}": r["ms_per_step"]
+                                  for r, _, _ in runs}
     graph = None
     if not args.no_graph:
         t_gw0 = time.time()
@@ -676,7 +680,7 @@ def measure_workload(args, world, rank, dev, sampler, cpu_seconds):
     e2e = None
     if not args.no_e2e:
         e2e = time_e2e(w, shape, plan, inputs, eo, dev, world, args.e2e_steps, pipe is not None, R,
-                       pipe["data_streams"] if pipe else 1)
+                       pipe["data_streams"] if pipe else 1, pipe["depth"] if pipe else 2)
 
     dd = None
     if args.dedup_steps > 0 and 1 <= w.P <= 16:
@@ -785,7 +789,7 @@ def combine_ulp_stats(plan, w, eo, shared):
                    "on the GPU; allowance n * 2^-24 * sum|terms| with n = the number of terms"}
 
 
-def time_e2e(w, shape, plan, inputs, eo, dev, world, steps, pipelined, R, data_streams=2):
+def time_e2e(w, shape, plan, inputs, eo, dev, world, steps, pipelined, R, data_streams=2, depth=2):
     """The same metric end to end: every step copies its inputs (router
     logits, x, the R expert-output rows the batch produces, shared-expert
     outputs) from pinned host memory to the device and reads y, the aux loss
@@ -820,7 +824,7 @@ def time_e2e(w, shape, plan, inputs, eo, dev, world, steps, pipelined, R, data_s
     K2 = max(1, steps)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if pipelined:
-        pipe = RoutePipeline(shape, dev, data_streams=data_streams)
+        pipe = RoutePipeline(shape, dev, depth=depth, data_streams=data_streams)
         bufs = [dev_buffers() for _ in pipe.plans]
         copy_stream = torch.cuda.Stream(dev)
         copied = [torch.cuda.Event() for _ in pipe.plans]
@@ -888,7 +892,12 @@ def pipe_streams(pipe) -> int:
     return len(getattr(pipe, "data_streams", [pipe.data_stream]))
 
 
-def time_pipelined(w, shape, inputs, eo, dev, world, K, W, route_priority="high", data_streams=2):
+# RoutePipeline configurations the bench times (plans, data streams); the
+# fastest is the pipelined figure
+PIPE_CONFIGS = ((2, 1), (2, 2), (3, 3))
+
+
+def time_pipelined(w, shape, inputs, eo, dev, world, K, W, route_priority="high", data_streams=2, depth=2):
     """K back-to-back batches through RoutePipeline: two plans and two input
     batches (the workload's seed and the next one) alternate, so every step
     routes a batch while the previous batch's dispatch and combine run."""
@@ -897,7 +906,7 @@ def time_pipelined(w, shape, inputs, eo, dev, world, K, W, route_priority="high"
     from combine_moe_gate_warp_gb300 import RoutePipeline, workloads
     w2 = workloads.Workload(**{**w.__dict__, "seed": w.seed + 1})
     inputs2 = workloads.make_inputs(w2, dev)
-    pipe = RoutePipeline(shape, dev, route_priority=route_priority, data_streams=data_streams)
+    pipe = RoutePipeline(shape, dev, depth=depth, route_priority=route_priority, data_streams=data_streams)
     eo2 = None if eo is None else workloads.make_expert_out(w2, max(pipe.plans[0].r_max, 1), dev)
     batches = [(inputs, eo), (inputs2, eo2)]
 
@@ -928,9 +937,9 @@ def time_pipelined(w, shape, inputs, eo, dev, world, K, W, route_priority="high"
     if st != 0:
         raise RuntimeError(f"device status {st} during the pipelined steps")
     return {"ms_per_step": ms,
-            "note": "back-to-back batches (two alternating input batches and plans): gate + layout of "
-                    "batch i on a high-priority stream overlap dispatch + combine of batch i-1; the data "
-                    "calls of consecutive batches on %d alternating streams" % pipe_streams(pipe)}
+            "note": "back-to-back batches (two alternating input batches, %d plans): the routing of batch "
+                    "i on a high-priority stream overlaps the data calls of the batches before it; the data "
+                    "calls of consecutive batches on %d alternating streams" % (len(pipe.plans), pipe_streams(pipe))}
 
 
 def time_graph(w, shape, inputs, eo, dev, world, K, W):
