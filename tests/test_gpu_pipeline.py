@@ -77,3 +77,29 @@ def test_pipeline_depth3_host_outputs():
         assert np.array_equal(bits(ys[i]), bits(ref.y[:w.T])), f"step {i}: y differs"
         og = oracle.gate(inp["logits"].cpu().numpy(), w.k, w.mode)
         assert abs(stats[i][0].item() - og[3]) <= 1e-9 and abs(stats[i][1].item() - og[4]) <= 1e-6
+
+
+@pytest.mark.parametrize("depth,streams", [(2, 1), (3, 3)])
+@pytest.mark.parametrize("w", [W["v2_top2"].scaled(1200), W["fp8_both"].scaled(700)], ids=lambda w: w.name)
+def test_pipeline_plans_and_data_streams(w, depth, streams):
+    """Other pipeline shapes: two plans with every data call on one stream,
+    and three plans each with its own data stream (three batches' calls in
+    flight at once) give the serial calls' bits."""
+    batches = []
+    for b in range(4):
+        wb = workloads.Workload(**{**w.__dict__, "seed": w.seed + 13 * b})
+        batches.append((workloads.make_inputs(wb, "cuda"), workloads.make_expert_out(wb, max(wb.r_max, 1), "cuda")))
+    torch.cuda.synchronize()
+    pipe = RoutePipeline(shape_of(w), "cuda", depth=depth, data_streams=streams)
+    assert len(pipe.data_streams) == streams
+    outs = [torch.empty((w.T, w.H), dtype=torch.bfloat16, device="cuda") for _ in range(8)]
+    for i in range(8):
+        inp, eo = batches[i % 4]
+        pipe.step(inp["logits"], inp["x"], eo, inp["shared"], out=outs[i])
+    assert pipe.status() == 0
+    for i in range(8):
+        inp, eo = batches[i % 4]
+        ref = RoutePlan(shape_of(w), "cuda")
+        ref.step(inp["logits"], inp["x"], eo, inp["shared"])
+        assert ref.status() == 0
+        assert np.array_equal(bits(outs[i]), bits(ref.y[:w.T])), f"step {i}: y differs from the serial calls"
