@@ -388,3 +388,11 @@ def test_route_large_batch_resized_tiles():
     w = workloads.Workload("route_resized", T=120001, H=64, E=64, k=8, P=8, logit_std=1.5, zipf_bias=True,
                            capacity_factor=1.25, seed=52)
     _full_check(w, fused=True)
+
+
+def test_route_large_batch_many_experts():
+    """256 experts (staging rounds of 64 tokens) in a batch whose tiles are
+    grown and resized: several gate rounds per tile, the softmax over all
+    experts, against the oracle in full."""
+    w = workloads.Workload("route_e256", T=100003, H=16, E=256, k=8, P=8, mode=workloads.SOFTMAX_TOPK, seed=53)
+    _full_check(w, fused=True)
