@@ -396,3 +396,13 @@ def test_route_large_batch_many_experts():
     experts, against the oracle in full."""
     w = workloads.Workload("route_e256", T=100003, H=16, E=256, k=8, P=8, mode=workloads.SOFTMAX_TOPK, seed=53)
     _full_check(w, fused=True)
+
+
+def test_combine_column_chunks_with_capacity():
+    """Rows too long for one ring unit at top-8 (14 KiB: two column chunks
+    per row, so units = 2 T and the unit's token a 32-bit division) under a
+    capacity (units from both ends of each block's share): every output
+    against the oracle."""
+    w = workloads.Workload("chunks_cap", T=2001, H=7168, E=16, k=8, P=4, logit_std=1.5, zipf_bias=True,
+                           capacity_factor=1.25, seed=54)
+    _full_check(w, fused=True)
